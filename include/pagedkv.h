@@ -1,0 +1,203 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so, the GB300 (sm_103a) hot path of a
+ * paged KV cache: slot mapping, the cache write, and paged attention over a
+ * block-table-indexed pool for one mixed continuous-batching step.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers named as device buffers are CUDA device pointers on the current
+ *   device, owned by the caller. The library never allocates, frees or keeps
+ *   them past the call, and never synchronises the stream inside a compute
+ *   call: work is only enqueued on `stream` (a cudaStream_t passed as void*;
+ *   NULL = the legacy default stream).
+ * - bf16 tensors are IEEE bfloat16 bit patterns. Row strides are counted in
+ *   elements and must keep every row 16-byte aligned.
+ * - Every call returns PKV_OK (0) or a negative PKV_ERR_* status. Argument
+ *   checks run on the host before anything is enqueued; a failed check
+ *   enqueues nothing. A CUDA launch error returns PKV_ERR_CUDA and
+ *   pkv_last_cuda_error() gives its text.
+ * - Bad *contents* of device arrays (a slot or block id outside the pool,
+ *   inconsistent lengths) cannot be seen by the host without a sync. Kernels
+ *   skip such entries instead of touching memory out of range and set bits in
+ *   a sticky per-device error word, read by pkv_get_device_errors().
+ *
+ * Pool layout (the pages' physical KV cache, "vllm v1 源码精读（三）", §3.3):
+ *   kv_cache[num_blocks][2][block_size][num_kv_heads][head_dim], bf16,
+ *   contiguous; index 0 of the second dimension holds K, 1 holds V.
+ *   block_size must be 16 (the pages' default, "vLLM 架构源码解析（一）" §1.1,
+ *   §5.1); head_dim must be 64 or 128.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_ABI_VERSION 1
+
+/* status codes */
+#define PKV_OK 0
+#define PKV_ERR_NULL_POINTER (-1) /* a required pointer is NULL             */
+#define PKV_ERR_BAD_SHAPE (-2)    /* a size or count is out of range         */
+#define PKV_ERR_UNSUPPORTED (-3)  /* valid but not built (block size, d, G)  */
+#define PKV_ERR_MISALIGNED (-4)   /* pointer or stride not 16-byte aligned   */
+#define PKV_ERR_WORKSPACE (-5)    /* workspace missing or too small          */
+#define PKV_ERR_CUDA (-6)         /* a CUDA runtime / driver call failed     */
+#define PKV_ERR_DEVICE (-7)       /* the current device is not sm_103        */
+
+/* bits of the sticky device error word */
+#define PKV_DEVERR_SLOT_RANGE 0x1u  /* slot >= num_blocks * block_size: row skipped */
+#define PKV_DEVERR_BLOCK_RANGE 0x2u /* table entry outside [0, num_blocks) in the
+                                       used range: its keys are masked out       */
+#define PKV_DEVERR_LENGTHS 0x4u     /* query_start_loc / seq_lens /
+                                       num_computed_tokens inconsistent, or a
+                                       sequence needs more than
+                                       max_blocks_per_req blocks                 */
+#define PKV_DEVERR_TIMEOUT 0x8u     /* an on-chip wait (TMA / tensor core) gave
+                                       up after its time limit                    */
+
+/* Shape of the physical pool. */
+typedef struct pkv_cache_layout {
+  int32_t num_blocks;   /* physical blocks in the pool, >= 1                  */
+  int32_t block_size;   /* tokens per block; must be 16                       */
+  int32_t num_kv_heads; /* kv heads per token                                 */
+  int32_t head_dim;     /* 64 or 128                                          */
+} pkv_cache_layout;
+
+/* Optional tuning of pkv_paged_attention; pass NULL for the defaults. */
+typedef struct pkv_attention_options {
+  /* Decode warps that split the step's decode KV stream between them
+   * (split-KV). 0 = one full wave of the device. A single warp means no
+   * split at all; tests use other values to vary the partitioning. */
+  int32_t decode_warps;
+  int32_t reserved[7]; /* must be zero */
+} pkv_attention_options;
+
+/* Library version (PKV_ABI_VERSION). */
+int32_t pkv_abi_version(void);
+
+/* Text for a status code; never NULL. */
+const char* pkv_status_string(int32_t status);
+
+/* Text of the last CUDA error this thread saw inside the library. */
+const char* pkv_last_cuda_error(void);
+
+/*
+ * pkv_slot_mapping -- physical slot of every new token of the varlen batch.
+ *
+ * "vllm v1 源码精读（三）" §3.4: request r's i-th new token sits at position
+ * pos = num_computed_tokens[r] + i and goes to
+ *   slot = block_table[r][pos / block_size] * block_size + pos % block_size
+ * (the page's worked examples: request 0 pos 17 -> 193, request 2 pos 32 ->
+ * 144 with tables [[5,12,-1],[3,-1,-1],[7,21,9]]).
+ *
+ * slot_mapping        out, device int64 [num_tokens]. Token t belongs to the
+ *                     request r with query_start_loc[r] <= t <
+ *                     query_start_loc[r+1]; tokens at or past
+ *                     query_start_loc[num_reqs] get -1 (padding). A token
+ *                     whose table entry is missing or outside the pool gets
+ *                     -1 and sets PKV_DEVERR_BLOCK_RANGE / _LENGTHS.
+ * block_table         device int32 [num_reqs][max_blocks_per_req], -1 = unused.
+ * query_start_loc     device int32 [num_reqs + 1], non-decreasing, [0] = 0.
+ * num_computed_tokens device int32 [num_reqs].
+ * num_blocks          pool size, for the range check.
+ */
+int32_t pkv_slot_mapping(int64_t* slot_mapping, const int32_t* block_table,
+                         int32_t max_blocks_per_req,
+                         const int32_t* query_start_loc,
+                         const int32_t* num_computed_tokens, int32_t num_reqs,
+                         int32_t num_tokens, int32_t num_blocks,
+                         int32_t block_size, void* stream);
+
+/*
+ * pkv_paged_kv_write -- reshape_and_cache: store each new token's K and V rows
+ * into the pool at its slot ("vLLM 架构源码解析（一）" §3.3.3 step 2;
+ * "vllm v1 源码精读（三）" §3.4, reshape_and_cache_flash). A bit copy:
+ *   kv_cache[s / 16][0][s % 16][:][:] = key[t],  [..][1][..] = value[t]
+ * for every t with s = slot_mapping[t] >= 0. Negative slots are skipped;
+ * slots >= num_blocks * 16 are skipped and set PKV_DEVERR_SLOT_RANGE. Two
+ * tokens with the same slot race (undefined which wins).
+ *
+ * kv_cache      in/out, device bf16 pool (layout above).
+ * key, value    device bf16 [num_tokens][num_kv_heads][head_dim]; row t starts
+ *               at key + t * key_row_stride (0 = num_kv_heads * head_dim).
+ * slot_mapping  device int64 [num_tokens].
+ */
+int32_t pkv_paged_kv_write(void* kv_cache, const void* key, const void* value,
+                           int64_t key_row_stride, int64_t value_row_stride,
+                           const int64_t* slot_mapping, int32_t num_tokens,
+                           pkv_cache_layout layout, void* stream);
+
+/*
+ * pkv_attention_workspace_size -- bytes of device workspace that
+ * pkv_paged_attention needs for `num_reqs` requests on the current device
+ * with the given options (NULL = defaults). Returns a negative status on bad
+ * arguments. The size does not depend on sequence lengths.
+ */
+int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
+                                     pkv_cache_layout layout,
+                                     const pkv_attention_options* options);
+
+/*
+ * pkv_paged_attention -- attention of one mixed step over the paged cache.
+ *
+ * Run it after pkv_paged_kv_write of the same step: the step's new tokens are
+ * read back from the pool ("vLLM 架构源码解析（一）" §3.3.3: write, then
+ * attend through the block tables; "vllm v1 源码精读（三）" §4.2: one varlen
+ * call holds prefill chunks and decodes; "Inside vLLM" §3.4: each sequence
+ * attends only its own tokens).
+ *
+ * For request r with c = num_computed_tokens[r], n = query_start_loc[r+1] -
+ * query_start_loc[r] and L = seq_lens[r] = c + n: its i-th query row
+ * (batch row query_start_loc[r] + i, absolute position c + i) and q head h
+ * attend keys j = 0 .. c + i of kv head h / (num_q_heads / num_kv_heads):
+ *   out = sum_j softmax_j(scale * q . k_j) v_j,
+ * key j read from block block_table[r][j / 16], offset j % 16.
+ * Rows with n == 1 run on the split-KV decode kernels (+ combine); rows of
+ * requests with n > 1 run on the tensor-core prefill kernel.
+ *
+ * out            device bf16 [num_tokens][num_q_heads][head_dim], contiguous.
+ *                Rows past query_start_loc[num_reqs] are not written.
+ * q              device bf16 [num_tokens][num_q_heads][head_dim]; row t at
+ *                q + t * q_row_stride (0 = num_q_heads * head_dim).
+ * kv_cache       device bf16 pool (layout above), read only.
+ * block_table    device int32 [num_reqs][max_blocks_per_req], -1 = unused;
+ *                entries from ceil(L / 16) on are never read.
+ * seq_lens, query_start_loc, num_computed_tokens: device int32 as above.
+ * num_tokens     rows of q / out (>= query_start_loc[num_reqs]).
+ * max_query_len  host hint: >= every n (like max_seqlen_q).
+ * max_seq_len    host hint: >= every L (like max_seqlen_k).
+ * num_q_heads    multiple of num_kv_heads; num_q_heads / num_kv_heads must be
+ *                1, 2, 4 or 8.
+ * scale          softmax scale (1/sqrt(head_dim) on the pages' models).
+ * workspace      device buffer of at least pkv_attention_workspace_size()
+ *                bytes, 256-byte aligned, private to this call while it runs
+ *                (no zeroing needed).
+ */
+int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride,
+                            const void* kv_cache, const int32_t* block_table,
+                            int32_t max_blocks_per_req, const int32_t* seq_lens,
+                            const int32_t* query_start_loc,
+                            const int32_t* num_computed_tokens, int32_t num_reqs,
+                            int32_t num_tokens, int32_t max_query_len,
+                            int32_t max_seq_len, int32_t num_q_heads, float scale,
+                            pkv_cache_layout layout, void* workspace,
+                            size_t workspace_bytes,
+                            const pkv_attention_options* options, void* stream);
+
+/*
+ * pkv_get_device_errors -- checked path: synchronise `stream`, then return
+ * in *flags the PKV_DEVERR_* bits that kernels on the current device have set
+ * since the last clear; clear them when `clear` is nonzero.
+ */
+int32_t pkv_get_device_errors(uint32_t* flags, int32_t clear, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

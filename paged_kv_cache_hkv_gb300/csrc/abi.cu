@@ -1,0 +1,374 @@
+// C ABI of libpagedkv.so: argument checks, launch planning, tensor maps.
+// Declarations and the contract of every entry point: include/pagedkv.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pagedkv.h"
+#include "launch.h"
+
+namespace {
+
+thread_local char g_cuda_error[256] = "";
+
+int32_t cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", where, cudaGetErrorString(e));
+  return PKV_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+  int num_sms = 0;
+  bool ok = false;
+  int full_wave_warps[2][4] = {};  // [D==128][log2 heads per warp]
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_init[kMaxDevices] = {};
+
+int32_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!g_dev_init[dev]) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.ok = (major == 10 && minor == 3);
+    g_dev_init[dev] = true;
+  }
+  if (!d.ok) return PKV_ERR_DEVICE;
+  *out = &d;
+  return PKV_OK;
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime so that the library
+// does not link the driver library directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int32_t encode_fn(EncodeTiledFn* fn) {
+  static EncodeTiledFn cached = nullptr;
+  static std::once_flag once;
+  static cudaError_t status = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                              cudaEnableDefault, &q);
+    if (status == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      cached = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!cached) return cuda_fail(status == cudaSuccess ? cudaErrorSymbolNotFound : status,
+                                "cuTensorMapEncodeTiled entry point");
+  *fn = cached;
+  return PKV_OK;
+}
+
+// 3-D bf16 map: dims {d0, d1, d2} (d0 contiguous), byte strides of dims 1, 2.
+int32_t make_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
+                 CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn;
+  int32_t st = encode_fn(&fn);
+  if (st != PKV_OK) return st;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
+                  static_cast<int>(r));
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+int32_t check_layout(const pkv_cache_layout& l) {
+  if (l.num_blocks < 1 || l.num_kv_heads < 1 || l.head_dim < 1 || l.block_size < 1)
+    return PKV_ERR_BAD_SHAPE;
+  if (l.block_size != 16) return PKV_ERR_UNSUPPORTED;
+  if (l.head_dim != 64 && l.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<long long>(l.num_blocks) * 32 >= (1ll << 31)) return PKV_ERR_BAD_SHAPE;
+  return PKV_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t hdr, dec_prefix, pf_req, pf_prefix, part_ml, part_o, total;
+};
+
+WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long warps) {
+  WsLayout w;
+  const long long slots = pkv::decode_partial_slots(num_reqs, virt_heads, warps);
+  size_t off = 0;
+  w.hdr = off;
+  off += round256(pkv::kHdrWords * sizeof(uint32_t));
+  w.dec_prefix = off;
+  off += round256((num_reqs + 1) * sizeof(int32_t));
+  w.pf_req = off;
+  off += round256((num_reqs + 1) * sizeof(int32_t));
+  w.pf_prefix = off;
+  off += round256((num_reqs + 1) * sizeof(int32_t));
+  w.part_ml = off;
+  off += round256(static_cast<size_t>(slots) * gw * sizeof(float2));
+  w.part_o = off;
+  off += round256(static_cast<size_t>(slots) * gw * head_dim * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+int32_t decode_warps_for(DeviceInfo* d, int head_dim, int group,
+                         const pkv_attention_options* opt, long long* warps) {
+  if (opt) {
+    for (int i = 0; i < 7; ++i)
+      if (opt->reserved[i] != 0) return PKV_ERR_BAD_SHAPE;
+    if (opt->decode_warps < 0) return PKV_ERR_BAD_SHAPE;
+    if (opt->decode_warps > 0) {
+      *warps = opt->decode_warps;
+      return PKV_OK;
+    }
+  }
+  const int di = head_dim == 128 ? 1 : 0;
+  const int gw = pkv::decode_heads_per_warp(group);
+  const int gi = gw == 4 ? 2 : (gw == 2 ? 1 : 0);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int& cached = d->full_wave_warps[di][gi];
+  if (cached == 0) {
+    int w = 0;
+    cudaError_t e = pkv::decode_full_wave_warps(head_dim, group, d->num_sms, &w);
+    if (e != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    cached = w;
+  }
+  *warps = cached;
+  return PKV_OK;
+}
+
+int32_t check_group(int num_q_heads, int num_kv_heads) {
+  if (num_q_heads < 1 || num_q_heads % num_kv_heads) return PKV_ERR_BAD_SHAPE;
+  const int g = num_q_heads / num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+const char* pkv_status_string(int32_t status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case PKV_ERR_BAD_SHAPE: return "a size or count is out of range";
+    case PKV_ERR_UNSUPPORTED: return "unsupported block size, head_dim or head grouping";
+    case PKV_ERR_MISALIGNED: return "pointer or row stride not 16-byte aligned";
+    case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PKV_ERR_CUDA: return "CUDA call failed (see pkv_last_cuda_error)";
+    case PKV_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}
+
+const char* pkv_last_cuda_error(void) { return g_cuda_error; }
+
+int32_t pkv_slot_mapping(int64_t* slot_mapping, const int32_t* block_table,
+                         int32_t max_blocks_per_req, const int32_t* query_start_loc,
+                         const int32_t* num_computed_tokens, int32_t num_reqs,
+                         int32_t num_tokens, int32_t num_blocks, int32_t block_size,
+                         void* stream) {
+  if (num_tokens < 0 || num_reqs < 0 || max_blocks_per_req < 0 || num_blocks < 1)
+    return PKV_ERR_BAD_SHAPE;
+  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!slot_mapping || !query_start_loc) return PKV_ERR_NULL_POINTER;
+  if (num_reqs > 0 && (!block_table || !num_computed_tokens)) return PKV_ERR_NULL_POINTER;
+  DeviceInfo* d;
+  int32_t st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = pkv::launch_slot_mapping(slot_mapping, block_table, max_blocks_per_req,
+                                           query_start_loc, num_computed_tokens, num_reqs,
+                                           num_tokens, num_blocks,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "slot_mapping launch");
+}
+
+int32_t pkv_paged_kv_write(void* kv_cache, const void* key, const void* value,
+                           int64_t key_row_stride, int64_t value_row_stride,
+                           const int64_t* slot_mapping, int32_t num_tokens,
+                           pkv_cache_layout layout, void* stream) {
+  int32_t st = check_layout(layout);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_BAD_SHAPE;
+  const int64_t row = static_cast<int64_t>(layout.num_kv_heads) * layout.head_dim;
+  if (key_row_stride == 0) key_row_stride = row;
+  if (value_row_stride == 0) value_row_stride = row;
+  if (key_row_stride < row || value_row_stride < row) return PKV_ERR_BAD_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!kv_cache || !key || !value || !slot_mapping) return PKV_ERR_NULL_POINTER;
+  if (!aligned16(kv_cache) || !aligned16(key) || !aligned16(value) || (key_row_stride % 8) ||
+      (value_row_stride % 8))
+    return PKV_ERR_MISALIGNED;
+  DeviceInfo* d;
+  st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = pkv::launch_kv_write(kv_cache, key, value, key_row_stride, value_row_stride,
+                                       slot_mapping, num_tokens, layout.num_blocks,
+                                       layout.num_kv_heads, layout.head_dim, d->num_sms,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_write launch");
+}
+
+int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
+                                     pkv_cache_layout layout,
+                                     const pkv_attention_options* options) {
+  int32_t st = check_layout(layout);
+  if (st != PKV_OK) return st;
+  if (num_reqs < 0) return PKV_ERR_BAD_SHAPE;
+  st = check_group(num_q_heads, layout.num_kv_heads);
+  if (st != PKV_OK) return st;
+  DeviceInfo* d;
+  st = device_info(&d);
+  if (st != PKV_OK) return st;
+  const int group = num_q_heads / layout.num_kv_heads;
+  long long warps = 0;
+  st = decode_warps_for(d, layout.head_dim, group, options, &warps);
+  if (st != PKV_OK) return st;
+  const int gw = pkv::decode_heads_per_warp(group);
+  const int virt = layout.num_kv_heads * (group / gw);
+  return static_cast<int64_t>(ws_layout(num_reqs, virt, gw, layout.head_dim, warps).total);
+}
+
+int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, const void* kv_cache,
+                            const int32_t* block_table, int32_t max_blocks_per_req,
+                            const int32_t* seq_lens, const int32_t* query_start_loc,
+                            const int32_t* num_computed_tokens, int32_t num_reqs,
+                            int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                            int32_t num_q_heads, float scale, pkv_cache_layout layout,
+                            void* workspace, size_t workspace_bytes,
+                            const pkv_attention_options* options, void* stream) {
+  int32_t st = check_layout(layout);
+  if (st != PKV_OK) return st;
+  st = check_group(num_q_heads, layout.num_kv_heads);
+  if (st != PKV_OK) return st;
+  if (num_reqs < 0 || num_tokens < 0 || max_blocks_per_req < 0 || max_query_len < 0 ||
+      max_seq_len < 0)
+    return PKV_ERR_BAD_SHAPE;
+  if (!(scale == scale)) return PKV_ERR_BAD_SHAPE;
+  const int64_t row = static_cast<int64_t>(num_q_heads) * layout.head_dim;
+  if (q_row_stride == 0) q_row_stride = row;
+  if (q_row_stride < row) return PKV_ERR_BAD_SHAPE;
+  if (num_reqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
+  if (static_cast<long long>(max_seq_len) > static_cast<long long>(max_blocks_per_req) * 16)
+    return PKV_ERR_BAD_SHAPE;
+  if (!out || !q || !kv_cache || !block_table || !seq_lens || !query_start_loc ||
+      !num_computed_tokens)
+    return PKV_ERR_NULL_POINTER;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(kv_cache) || (q_row_stride % 8))
+    return PKV_ERR_MISALIGNED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_WORKSPACE;
+
+  DeviceInfo* d;
+  st = device_info(&d);
+  if (st != PKV_OK) return st;
+  const int group = num_q_heads / layout.num_kv_heads;
+  long long warps = 0;
+  st = decode_warps_for(d, layout.head_dim, group, options, &warps);
+  if (st != PKV_OK) return st;
+  const int gw = pkv::decode_heads_per_warp(group);
+  const int virt = layout.num_kv_heads * (group / gw);
+  const WsLayout wl = ws_layout(num_reqs, virt, gw, layout.head_dim, warps);
+  if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
+
+  char* wsb = static_cast<char*>(workspace);
+  pkv::AttnWorkspace ws;
+  ws.hdr = reinterpret_cast<uint32_t*>(wsb + wl.hdr);
+  ws.dec_prefix = reinterpret_cast<int32_t*>(wsb + wl.dec_prefix);
+  ws.pf_req = reinterpret_cast<int32_t*>(wsb + wl.pf_req);
+  ws.pf_prefix = reinterpret_cast<int32_t*>(wsb + wl.pf_prefix);
+  ws.part_ml = reinterpret_cast<float2*>(wsb + wl.part_ml);
+  ws.part_o = reinterpret_cast<float*>(wsb + wl.part_o);
+
+  pkv::AttnArgs a;
+  a.out = static_cast<uint16_t*>(out);
+  a.q = static_cast<const uint16_t*>(q);
+  a.q_stride = q_row_stride;
+  a.kv_cache = kv_cache;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks_per_req;
+  a.seq_lens = seq_lens;
+  a.qsl = query_start_loc;
+  a.num_computed = num_computed_tokens;
+  a.num_reqs = num_reqs;
+  a.num_tokens = num_tokens;
+  a.max_query_len = max_query_len;
+  a.max_seq_len = max_seq_len;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = layout.num_kv_heads;
+  a.head_dim = layout.head_dim;
+  a.num_blocks = layout.num_blocks;
+  a.scale = scale;
+
+  const int D = layout.head_dim, Hkv = layout.num_kv_heads;
+  const uint64_t row_bytes = static_cast<uint64_t>(Hkv) * D * 2;
+  // pool as rows of one kv head: {d, kv head, (block*2 + k|v)*16 + offset}
+  CUtensorMap kv_map;
+  st = make_map(&kv_map, kv_cache, D, Hkv, static_cast<uint64_t>(layout.num_blocks) * 32,
+                static_cast<uint64_t>(D) * 2, row_bytes, D, 1, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != PKV_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pkv::launch_plan(a, ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  if (max_query_len > 1) {
+    // pool for the tensor-core path: 64-element (128-byte) swizzled rows
+    CUtensorMap kv_map_sw, q_map;
+    st = make_map(&kv_map_sw, kv_cache, D, Hkv, static_cast<uint64_t>(layout.num_blocks) * 32,
+                  static_cast<uint64_t>(D) * 2, row_bytes, 64, 1, 16,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != PKV_OK) return st;
+    st = make_map(&q_map, q, D, num_q_heads, num_tokens, static_cast<uint64_t>(D) * 2,
+                  static_cast<uint64_t>(q_row_stride) * 2, 64, group, 128 / group,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != PKV_OK) return st;
+    e = pkv::launch_prefill(a, ws, kv_map_sw, q_map, d->num_sms, s);
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  }
+  e = pkv::launch_decode(a, ws, kv_map, static_cast<int>(warps), s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return PKV_OK;
+}
+
+int32_t pkv_get_device_errors(uint32_t* flags, int32_t clear, void* stream) {
+  if (!flags) return PKV_ERR_NULL_POINTER;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t v = 0;
+  e = pkv::read_errors_kvwrite(&v, clear != 0);
+  if (e == cudaSuccess) e = pkv::read_errors_decode(&v, clear != 0);
+  if (e == cudaSuccess) e = pkv::read_errors_prefill(&v, clear != 0);
+  if (e != cudaSuccess) return cuda_fail(e, "reading device error word");
+  *flags = v;
+  return PKV_OK;
+}
+
+}  // extern "C"

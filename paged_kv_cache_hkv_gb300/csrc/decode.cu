@@ -1,0 +1,662 @@
+// Plan, split-KV paged decode attention and the split-KV combine (sm_103a).
+//
+// Decode ("vLLM 架构源码解析（一）" §3.3.3, §4.2; "vllm v1 源码精读（三）" §4.2):
+// a request with one new token attends every one of its L cached keys, read
+// block by block through its block table without gathering them into a
+// contiguous buffer. GQA: the G = Hq/Hkv q heads of a kv head share every
+// K/V row, so one warp handles all of them (up to 4) and each row is read
+// from HBM once.
+//
+// Work split (split-KV, "PagedAttention v2" in §4.2 of the first page; the
+// pages only name it): the decode KV stream of the whole step is the
+// sequence of (request, kv head, block) in that order; warp w of W takes the
+// contiguous range [w*N/W, (w+1)*N/W). Every warp streams the same number
+// of blocks whatever the length mix, and a (request, kv head) cut by a range
+// boundary leaves one partial (m, l, o) per warp that touched it; the
+// combine kernel merges those with the usual log-sum-exp rule. A
+// (request, kv head) that falls inside one warp's range is finished there
+// and written straight to the output.
+//
+// Inside a warp: a ring of S shared-memory stages, each holding one block's
+// 16 K rows and 16 V rows of one kv head (one 3-D TMA copy, 2*16*D*2 bytes)
+// plus, on the first block of a piece, the G query rows (one bulk copy).
+// Lane 0 issues the copies S-1 blocks ahead of the block being computed.
+// Online softmax runs in base 2 with q pre-scaled by scale*log2(e).
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+static __device__ uint32_t g_errors_decode;
+
+// ------------------------------------------------------------------ plan
+// Block-wide exclusive scan of three counters (blockDim.x == 1024).
+struct Int3 {
+  int a, b, c;
+};
+
+__device__ __forceinline__ Int3 block_exclusive_scan(Int3 v, Int3* total) {
+  __shared__ Int3 warp_tot[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  Int3 inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, inc.a, off);
+    const int b = __shfl_up_sync(0xffffffffu, inc.b, off);
+    const int c = __shfl_up_sync(0xffffffffu, inc.c, off);
+    if (lane >= off) {
+      inc.a += a;
+      inc.b += b;
+      inc.c += c;
+    }
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    Int3 w = warp_tot[lane];
+    Int3 wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, wi.a, off);
+      const int b = __shfl_up_sync(0xffffffffu, wi.b, off);
+      const int c = __shfl_up_sync(0xffffffffu, wi.c, off);
+      if (lane >= off) {
+        wi.a += a;
+        wi.b += b;
+        wi.c += c;
+      }
+    }
+    warp_tot[lane] = Int3{wi.a - w.a, wi.b - w.b, wi.c - w.c};
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const Int3 base = warp_tot[warp];
+  __syncthreads();
+  return Int3{base.a + inc.a - v.a, base.b + inc.b - v.b, base.c + inc.c - v.c};
+}
+
+// One CTA of 1024 threads walks the requests once: decode blocks per
+// request (prefix), the compact list of prefill requests and their work
+// items, and length checks.
+__global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, AttnWorkspace ws, int tile_q) {
+  __shared__ Int3 total;
+  __shared__ int carry_dec, carry_req, carry_items;
+  if (threadIdx.x == 0) {
+    carry_dec = carry_req = carry_items = 0;
+  }
+  __syncthreads();
+  const int R = a.num_reqs;
+  for (int base = 0; base < R; base += 1024) {
+    const int r = base + threadIdx.x;
+    Int3 v{0, 0, 0};
+    if (r < R) {
+      const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
+      const int n = q1 - q0, L = __ldg(a.seq_lens + r), c = __ldg(a.num_computed + r);
+      bool bad = n < 0 || q0 < 0 || q1 > a.num_tokens || c < 0 || L != c + n ||
+                 (r == 0 && q0 != 0);
+      const long long nblk = (static_cast<long long>(L) + kBlockSize - 1) / kBlockSize;
+      if (!bad && n > 0 && nblk > a.max_blocks) bad = true;
+      if (bad) {
+        atomicOr(&g_errors_decode, kErrLengths);
+      } else if (n == 1) {
+        v.a = static_cast<int>(nblk);
+      } else if (n > 1) {
+        v.b = 1;
+        v.c = ((n + tile_q - 1) / tile_q) * a.num_kv_heads;
+      }
+    }
+    const Int3 ex = block_exclusive_scan(v, &total);
+    if (r < R) {
+      ws.dec_prefix[r] = carry_dec + ex.a;
+      if (v.b) {
+        ws.pf_req[carry_req + ex.b] = r;
+        ws.pf_prefix[carry_req + ex.b] = carry_items + ex.c;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      carry_dec += total.a;
+      carry_req += total.b;
+      carry_items += total.c;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    ws.dec_prefix[R] = carry_dec;
+    ws.pf_prefix[carry_req] = carry_items;
+    ws.hdr[kHdrDecodeBlocks] = static_cast<uint32_t>(carry_dec);
+    ws.hdr[kHdrPrefillReqs] = static_cast<uint32_t>(carry_req);
+    ws.hdr[kHdrPrefillItems] = static_cast<uint32_t>(carry_items);
+    ws.hdr[kHdrPrefillNext] = 0u;
+  }
+}
+
+// ------------------------------------------------------------------ decode
+struct DecodeParams {
+  const uint16_t* q;
+  long long q_stride;
+  uint16_t* out;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int num_reqs, num_q_heads, num_blocks;
+  int head_groups;  // q-head groups of GW per kv head
+  int virt_heads;   // num_kv_heads * head_groups
+  long long warps;  // W
+  float scale_log2;
+  const int32_t* dec_prefix;
+  const uint32_t* hdr;
+  float2* part_ml;
+  float* part_o;
+};
+
+// Warp that owns position x of the decode stream: ranges start at
+// floor(w * N / W).
+__device__ __forceinline__ long long owner_warp(long long x, long long N, long long W) {
+  return ((x + 1) * W + N - 1) / N - 1;
+}
+
+template <int D, int GW, int S>
+struct DecodeCfg {
+  static constexpr int LPK = D / 8;     // lanes per key row (8 bf16 per lane)
+  static constexpr int KPI = 32 / LPK;  // keys per warp instruction ("sub-groups")
+  static constexpr int KPL = 16 / KPI;  // keys per lane per block
+  static constexpr int NV = GW * KPL;   // partial scores per lane per block
+  static constexpr int NPL = NV >= LPK ? NV / LPK : 1;  // full scores per lane
+  static constexpr int DUP = NV >= LPK ? 1 : LPK / NV;  // lanes holding the same score
+  static constexpr int LPH = LPK / GW;                  // lanes per head in a sub-group
+  static constexpr uint32_t kKvBytes = 32u * D * 2u;
+  static constexpr uint32_t kQBytes = GW * D * 2u;
+  static_assert(KPL * KPI == 16, "block of 16 keys");
+  static_assert(KPL % NPL == 0, "a lane's scores stay in one head");
+
+  struct alignas(128) WarpSmem {
+    uint16_t kv[S][32][D];  // rows 0..15 K, 16..31 V of one kv head
+    uint16_t q[S][GW * D];
+    int4 meta0[S];  // r, virtual head, block, flags
+    int4 meta1[S];  // valid keys, token row, output slot (-1 = final)
+    uint64_t full[S];
+    alignas(16) float p[KPI][NV];
+    float2 hs[GW];
+  };
+};
+
+enum : int { kFirst = 1, kLast = 2, kInvalid = 4, kEnd = 8 };
+
+// Reduce-scatter across the LPK lanes of a sub-group: on return v[0..)
+// holds full sums for score indices (li * NV / LPK) + i.
+template <int N, int OFF>
+struct ReduceScatter {
+  static __device__ __forceinline__ void run(float* v, int li) {
+    if constexpr (OFF >= 1) {
+      if constexpr (N >= 2) {
+        constexpr int H = N / 2;
+        const bool upper = (li & OFF) != 0;
+#pragma unroll
+        for (int i = 0; i < H; ++i) {
+          const float send = upper ? v[i] : v[i + H];
+          const float keep = upper ? v[i + H] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+        }
+        ReduceScatter<H, OFF / 2>::run(v, li);
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], OFF);
+        ReduceScatter<1, OFF / 2>::run(v, li);
+      }
+    }
+  }
+};
+
+template <int D, int GW, int S, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
+    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+  using C = DecodeCfg<D, GW, S>;
+  using Smem = typename C::WarpSmem;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // dynamic shared memory is only guaranteed 16-byte aligned: round up
+  unsigned char* smem_base = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  Smem& sm = reinterpret_cast<Smem*>(smem_base)[warp];
+  const int sub = lane / C::LPK, li = lane % C::LPK;
+
+  const long long W = p.warps;
+  const long long w = static_cast<long long>(blockIdx.x) * WARPS + warp;
+  if (w >= W) return;
+  const long long N = static_cast<long long>(p.virt_heads) * p.hdr[kHdrDecodeBlocks];
+  const long long x0 = w * N / W, x1 = (w + 1) * N / W;
+  if (x0 >= x1) return;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(&sm.full[s], 1);
+    fence_barrier_init();
+    prefetch_tensormap(&kv_map);
+  }
+  __syncwarp();
+
+  // ---------------- producer state (identical in every lane)
+  long long x = x0;
+  int r, vg, blk, nblk, L = 0, t = 0, out_slot = -1;
+  bool new_piece = true;
+  {
+    const long long u = x0 / p.virt_heads;
+    r = upper_index(p.dec_prefix, p.num_reqs, u);
+    const int pr = __ldg(p.dec_prefix + r);
+    nblk = __ldg(p.dec_prefix + r + 1) - pr;
+    const long long rem = x0 - static_cast<long long>(p.virt_heads) * pr;
+    vg = static_cast<int>(rem / nblk);
+    blk = static_cast<int>(rem - static_cast<long long>(vg) * nblk);
+    L = __ldg(p.seq_lens + r);
+    t = __ldg(p.qsl + r);
+  }
+  int win_r = -1, win_base = 0, win_val = -1;
+
+  auto produce = [&](int s) {
+    if (x >= x1) {
+      if (lane == 0) {
+        sm.meta0[s] = make_int4(0, 0, 0, kEnd);
+        mbar_arrive(&sm.full[s]);
+      }
+      return;
+    }
+    if (new_piece) {
+      const long long a = static_cast<long long>(p.virt_heads) * __ldg(p.dec_prefix + r) +
+                          static_cast<long long>(vg) * nblk;
+      const long long wf = owner_warp(a, N, W), wl = owner_warp(a + nblk - 1, N, W);
+      out_slot = (wf == wl) ? -1 : static_cast<int>(static_cast<long long>(r) * p.virt_heads + vg + w);
+    }
+    if (r != win_r || blk < win_base || blk >= win_base + 32) {
+      win_r = r;
+      win_base = blk;
+      const int j = blk + lane;
+      win_val = (j < nblk) ? __ldg(p.block_table + static_cast<long long>(r) * p.max_blocks + j) : -1;
+    }
+    const int phys = __shfl_sync(0xffffffffu, win_val, blk - win_base);
+    const bool valid = phys >= 0 && phys < p.num_blocks;
+    int flags = (new_piece ? kFirst : 0) | ((blk == nblk - 1 || x == x1 - 1) ? kLast : 0) |
+                (valid ? 0 : kInvalid);
+    const int nvalid = min(kBlockSize, L - blk * kBlockSize);
+    if (lane == 0) {
+      sm.meta0[s] = make_int4(r, vg, blk, flags);
+      sm.meta1[s] = make_int4(nvalid, t, out_slot, 0);
+      const uint32_t tx = (valid ? C::kKvBytes : 0u) + (new_piece ? C::kQBytes : 0u);
+      if (!valid) atomicOr(&g_errors_decode, kErrBlockRange);
+      if (tx) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&sm.full[s], tx);
+        if (valid)
+          tma_load_3d(&sm.kv[s][0][0], &kv_map, 0, vg / p.head_groups, phys * 32, &sm.full[s]);
+        if (new_piece)
+          bulk_load(&sm.q[s][0], p.q + static_cast<long long>(t) * p.q_stride + vg * GW * D,
+                    C::kQBytes, &sm.full[s]);
+      } else {
+        mbar_arrive(&sm.full[s]);
+      }
+    }
+    // advance the odometer (request, virtual head, block)
+    ++x;
+    ++blk;
+    new_piece = false;
+    if (blk == nblk) {
+      blk = 0;
+      new_piece = true;
+      if (++vg == p.virt_heads) {
+        vg = 0;
+        if (x < x1) {
+          do {
+            ++r;
+            nblk = __ldg(p.dec_prefix + r + 1) - __ldg(p.dec_prefix + r);
+          } while (nblk == 0);
+          L = __ldg(p.seq_lens + r);
+          t = __ldg(p.qsl + r);
+        }
+      }
+    }
+  };
+
+  // ---------------- consumer state
+  float2 q2[GW][4];  // q * scale * log2(e), dims li*8 .. li*8+7 as pairs
+  float2 o2[GW][4];  // unnormalised output, same dims
+  float m_run = -INFINITY, l_run = 0.f;  // for head hm of this lane
+  const int idx_base = (li * C::NV) / C::LPK;
+  const int hm = idx_base / C::KPL;
+
+#pragma unroll
+  for (int s = 0; s < S; ++s) produce(s);
+
+  uint32_t phases = 0;
+  int s = 0;
+  while (true) {
+    const uint32_t par = (phases >> s) & 1u;
+    phases ^= 1u << s;
+    if (!mbar_wait(&sm.full[s], par)) {
+      atomicOr(&g_errors_decode, kErrTimeout);
+      // drain every stage that may still have a copy in flight, then stop
+      for (int k = 0; k < S; ++k)
+        if (k != s) mbar_wait(&sm.full[k], (phases >> k) & 1u, kDrainLimitNs);
+      break;
+    }
+    const int4 m0 = sm.meta0[s];
+    if (m0.w & kEnd) break;
+    const int4 m1 = sm.meta1[s];
+    const int flags = m0.w;
+    const uint32_t kv_base = smem_u32(&sm.kv[s][0][0]);
+
+    if (flags & kFirst) {
+      const uint32_t qa = smem_u32(&sm.q[s][0]) + li * 16;
+#pragma unroll
+      for (int h = 0; h < GW; ++h) {
+        const uint4 qv = ld_shared_v4(qa + h * D * 2);
+        const uint32_t wd[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          q2[h][e] = make_float2(bf16_lo(wd[e]) * p.scale_log2, bf16_hi(wd[e]) * p.scale_log2);
+          o2[h][e] = make_float2(0.f, 0.f);
+        }
+      }
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+    const bool bvalid = !(flags & kInvalid);
+    const int nvalid = m1.x;
+
+    // ---- scores: acc[h * KPL + j] for key j*KPI + sub, partial over 8 dims
+    float acc[C::NV];
+#pragma unroll
+    for (int j = 0; j < C::KPL; ++j) {
+      const int key = j * C::KPI + sub;
+      const uint4 kv4 = ld_shared_v4(kv_base + (key * D + li * 8) * 2);
+      const uint32_t wd[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
+      float2 k2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(wd[e]), bf16_hi(wd[e]));
+#pragma unroll
+      for (int h = 0; h < GW; ++h) {
+        float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a2 = ffma2(q2[h][e], k2[e], a2);
+        acc[h * C::KPL + j] = a2.x + a2.y;
+      }
+    }
+    ReduceScatter<C::NV, C::LPK / 2>::run(acc, li);
+
+    // ---- online softmax for head hm
+    float sc[C::NPL];
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < C::NPL; ++i) {
+      const int jj = (idx_base + i) % C::KPL;
+      const int key = jj * C::KPI + sub;
+      sc[i] = (bvalid && key < nvalid) ? acc[i] : -INFINITY;
+      lmax = fmaxf(lmax, sc[i]);
+    }
+#pragma unroll
+    for (int off = 1; off < C::LPH; off <<= 1)
+      lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+#pragma unroll
+    for (int off = C::LPK; off < 32; off <<= 1)
+      lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+    const float m_new = fmaxf(m_run, lmax);
+    const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+    float psum = 0.f;
+#pragma unroll
+    for (int i = 0; i < C::NPL; ++i) {
+      const float pv = (sc[i] == -INFINITY) ? 0.f : exp2f(sc[i] - m_new);
+      sm.p[sub][idx_base + i] = pv;
+      psum += pv;
+    }
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+    if (sub == 0 && (li % C::LPH) == 0) sm.hs[hm].x = alpha;
+    __syncwarp();
+
+    // ---- o = o * alpha + sum_j p_j v_j
+    {
+      float pj[C::NV];
+#pragma unroll
+      for (int i = 0; i < C::NV; i += 4) {
+        const float4 f = ld_shared_f4(smem_u32(&sm.p[sub][i]));
+        pj[i] = f.x;
+        pj[i + 1] = f.y;
+        pj[i + 2] = f.z;
+        pj[i + 3] = f.w;
+      }
+#pragma unroll
+      for (int h = 0; h < GW; ++h) {
+        const float a = sm.hs[h].x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(o2[h][e].x * a, o2[h][e].y * a);
+      }
+#pragma unroll
+      for (int j = 0; j < C::KPL; ++j) {
+        const int key = j * C::KPI + sub;
+        if (bvalid && key < nvalid) {
+          const uint4 vv = ld_shared_v4(kv_base + ((16 + key) * D + li * 8) * 2);
+          const uint32_t wd[4] = {vv.x, vv.y, vv.z, vv.w};
+          float2 v2[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v2[e] = make_float2(bf16_lo(wd[e]), bf16_hi(wd[e]));
+#pragma unroll
+          for (int h = 0; h < GW; ++h) {
+            const float pp = pj[h * C::KPL + j];
+            const float2 p2 = make_float2(pp, pp);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o2[h][e] = ffma2(p2, v2[e], o2[h][e]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+
+    // ---- end of this warp's piece of (request, head group)
+    if (flags & kLast) {
+#pragma unroll
+      for (int off = C::LPK; off < 32; off <<= 1)
+#pragma unroll
+        for (int h = 0; h < GW; ++h)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            o2[h][e].x += __shfl_xor_sync(0xffffffffu, o2[h][e].x, off);
+            o2[h][e].y += __shfl_xor_sync(0xffffffffu, o2[h][e].y, off);
+          }
+      float lo = (C::DUP == 1 || (li % C::DUP) == 0) ? l_run : 0.f;
+#pragma unroll
+      for (int off = 1; off < C::LPH; off <<= 1) lo += __shfl_xor_sync(0xffffffffu, lo, off);
+#pragma unroll
+      for (int off = C::LPK; off < 32; off <<= 1) lo += __shfl_xor_sync(0xffffffffu, lo, off);
+      if (sub == 0 && (li % C::LPH) == 0) sm.hs[hm] = make_float2(m_run, lo);
+      __syncwarp();
+      const int vgh = m0.y, slot = m1.z, row = m1.y;
+      if (sub == 0) {
+#pragma unroll
+        for (int h = 0; h < GW; ++h) {
+          const float2 ml = sm.hs[h];
+          if (slot < 0) {
+            const float inv = 1.f / ml.y;
+            uint4 ov;
+            ov.x = pack_bf16x2(o2[h][0].x * inv, o2[h][0].y * inv);
+            ov.y = pack_bf16x2(o2[h][1].x * inv, o2[h][1].y * inv);
+            ov.z = pack_bf16x2(o2[h][2].x * inv, o2[h][2].y * inv);
+            ov.w = pack_bf16x2(o2[h][3].x * inv, o2[h][3].y * inv);
+            const long long off =
+                (static_cast<long long>(row) * p.num_q_heads + vgh * GW + h) * D + li * 8;
+            *reinterpret_cast<uint4*>(p.out + off) = ov;
+          } else {
+            float4* dst = reinterpret_cast<float4*>(
+                p.part_o + (static_cast<long long>(slot) * GW + h) * D + li * 8);
+            dst[0] = make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
+            dst[1] = make_float4(o2[h][2].x, o2[h][2].y, o2[h][3].x, o2[h][3].y);
+            if (li == 0) p.part_ml[static_cast<long long>(slot) * GW + h] = ml;
+          }
+        }
+      }
+      __syncwarp();
+    }
+
+    produce(s);
+    s = (s + 1 == S) ? 0 : s + 1;
+  }
+}
+
+// ------------------------------------------------------------------ combine
+// One warp per (request, q head) whose kv head was split between warps.
+template <int D, int GW>
+__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int num_items) {
+  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (gw >= num_items) return;
+  const int h = gw % GW;
+  const int rv = gw / GW;
+  const int vg = rv % p.virt_heads, r = rv / p.virt_heads;
+  const int pr = __ldg(p.dec_prefix + r);
+  const int nblk = __ldg(p.dec_prefix + r + 1) - pr;
+  if (nblk == 0) return;
+  const long long W = p.warps;
+  const long long N = static_cast<long long>(p.virt_heads) * p.hdr[kHdrDecodeBlocks];
+  const long long a = static_cast<long long>(p.virt_heads) * pr + static_cast<long long>(vg) * nblk;
+  const long long wf = owner_warp(a, N, W), wl = owner_warp(a + nblk - 1, N, W);
+  if (wf == wl) return;
+  constexpr int E = D / 32;  // dims per lane
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float M = -INFINITY, Ls = 0.f;
+  const long long base = static_cast<long long>(r) * p.virt_heads + vg;
+  for (long long ww = wf; ww <= wl; ++ww) {
+    if (ww * N / W == (ww + 1) * N / W) continue;  // empty range: wrote nothing
+    const long long slot = base + ww;
+    const float2 ml = p.part_ml[slot * GW + h];
+    const float Mn = fmaxf(M, ml.x);
+    if (Mn == -INFINITY) continue;
+    const float sa = exp2f(M - Mn), sb = exp2f(ml.x - Mn);
+    Ls = Ls * sa + ml.y * sb;
+    const float* src = p.part_o + (slot * GW + h) * D + lane * E;
+    if constexpr (E == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] = acc[0] * sa + v.x * sb;
+      acc[1] = acc[1] * sa + v.y * sb;
+      acc[2] = acc[2] * sa + v.z * sb;
+      acc[3] = acc[3] * sa + v.w * sb;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] = acc[0] * sa + v.x * sb;
+      acc[1] = acc[1] * sa + v.y * sb;
+    }
+    M = Mn;
+  }
+  const float inv = 1.f / Ls;
+  const int row = __ldg(p.qsl + r);
+  uint16_t* dst = p.out + (static_cast<long long>(row) * p.num_q_heads + vg * GW + h) * D + lane * E;
+  if constexpr (E == 4) {
+    uint2 ov;
+    ov.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    ov.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = ov;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+// ------------------------------------------------------------------ host
+constexpr int kDecodeStages = 3;
+constexpr int kDecodeWarps = 4;
+
+template <int D, int GW>
+constexpr size_t decode_smem_bytes() {
+  return sizeof(typename DecodeCfg<D, GW, kDecodeStages>::WarpSmem) * kDecodeWarps + 128;
+}
+
+template <int D, int GW>
+static cudaError_t decode_occupancy(int* ctas_per_sm) {
+  auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps>;
+  const size_t smem = decode_smem_bytes<D, GW>();
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, kern, kDecodeWarps * 32, smem);
+}
+
+cudaError_t decode_full_wave_warps(int head_dim, int group, int num_sms, int* warps) {
+  const int gw = decode_heads_per_warp(group);
+  int ctas = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (head_dim == 128 && gw == 4) e = decode_occupancy<128, 4>(&ctas);
+  if (head_dim == 128 && gw == 2) e = decode_occupancy<128, 2>(&ctas);
+  if (head_dim == 128 && gw == 1) e = decode_occupancy<128, 1>(&ctas);
+  if (head_dim == 64 && gw == 4) e = decode_occupancy<64, 4>(&ctas);
+  if (head_dim == 64 && gw == 2) e = decode_occupancy<64, 2>(&ctas);
+  if (head_dim == 64 && gw == 1) e = decode_occupancy<64, 1>(&ctas);
+  if (e != cudaSuccess) return e;
+  if (ctas < 1) ctas = 1;
+  *warps = num_sms * ctas * kDecodeWarps;
+  return cudaSuccess;
+}
+
+cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream) {
+  const int group = a.num_q_heads / a.num_kv_heads;
+  plan_kernel<<<1, 1024, 0, stream>>>(a, ws, 128 / group);
+  return cudaGetLastError();
+}
+
+template <int D, int GW>
+static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_map,
+                                   cudaStream_t stream) {
+  auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps>;
+  const size_t smem = decode_smem_bytes<D, GW>();
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long grid = (p.warps + kDecodeWarps - 1) / kDecodeWarps;
+  kern<<<static_cast<unsigned>(grid), kDecodeWarps * 32, smem, stream>>>(kv_map, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int items = p.num_reqs * p.virt_heads * GW;
+  combine_kernel<D, GW><<<(items + 3) / 4, 128, 0, stream>>>(p, items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
+                          int decode_warps, cudaStream_t stream) {
+  const int group = a.num_q_heads / a.num_kv_heads;
+  const int gw = decode_heads_per_warp(group);
+  DecodeParams p;
+  p.q = a.q;
+  p.q_stride = a.q_stride;
+  p.out = a.out;
+  p.block_table = a.block_table;
+  p.max_blocks = a.max_blocks;
+  p.seq_lens = a.seq_lens;
+  p.qsl = a.qsl;
+  p.num_reqs = a.num_reqs;
+  p.num_q_heads = a.num_q_heads;
+  p.num_blocks = a.num_blocks;
+  p.head_groups = group / gw;
+  p.virt_heads = a.num_kv_heads * p.head_groups;
+  p.warps = decode_warps;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.dec_prefix = ws.dec_prefix;
+  p.hdr = ws.hdr;
+  p.part_ml = ws.part_ml;
+  p.part_o = ws.part_o;
+  if (a.head_dim == 128 && gw == 4) return launch_decode_t<128, 4>(p, kv_map, stream);
+  if (a.head_dim == 128 && gw == 2) return launch_decode_t<128, 2>(p, kv_map, stream);
+  if (a.head_dim == 128 && gw == 1) return launch_decode_t<128, 1>(p, kv_map, stream);
+  if (a.head_dim == 64 && gw == 4) return launch_decode_t<64, 4>(p, kv_map, stream);
+  if (a.head_dim == 64 && gw == 2) return launch_decode_t<64, 2>(p, kv_map, stream);
+  if (a.head_dim == 64 && gw == 1) return launch_decode_t<64, 1>(p, kv_map, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_errors_decode(uint32_t* out, bool clear) {
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_errors_decode, sizeof(v));
+  if (e != cudaSuccess) return e;
+  *out |= v;
+  if (clear) {
+    const uint32_t z = 0;
+    e = cudaMemcpyToSymbol(g_errors_decode, &z, sizeof(z));
+  }
+  return e;
+}
+
+}  // namespace pkv

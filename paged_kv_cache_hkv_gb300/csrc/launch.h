@@ -1,0 +1,77 @@
+// Internal launch interface between the C ABI shim and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Header words at the start of the attention workspace (written by the plan
+// kernel every call).
+enum : int {
+  kHdrDecodeBlocks = 0,  // sum of ceil(L/16) over decode requests
+  kHdrPrefillReqs = 1,   // requests with query_len > 1
+  kHdrPrefillItems = 2,  // prefill work items (tile x kv head)
+  kHdrPrefillNext = 3,   // work counter of the persistent prefill kernel
+  kHdrWords = 64,
+};
+
+// Device pointers into the attention workspace.
+struct AttnWorkspace {
+  uint32_t* hdr;         // [kHdrWords]
+  int32_t* dec_prefix;   // [R + 1]: decode blocks before request r
+  int32_t* pf_req;       // [R]: request id of the k-th prefill request
+  int32_t* pf_prefix;    // [R + 1]: prefill items before the k-th prefill request
+  float2* part_ml;       // [slots][GW]: (running max in log2 units, sum)
+  float* part_o;         // [slots][GW][D]: unnormalised partial outputs
+};
+
+struct AttnArgs {
+  uint16_t* out;  // bf16 [T][Hq][D]
+  const uint16_t* q;  // bf16 rows of q_stride elements
+  long long q_stride;  // elements between token rows of q
+  const void* kv_cache;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  const int32_t* num_computed;
+  int num_reqs, num_tokens, max_query_len, max_seq_len;
+  int num_q_heads, num_kv_heads, head_dim, num_blocks;
+  float scale;
+};
+
+// Heads handled together by one decode warp, and head groups per kv head.
+inline int decode_heads_per_warp(int group) { return group < 4 ? group : 4; }
+
+// slots of split-KV partials the decode kernel may write
+inline long long decode_partial_slots(int num_reqs, int virt_heads, long long warps) {
+  return static_cast<long long>(num_reqs) * virt_heads + warps;
+}
+
+cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int max_blocks,
+                                const int32_t* qsl, const int32_t* num_computed, int num_reqs,
+                                int num_tokens, int num_blocks, cudaStream_t stream);
+
+cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long long key_stride,
+                            long long value_stride, const int64_t* slots, int num_tokens,
+                            int num_blocks, int num_kv_heads, int head_dim, int num_sms,
+                            cudaStream_t stream);
+
+cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream);
+
+// Decode warps in one full wave on this device for the given shape.
+cudaError_t decode_full_wave_warps(int head_dim, int group, int num_sms, int* warps);
+
+cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
+                          int decode_warps, cudaStream_t stream);
+
+cudaError_t launch_prefill(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
+                           const CUtensorMap& q_map, int num_sms, cudaStream_t stream);
+
+cudaError_t read_errors_kvwrite(uint32_t* out, bool clear);
+cudaError_t read_errors_decode(uint32_t* out, bool clear);
+cudaError_t read_errors_prefill(uint32_t* out, bool clear);
+
+}  // namespace pkv

@@ -1,0 +1,86 @@
+"""Device-resident copy of one step's inputs, run through the C ABI.
+
+``DeviceStep`` uploads a host step (``synth.PagedStep``) once and runs the
+hot path on it: slot mapping, cache write, attention. It is what the tests,
+the smoke check and the benchmark drive.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding
+
+
+def _bf16(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def _i32(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def bf16_to_numpy(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> host uint16 bit patterns."""
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class DeviceStep:
+    """One step's inputs on the GPU plus its output buffers."""
+
+    def __init__(self, step, device="cuda", decode_warps=None, upload_pool=True):
+        self.step = step
+        self.device = torch.device(device)
+        dev = self.device
+        self.kv_cache = _bf16(step.kv_cache, dev) if upload_pool else None
+        self.q = _bf16(step.q, dev)
+        self.k = _bf16(step.k, dev)
+        self.v = _bf16(step.v, dev)
+        self.block_table = _i32(step.block_table, dev)
+        self.seq_lens = _i32(step.seq_lens, dev)
+        self.query_start_loc = _i32(step.query_start_loc, dev)
+        self.num_computed = _i32(step.num_computed, dev)
+        T = step.num_tokens
+        self.slot_mapping = torch.empty(T, dtype=torch.int64, device=dev)
+        self.out = torch.zeros((T, step.num_q_heads, step.head_dim), dtype=torch.bfloat16,
+                               device=dev)
+        self.decode_warps = decode_warps
+        self.layout = binding.pkv_cache_layout(step.num_blocks, step.block_size,
+                                               step.num_kv_heads, step.head_dim)
+        nbytes = binding.pkv_attention_workspace_size(step.num_reqs, step.num_q_heads,
+                                                      self.layout, decode_warps=decode_warps)
+        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+
+    # -- the three calls of the hot path
+    def slot_map(self, stream=None):
+        s = self.step
+        binding.pkv_slot_mapping(self.slot_mapping, self.block_table, self.query_start_loc,
+                                 self.num_computed, s.num_blocks, s.block_size, stream=stream)
+
+    def write(self, stream=None):
+        binding.pkv_paged_kv_write(self.kv_cache, self.k, self.v, self.slot_mapping,
+                                   stream=stream)
+
+    def attend(self, stream=None):
+        s = self.step
+        binding.pkv_paged_attention(
+            self.out, self.q, self.kv_cache, self.block_table, self.seq_lens,
+            self.query_start_loc, self.num_computed, max_query_len=s.max_query_len,
+            max_seq_len=s.max_seq_len, scale=s.scale, workspace=self.workspace,
+            decode_warps=self.decode_warps, stream=stream)
+
+    def run(self, stream=None):
+        self.slot_map(stream)
+        self.write(stream)
+        self.attend(stream)
+
+    # -- host copies
+    def out_host(self) -> np.ndarray:
+        return bf16_to_numpy(self.out)
+
+    def pool_host(self) -> np.ndarray:
+        return bf16_to_numpy(self.kv_cache).reshape(self.step.kv_cache.shape)
+
+    def slots_host(self) -> np.ndarray:
+        return self.slot_mapping.cpu().numpy()

@@ -1,0 +1,178 @@
+"""CUDA path vs the CPU oracle on the GPU (through the C ABI).
+
+Slot mapping and the cache write must be bit-exact (the whole pool is
+compared, so untouched slots must be unchanged too); attention must be within
+|gpu - oracle| <= max(2e-2, 1e-2 * |oracle|) per element.
+"""
+
+import numpy as np
+import pytest
+
+from parity import assert_close, oracle_step
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU containers
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from paged_kv_cache_hkv_gb300 import binding, synth  # noqa: E402
+from paged_kv_cache_hkv_gb300.runner import DeviceStep  # noqa: E402
+from paged_kv_cache_hkv_gb300.synth import RequestSpec, make_step  # noqa: E402
+
+
+@pytest.fixture(autouse=True)
+def _clear_errors():
+    binding.pkv_get_device_errors(clear=True)
+    yield
+
+
+def run_and_check(step, decode_warps=None, rows=None, check_pool=True):
+    ds = DeviceStep(step, decode_warps=decode_warps)
+    ds.run()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_errors(clear=True) == 0
+    slots, pool, ref = oracle_step(step, rows=rows)
+    assert np.array_equal(ds.slots_host(), slots)
+    if check_pool:
+        assert np.array_equal(ds.pool_host(), pool)
+    return assert_close(ds.out_host(), ref, rows=rows)
+
+
+# ---------------------------------------------------------------- workloads
+DECODE_WORKLOADS = ["tiny_decode", "llama_decode", "prefix_sharing", "long_context"]
+
+
+@pytest.mark.parametrize("name", DECODE_WORKLOADS)
+def test_decode_workload_parity(name):
+    step = synth.WORKLOADS[name]()
+    run_and_check(step, check_pool=(name != "long_context"))
+
+
+def test_long_context_pool_written_exactly():
+    step = synth.long_context()
+    ds = DeviceStep(step)
+    ds.slot_map()
+    ds.write()
+    slots, _, _ = oracle_step(step, rows=[])
+    assert np.array_equal(ds.slots_host(), slots)
+    pool = ds.pool_host()
+    # every written row is the input row; compare all blocks the step touches
+    blocks = np.unique(step.block_table[step.block_table >= 0])
+    expect = step.kv_cache[blocks].copy()
+    for t, s in enumerate(slots):
+        bi = np.searchsorted(blocks, s // 16)
+        expect[bi, 0, s % 16] = step.k[t]
+        expect[bi, 1, s % 16] = step.v[t]
+    assert np.array_equal(pool[blocks], expect)
+
+
+def test_mixed_step_parity():
+    step = synth.mixed_step()
+    run_and_check(step)
+
+
+# ---------------------------------------------------------------- split-KV
+@pytest.mark.parametrize("warps", [1, 3, 7, 64, 1000, 5000])
+def test_split_kv_partitionings(warps):
+    step = make_step([RequestSpec(L - 1, 1) for L in (1, 2, 15, 16, 17, 33, 100, 257, 1000,
+                                                       3001)],
+                     num_q_heads=8, num_kv_heads=2, head_dim=128, seed=40 + warps)
+    run_and_check(step, decode_warps=warps)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(4, 4, 128), (8, 4, 128), (16, 4, 128), (32, 4, 128),
+                                      (4, 4, 64), (8, 4, 64), (16, 4, 64), (64, 8, 64),
+                                      (12, 3, 128)])
+def test_decode_head_shapes(Hq, Hkv, D):
+    rng = np.random.default_rng(Hq * 100 + D)
+    lens = rng.integers(1, 700, size=23)
+    step = make_step([RequestSpec(int(L) - 1, 1) for L in lens], num_q_heads=Hq,
+                     num_kv_heads=Hkv, head_dim=D, seed=int(Hq + D))
+    run_and_check(step)
+    run_and_check(step, decode_warps=37)
+
+
+def test_decode_shuffled_order_same_rows():
+    rng = np.random.default_rng(7)
+    lens = rng.integers(20, 900, size=17)
+    specs = [RequestSpec(int(L) - 1, 1) for L in lens]
+    a = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=9)
+    run_and_check(a, decode_warps=50)
+
+
+def test_padding_rows_and_empty_requests():
+    # a request with no new tokens and trailing padding rows past the batch
+    specs = [RequestSpec(30, 1), RequestSpec(12, 0), RequestSpec(64, 1)]
+    step = make_step(specs, num_q_heads=8, num_kv_heads=2, head_dim=64, seed=5)
+    ds = DeviceStep(step)
+    T = step.num_tokens
+    pad = 3
+    # grow the token arrays by padding rows
+    ds.q = torch.cat([ds.q, torch.zeros((pad,) + tuple(ds.q.shape[1:]), dtype=ds.q.dtype,
+                                        device=ds.q.device)])
+    ds.out = torch.full((T + pad, 8, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    ds.slot_mapping = torch.empty(T + pad, dtype=torch.int64, device="cuda")
+    ds.k = torch.cat([ds.k, torch.zeros((pad, 2, 64), dtype=ds.k.dtype, device="cuda")])
+    ds.v = torch.cat([ds.v, torch.zeros((pad, 2, 64), dtype=ds.v.dtype, device="cuda")])
+    ds.run()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_errors(clear=True) == 0
+    slots = ds.slots_host()
+    assert (slots[T:] == -1).all()
+    ref_slots, pool, ref = oracle_step(step)
+    assert np.array_equal(slots[:T], ref_slots)
+    assert np.array_equal(ds.pool_host(), pool)
+    out = ds.out_host()
+    assert_close(out[:T], ref)
+    assert (out[T:] == 0x40E0).all()  # padding rows untouched (7.0 in bf16)
+
+
+def test_empty_batch_is_a_no_op():
+    step = make_step([RequestSpec(5, 1)], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=1)
+    ds = DeviceStep(step)
+    lay = ds.layout
+    lib = binding.load()
+    assert lib.pkv_paged_attention(None, None, 0, None, None, 0, None, None, None, 0, 0, 0, 0,
+                                   4, 1.0, lay, None, 0, None, None) == 0
+    assert lib.pkv_paged_kv_write(None, None, None, 0, 0, None, 0, lay, None) == 0
+
+
+# ---------------------------------------------------------------- bad data
+def test_out_of_range_slot_is_skipped_and_flagged():
+    step = make_step([RequestSpec(3, 2)], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=2)
+    ds = DeviceStep(step)
+    before = ds.pool_host()
+    bad = torch.tensor([step.num_blocks * 16 + 5, -1], dtype=torch.int64, device="cuda")
+    binding.pkv_paged_kv_write(ds.kv_cache, ds.k, ds.v, bad)
+    flags = binding.pkv_get_device_errors(clear=True)
+    assert flags & binding.DEVERR_SLOT_RANGE
+    assert np.array_equal(ds.pool_host(), before)
+
+
+def test_bad_block_id_is_masked_and_flagged():
+    step = make_step([RequestSpec(40, 1), RequestSpec(20, 1)], num_q_heads=4, num_kv_heads=2,
+                     head_dim=64, seed=3)
+    ds = DeviceStep(step)
+    ds.slot_map()
+    ds.write()
+    bt = ds.block_table.clone()
+    bt[0, 0] = step.num_blocks + 100  # outside the pool
+    ds.block_table = bt
+    ds.attend()
+    flags = binding.pkv_get_device_errors(clear=True)
+    assert flags & binding.DEVERR_BLOCK_RANGE
+    # request 1 is untouched by the bad entry of request 0
+    _, _, ref = oracle_step(step)
+    assert_close(ds.out_host()[1:], ref[1:])
+
+
+def test_inconsistent_lengths_are_flagged():
+    step = make_step([RequestSpec(10, 1)], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=4)
+    ds = DeviceStep(step)
+    ds.slot_map()
+    ds.write()
+    ds.seq_lens = ds.seq_lens + 1  # no longer num_computed + query_len
+    ds.attend()
+    assert binding.pkv_get_device_errors(clear=True) & binding.DEVERR_LENGTHS
