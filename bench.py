@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Benchmark of one mixed continuous-batching step of paged attention.
+
+One step = the whole hot path on one batch: slot mapping, the cache write of
+every new token, and attention of every query row (split-KV decode + combine
+for decode rows, tensor-core prefill for chunk rows), through the C ABI.
+
+Default workload (one layer, Llama-3-8B shapes: 32 q / 8 kv heads, d=128,
+bf16, block size 16): a 512-token prefill chunk over 1536 cached tokens,
+8 fresh 64-token prefills and 1280 decodes with contexts uniform in
+[128, 2048] -- 2304 new tokens, about 5.7 GB of K/V read per step, so the
+inputs are far larger than L2 and no flush is needed.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle on
+a bounded per-step sample of the same workload instead.
+"""
+
+import os
+
+# The CPU oracle runs single-threaded so that its core count is exact.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import re  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_hkv_gb300 import synth  # noqa: E402
+
+METRIC = "mixed-step attention tokens/s per layer"
+UNIT = "tokens/s"
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--workload", default="mixed_step", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--seed", type=int, default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ work
+def step_work(step):
+    """Algorithmic bytes and flops of one step.
+
+    decode_kv_bytes: K and V rows each decode row reads once (L * Hkv * D * 2
+    bytes each); prefill_flops: 4 * D * Hq per causal (query, key) pair
+    (QK^T and PV); write_bytes: each new token's K and V rows read and
+    written."""
+    D, Hq, Hkv = step.head_dim, step.num_q_heads, step.num_kv_heads
+    dec = step.query_len == 1
+    decode_kv = int(step.seq_lens[dec].astype(np.int64).sum()) * Hkv * D * 2 * 2
+    pairs = 0
+    for c, n in zip(step.num_computed[~dec], step.query_len[~dec]):
+        c, n = int(c), int(n)
+        pairs += n * c + n * (n + 1) // 2
+    return {
+        "decode_kv_bytes": decode_kv,
+        "decode_rows": int(dec.sum()),
+        "prefill_pairs": pairs,
+        "prefill_flops": 4 * D * Hq * pairs,
+        "write_bytes": 2 * step.num_tokens * Hkv * D * 2 * 2,
+        "tokens": step.num_tokens,
+    }
+
+
+def kernels_per_step(step):
+    return 1 + 1 + 1 + (1 if step.max_query_len > 1 else 0) + 2
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.sel = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = []
+
+    def start(self):
+        cmd = ["nvidia-smi"] + self.sel + [f"--query-gpu={self.FIELDS}",
+                                           "--format=csv,noheader,nounits", "-lms", "50"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.06)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ oracle timing
+def stratified_sample(step_specs, seed, per_class):
+    """Specs of a bounded sample: rows drawn from each class of request
+    (the long chunk, the fresh prefills, the decodes) and the factor that
+    scales each class's time to the whole step."""
+    rng = np.random.default_rng(seed + 1000)
+    classes = {}
+    for i, s in enumerate(step_specs):
+        key = "decode" if s.query_len == 1 else ("chunk" if s.num_computed > 0 else "prefill")
+        classes.setdefault(key, []).append(i)
+    plan = []
+    for key, idx in classes.items():
+        total_rows = sum(step_specs[i].query_len for i in idx)
+        if key == "decode":
+            take = list(rng.choice(idx, size=min(per_class["decode"], len(idx)), replace=False))
+            rows = [(i, 0) for i in take]
+        else:
+            i = int(rng.choice(idx))
+            n = step_specs[i].query_len
+            rr = sorted(rng.choice(n, size=min(per_class[key], n), replace=False))
+            rows = [(i, int(x)) for x in rr]
+        plan.append((key, rows, total_rows / len(rows)))
+    return plan
+
+
+def time_oracle_sample(step_specs, shape, seed, per_class):
+    """Time the oracle (slot mapping, write, attention) on a stratified
+    sample; returns (estimated seconds for the whole step, description)."""
+    import oracle
+    plan = stratified_sample(step_specs, seed, per_class)
+    total = 0.0
+    desc = []
+    for key, rows, scale in plan:
+        reqs = sorted({i for i, _ in rows})
+        sub_specs = [step_specs[i] for i in reqs]
+        sub = synth.make_step(sub_specs, seed=seed, **shape)
+        pos = {i: k for k, i in enumerate(reqs)}
+        sel = [int(sub.query_start_loc[pos[i]]) + j for i, j in rows]
+        t0 = time.perf_counter()
+        slots = oracle.slot_mapping(sub.block_table, sub.query_start_loc, sub.num_computed)
+        pool = oracle.kv_write(sub.kv_cache, sub.k, sub.v, slots)
+        oracle.paged_attention(sub.q, pool, sub.block_table, sub.seq_lens, sub.query_start_loc,
+                               sub.num_computed, sub.scale, rows=sel)
+        dt = time.perf_counter() - t0
+        total += dt * scale
+        desc.append(f"{len(rows)} {key} rows x{scale:.0f}")
+    return total, "; ".join(desc)
+
+
+def shape_of(step):
+    return dict(num_q_heads=step.num_q_heads, num_kv_heads=step.num_kv_heads,
+                head_dim=step.head_dim)
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    seed = args.seed if args.seed is not None else {"mixed_step": 3}.get(args.workload, 0)
+    meta = synth.WORKLOADS[args.workload](seed=seed, materialize=False)
+    shape = shape_of(meta)
+    per = {"decode": 4, "chunk": 8, "prefill": 4}
+    for w in range(args.warmup):
+        time_oracle_sample(meta.specs, shape, seed + w, per)
+    est = []
+    desc = ""
+    for k in range(args.steps):
+        t, desc = time_oracle_sample(meta.specs, shape, seed + 100 + k, per)
+        est.append(t)
+    sec = float(np.mean(est))
+    value = meta.num_tokens / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "tokens_per_step": meta.num_tokens},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "per step: " + desc + " (step time extrapolated by class)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ native arm
+def traffic_from_profile(kernel_src):
+    """DRAM traffic per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_mixed_step.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m and t):
+        return None
+    with open(kernel_src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != m.group(1):
+            return None
+    return float(t.group(1))
+
+
+def run_native(args):
+    import torch
+
+    from paged_kv_cache_hkv_gb300 import binding
+    from paged_kv_cache_hkv_gb300.runner import DeviceStep
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the native arm has no CPU path)")
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+
+    base_seed = args.seed if args.seed is not None else {"mixed_step": 3, "tiny_decode": 1,
+                                                         "llama_decode": 2, "prefix_sharing": 4,
+                                                         "long_context": 5}[args.workload]
+    seed = base_seed + rank  # replicas: each rank its own batch
+    step = synth.WORKLOADS[args.workload](seed=seed)
+    ds = DeviceStep(step)
+    binding.pkv_get_device_errors(clear=True)
+    work = step_work(step)
+    stream = torch.cuda.current_stream()
+
+    def sync_all():
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        ds.run()
+    torch.cuda.synchronize()
+    flags = binding.pkv_get_device_errors(clear=True)
+    if flags:
+        raise SystemExit(f"device error flags {flags:#x} during warm-up")
+
+    K = args.steps
+    trace = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.PKV_TRACE_EVENTS)]
+             for _ in range(K)]
+    for ev in trace:  # torch creates the CUDA event on its first record
+        for e in ev:
+            e.record(stream)
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sync_all()
+    sampler.start()
+    time.sleep(0.15)
+    t_start.record(stream)
+    s = ds.step
+    for k in range(K):
+        ds.slot_map()
+        ds.write()
+        binding.pkv_paged_attention(
+            ds.out, ds.q, ds.kv_cache, ds.block_table, ds.seq_lens, ds.query_start_loc,
+            ds.num_computed, max_query_len=s.max_query_len, max_seq_len=s.max_seq_len,
+            scale=s.scale, workspace=ds.workspace, trace_events=trace[k])
+    t_stop.record(stream)
+    sync_all()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_stop)
+    per_kernel = np.zeros(binding.PKV_TRACE_EVENTS - 1)
+    for ev in trace:
+        for i in range(binding.PKV_TRACE_EVENTS - 1):
+            per_kernel[i] += ev[i].elapsed_time(ev[i + 1])
+    per_kernel /= K  # ms per launch: plan, prefill, decode, combine
+    if pg is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = work["tokens"] * world / (ms_per_step * 1e-3)
+    flags = binding.pkv_get_device_errors(clear=True)
+    if flags:
+        raise SystemExit(f"device error flags {flags:#x} in the timed region")
+
+    # ---- end to end: host inputs in, host output out, every step
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        host_in = [(pin(t), t) for t in (ds.q, ds.k, ds.v, ds.block_table, ds.seq_lens,
+                                         ds.query_start_loc, ds.num_computed)]
+        host_out = torch.empty(ds.out.shape, dtype=ds.out.dtype, pin_memory=True)
+        h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+        d2h = host_out.numel() * host_out.element_size()
+        sync_all()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            for h, d in host_in:
+                d.copy_(h, non_blocking=True)
+            ds.run()
+            host_out.copy_(ds.out, non_blocking=True)
+        e1.record(stream)
+        sync_all()
+        e2e_ms = e0.elapsed_time(e1)
+        if pg is not None:
+            t = torch.tensor([e2e_ms], device="cuda")
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": work["tokens"] * world / (e2e_ms / K * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # ---- roofline of the dominant kernel (decode)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        hbm_peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        hbm_peak, peak_src = 6800.0, "fallback"
+    dec_ms = per_kernel[2]
+    dec_gbs = work["decode_kv_bytes"] / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
+    traffic = traffic_from_profile(os.path.join(ROOT, "paged_kv_cache_hkv_gb300", "csrc",
+                                                "decode.cu"))
+    roofline = {"kernel": "decode_kernel", "bound": "hbm", "achieved": dec_gbs,
+                "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
+                "frac": dec_gbs / hbm_peak if dec_gbs else None, "traffic": traffic,
+                "algorithmic_bytes_per_launch": work["decode_kv_bytes"]}
+    pf_ms = per_kernel[1]
+    tc_peak = float(peaks.get("bf16_tflops", 1900.0))
+    prefill = None
+    if work["prefill_flops"] and pf_ms > 0:
+        tf = work["prefill_flops"] / (pf_ms * 1e-3) / 1e12
+        prefill = {"kernel": "prefill_kernel", "bound": "tensor", "achieved": tf,
+                   "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
+                   "algorithmic_flops_per_launch": work["prefill_flops"]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec, desc = time_oracle_sample(step.specs, shape_of(step), seed,
+                                       {"decode": 64, "chunk": 64, "prefill": 64})
+        cpu = {"value": work["tokens"] / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": desc + "; step time extrapolated by class"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "tokens_per_step": work["tokens"],
+                   "requests": step.num_reqs, "decode_rows": work["decode_rows"],
+                   "heads": f"{step.num_q_heads}q/{step.num_kv_heads}kv", "head_dim": step.head_dim,
+                   "block_size": step.block_size, "pool_blocks": step.num_blocks,
+                   "decode_kv_bytes_per_step": work["decode_kv_bytes"],
+                   "prefill_flops_per_step": work["prefill_flops"],
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "decode_kv_read_gbs": dec_gbs,
+        "kernel_ms": {"plan": per_kernel[0], "prefill": per_kernel[1],
+                      "decode": per_kernel[2], "combine": per_kernel[3]},
+        "roofline": roofline,
+        "prefill_roofline": prefill,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * kernels_per_step(step),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

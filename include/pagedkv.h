@@ -68,14 +68,24 @@ typedef struct pkv_cache_layout {
   int32_t head_dim;     /* 64 or 128                                          */
 } pkv_cache_layout;
 
-/* Optional tuning of pkv_paged_attention; pass NULL for the defaults. */
+/* Optional tuning and tracing of pkv_paged_attention; pass NULL for the
+ * defaults. */
 typedef struct pkv_attention_options {
   /* Decode warps that split the step's decode KV stream between them
    * (split-KV). 0 = one full wave of the device. A single warp means no
    * split at all; tests use other values to vary the partitioning. */
   int32_t decode_warps;
   int32_t reserved[7]; /* must be zero */
+  /* Tracing: NULL, or PKV_TRACE_EVENTS cudaEvent_t handles (as void*) owned
+   * by the caller. The call records them on `stream` around its kernels:
+   * [0] before the plan kernel, [1] before the prefill kernel, [2] before
+   * the decode kernel, [3] before the combine kernel, [4] after it.
+   * Consecutive pairs bracket one kernel each (an empty bracket when a
+   * kernel is not needed). */
+  void** trace_events;
 } pkv_attention_options;
+
+#define PKV_TRACE_EVENTS 5
 
 /* Library version (PKV_ABI_VERSION). */
 int32_t pkv_abi_version(void);

@@ -32,8 +32,12 @@ class pkv_cache_layout(ctypes.Structure):
                 ("head_dim", c_i32)]
 
 
+PKV_TRACE_EVENTS = 5
+
+
 class pkv_attention_options(ctypes.Structure):
-    _fields_ = [("decode_warps", c_i32), ("reserved", c_i32 * 7)]
+    _fields_ = [("decode_warps", c_i32), ("reserved", c_i32 * 7),
+                ("trace_events", ctypes.POINTER(c_void_p))]
 
 
 _SIGNATURES = {
@@ -152,11 +156,20 @@ def pkv_paged_kv_write(kv_cache, key, value, slot_mapping, stream=None):
         _ptr(slot_mapping), key.shape[0], lay, _stream(stream)))
 
 
-def _options(decode_warps):
-    if decode_warps is None:
+def _options(decode_warps, trace_events=None):
+    if decode_warps is None and trace_events is None:
         return None
     o = pkv_attention_options()
-    o.decode_warps = int(decode_warps)
+    o.decode_warps = int(decode_warps or 0)
+    if trace_events is not None:
+        if len(trace_events) != PKV_TRACE_EVENTS:
+            raise ValueError(f"trace_events needs {PKV_TRACE_EVENTS} torch.cuda.Event")
+        handles = [e.cuda_event for e in trace_events]
+        if not all(handles):
+            raise ValueError("trace events must be created (recorded once) before use")
+        arr = (c_void_p * PKV_TRACE_EVENTS)(*[c_void_p(h) for h in handles])
+        o.trace_events = ctypes.cast(arr, ctypes.POINTER(c_void_p))
+        o._keep = arr
     return ctypes.pointer(o)
 
 
@@ -173,8 +186,12 @@ def pkv_attention_workspace_size(num_reqs: int, num_q_heads: int, kv_cache,
 
 def pkv_paged_attention(out, q, kv_cache, block_table, seq_lens, query_start_loc,
                         num_computed_tokens, *, max_query_len: int, max_seq_len: int,
-                        scale: float, workspace, decode_warps=None, stream=None):
-    """out [T, Hq, D] bf16 <- attention of one mixed step (see pagedkv.h)."""
+                        scale: float, workspace, decode_warps=None, trace_events=None,
+                        stream=None):
+    """out [T, Hq, D] bf16 <- attention of one mixed step (see pagedkv.h).
+
+    trace_events: optional list of PKV_TRACE_EVENTS torch.cuda.Event (created
+    with enable_timing=True) recorded around the call's kernels."""
     for t, n in ((out, "out"), (q, "q"), (kv_cache, "kv_cache")):
         _require(t, torch.bfloat16, n)
     for t, n in ((block_table, "block_table"), (seq_lens, "seq_lens"),
@@ -191,7 +208,7 @@ def pkv_paged_attention(out, q, kv_cache, block_table, seq_lens, query_start_loc
         block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), _ptr(num_computed_tokens),
         seq_lens.shape[0], q.shape[0], int(max_query_len), int(max_seq_len), q.shape[1],
         float(scale), lay, _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _options(decode_warps), _stream(stream)))
+        _options(decode_warps, trace_events), _stream(stream)))
     return out
 
 

@@ -336,7 +336,13 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   if (st != PKV_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pkv::launch_plan(a, ws, s);
+  void** ev = options ? options->trace_events : nullptr;
+  auto mark = [&](int i) -> cudaError_t {
+    return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
+  };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = pkv::launch_plan(a, ws, s);
+  if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   if (max_query_len > 1) {
     // pool for the tensor-core path: 64-element (128-byte) swizzled rows
@@ -353,7 +359,9 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
-  e = pkv::launch_decode(a, ws, kv_map, static_cast<int>(warps), s);
+  e = mark(2);
+  if (e == cudaSuccess) e = pkv::launch_decode(a, ws, kv_map, static_cast<int>(warps), s, ev);
+  if (e == cudaSuccess) e = mark(4);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
 }

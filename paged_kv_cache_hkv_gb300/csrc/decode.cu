@@ -600,7 +600,7 @@ cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t
 
 template <int D, int GW>
 static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_map,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, void** trace) {
   auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps>;
   const size_t smem = decode_smem_bytes<D, GW>();
   cudaError_t e =
@@ -609,6 +609,7 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_
   const long long grid = (p.warps + kDecodeWarps - 1) / kDecodeWarps;
   kern<<<static_cast<unsigned>(grid), kDecodeWarps * 32, smem, stream>>>(kv_map, p);
   e = cudaGetLastError();
+  if (e == cudaSuccess && trace) e = cudaEventRecord(static_cast<cudaEvent_t>(trace[3]), stream);
   if (e != cudaSuccess) return e;
   const int items = p.num_reqs * p.virt_heads * GW;
   combine_kernel<D, GW><<<(items + 3) / 4, 128, 0, stream>>>(p, items);
@@ -616,7 +617,7 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
-                          int decode_warps, cudaStream_t stream) {
+                          int decode_warps, cudaStream_t stream, void** trace) {
   const int group = a.num_q_heads / a.num_kv_heads;
   const int gw = decode_heads_per_warp(group);
   DecodeParams p;
@@ -638,12 +639,12 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUte
   p.hdr = ws.hdr;
   p.part_ml = ws.part_ml;
   p.part_o = ws.part_o;
-  if (a.head_dim == 128 && gw == 4) return launch_decode_t<128, 4>(p, kv_map, stream);
-  if (a.head_dim == 128 && gw == 2) return launch_decode_t<128, 2>(p, kv_map, stream);
-  if (a.head_dim == 128 && gw == 1) return launch_decode_t<128, 1>(p, kv_map, stream);
-  if (a.head_dim == 64 && gw == 4) return launch_decode_t<64, 4>(p, kv_map, stream);
-  if (a.head_dim == 64 && gw == 2) return launch_decode_t<64, 2>(p, kv_map, stream);
-  if (a.head_dim == 64 && gw == 1) return launch_decode_t<64, 1>(p, kv_map, stream);
+  if (a.head_dim == 128 && gw == 4) return launch_decode_t<128, 4>(p, kv_map, stream, trace);
+  if (a.head_dim == 128 && gw == 2) return launch_decode_t<128, 2>(p, kv_map, stream, trace);
+  if (a.head_dim == 128 && gw == 1) return launch_decode_t<128, 1>(p, kv_map, stream, trace);
+  if (a.head_dim == 64 && gw == 4) return launch_decode_t<64, 4>(p, kv_map, stream, trace);
+  if (a.head_dim == 64 && gw == 2) return launch_decode_t<64, 2>(p, kv_map, stream, trace);
+  if (a.head_dim == 64 && gw == 1) return launch_decode_t<64, 1>(p, kv_map, stream, trace);
   return cudaErrorInvalidValue;
 }
 

@@ -64,8 +64,10 @@ cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t
 // Decode warps in one full wave on this device for the given shape.
 cudaError_t decode_full_wave_warps(int head_dim, int group, int num_sms, int* warps);
 
+// trace: NULL or the caller's event array; event [3] is recorded between the
+// decode and the combine kernel.
 cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
-                          int decode_warps, cudaStream_t stream);
+                          int decode_warps, cudaStream_t stream, void** trace);
 
 cudaError_t launch_prefill(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
                            const CUtensorMap& q_map, int num_sms, cudaStream_t stream);

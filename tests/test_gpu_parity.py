@@ -176,3 +176,58 @@ def test_inconsistent_lengths_are_flagged():
     ds.seq_lens = ds.seq_lens + 1  # no longer num_computed + query_len
     ds.attend()
     assert binding.pkv_get_device_errors(clear=True) & binding.DEVERR_LENGTHS
+
+
+# ---------------------------------------------------------------- prefill (tensor cores)
+PREFILL_SPECS = [RequestSpec(0, 2), RequestSpec(15, 3), RequestSpec(16, 17), RequestSpec(17, 100),
+                 RequestSpec(200, 129), RequestSpec(1, 1), RequestSpec(33, 300),
+                 RequestSpec(127, 1), RequestSpec(0, 128), RequestSpec(250, 64)]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (8, 8, 128), (16, 8, 128), (64, 8, 128),
+                                      (8, 4, 64), (8, 8, 64), (16, 2, 64), (32, 4, 64)])
+def test_prefill_mixed_shapes(Hq, Hkv, D):
+    step = make_step(PREFILL_SPECS, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                     seed=Hq * 7 + D)
+    run_and_check(step)
+
+
+def test_prefill_chunks_match_one_shot_on_gpu():
+    """A prompt split into chunks over three steps gives the rows of the
+    one-shot prefill (each chunk attends the cached prefix plus itself)."""
+    full = make_step([RequestSpec(0, 400)], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                     seed=77, shuffle_pool=True)
+    ds = DeviceStep(full)
+    ds.run()
+    one_shot = ds.out_host().copy()
+    for c, n in ((0, 150), (150, 131), (281, 119)):
+        step = make_step([RequestSpec(c, n)], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                         seed=77)
+        # reuse the one-shot pool, table and rows: the cache already holds
+        # every token of the prompt after the one-shot write
+        q = ds.q[c:c + n].contiguous()
+        out = torch.zeros_like(q)
+        qsl = torch.tensor([0, n], dtype=torch.int32, device="cuda")
+        sl = torch.tensor([c + n], dtype=torch.int32, device="cuda")
+        nc = torch.tensor([c], dtype=torch.int32, device="cuda")
+        ws = torch.empty(binding.pkv_attention_workspace_size(1, 32, ds.layout), dtype=torch.uint8,
+                         device="cuda")
+        binding.pkv_paged_attention(out, q, ds.kv_cache, ds.block_table, sl, qsl, nc,
+                                    max_query_len=n, max_seq_len=c + n, scale=step.scale,
+                                    workspace=ws)
+        torch.cuda.synchronize()
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        a = got.view(np.uint16).astype(np.uint32) << 16
+        b = one_shot[c:c + n].astype(np.uint32) << 16
+        diff = np.abs(a.view(np.float32) - b.view(np.float32))
+        assert diff.max() <= 2e-2, diff.max()
+    assert binding.pkv_get_device_errors(clear=True) == 0
+
+
+def test_mixed_batch_order_independence():
+    specs = [RequestSpec(40, 24), RequestSpec(300, 1), RequestSpec(0, 37), RequestSpec(17, 1),
+             RequestSpec(5, 200), RequestSpec(999, 1)]
+    step = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=61)
+    run_and_check(step)
+    rev = make_step(specs[::-1], num_q_heads=32, num_kv_heads=8, head_dim=128, seed=61)
+    run_and_check(rev, decode_warps=9)
