@@ -48,6 +48,9 @@ extern "C" {
 #define PKV_ERR_WORKSPACE (-5)    /* workspace missing or too small          */
 #define PKV_ERR_CUDA (-6)         /* a CUDA runtime / driver call failed     */
 #define PKV_ERR_DEVICE (-7)       /* the current device is not sm_103        */
+#define PKV_ERR_SCRATCH_LIMIT (-8) /* the call needs more scratch than the
+                                      library's built-in array holds (see
+                                      pkv_paged_attention_static_workspace)    */
 
 /* bits of the sticky device error word */
 #define PKV_DEVERR_SLOT_RANGE 0x1u  /* slot >= num_blocks * block_size: row skipped */
@@ -198,6 +201,46 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride,
                             pkv_cache_layout layout, void* workspace,
                             size_t workspace_bytes,
                             const pkv_attention_options* options, void* stream);
+
+/*
+ * pkv_paged_attention_static_workspace -- pkv_paged_attention for callers
+ * that cannot allocate device memory. The pages have no counterpart to this
+ * entry point; it exists for how the library is called, not for what it
+ * computes.
+ *
+ * Some callers have no way to hand the library a workspace: a server that
+ * gave all device memory to its own caching allocator and KV pool at start-up
+ * and may not call cudaMalloc afterwards, a plugin inside a host framework
+ * that forbids raw device allocations, or a plain C caller with no allocator
+ * at all. This call takes the same arguments as pkv_paged_attention except the
+ * workspace, and uses instead one scratch array compiled into the library:
+ * PKV_STATIC_WORKSPACE_BYTES of device memory that every GPU which loads the
+ * library holds until the process exits. It never calls cudaMalloc, cudaFree
+ * or any allocating routine.
+ *
+ * - Size limit: if the call would need more scratch than the array holds
+ *   (pkv_attention_workspace_size() > PKV_STATIC_WORKSPACE_BYTES) it returns
+ *   PKV_ERR_SCRATCH_LIMIT and enqueues nothing. With the default options the
+ *   Llama-3-8B layer shape (32 q / 8 kv heads, d = 128) fits about 1860
+ *   requests per call on a 152-SM GB300.
+ * - First call per device: it looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make this first call
+ *   before any stream capture.
+ * - Shared state: every call on a device uses the same array and leaves its
+ *   contents behind. Nothing needs to start at zero (each call re-plans the
+ *   whole scratch area first). Calls whose kernels overlap on the GPU (on
+ *   different streams, or from different threads) race on the array and give
+ *   wrong results: keep them ordered, e.g. on one stream.
+ */
+#define PKV_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+
+int32_t pkv_paged_attention_static_workspace(
+    void* out, const void* q, int64_t q_row_stride, const void* kv_cache,
+    const int32_t* block_table, int32_t max_blocks_per_req, const int32_t* seq_lens,
+    const int32_t* query_start_loc, const int32_t* num_computed_tokens, int32_t num_reqs,
+    int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+    float scale, pkv_cache_layout layout, const pkv_attention_options* options,
+    void* stream);
 
 /*
  * pkv_get_device_errors -- checked path: synchronise `stream`, then return

@@ -21,6 +21,7 @@ c_i32, c_i64, c_u32, c_void_p, c_size_t, c_float = (
     ctypes.c_float)
 
 PKV_OK = 0
+PKV_ERR_SCRATCH_LIMIT = -8
 DEVERR_SLOT_RANGE = 0x1
 DEVERR_BLOCK_RANGE = 0x2
 DEVERR_LENGTHS = 0x4
@@ -55,6 +56,10 @@ _SIGNATURES = {
                                     c_i32, c_float, pkv_cache_layout, c_void_p, c_size_t,
                                     ctypes.POINTER(pkv_attention_options), c_void_p]),
     "pkv_get_device_errors": (c_i32, [ctypes.POINTER(c_u32), c_i32, c_void_p]),
+    "pkv_paged_attention_static_workspace": (
+        c_i32, [c_void_p, c_void_p, c_i64, c_void_p, c_void_p, c_i32, c_void_p, c_void_p,
+                c_void_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_float, pkv_cache_layout,
+                ctypes.POINTER(pkv_attention_options), c_void_p]),
 }
 
 _lib = None
@@ -218,3 +223,28 @@ def pkv_get_device_errors(clear: bool = True, stream=None) -> int:
     _check("pkv_get_device_errors",
            load().pkv_get_device_errors(ctypes.byref(v), int(clear), _stream(stream)))
     return int(v.value)
+
+
+def pkv_paged_attention_static_workspace(out, q, kv_cache, block_table, seq_lens,
+                                         query_start_loc, num_computed_tokens, *,
+                                         max_query_len: int, max_seq_len: int, scale: float,
+                                         decode_warps=None, stream=None):
+    """pkv_paged_attention without a caller workspace: for callers that cannot
+    allocate device memory, the library uses its built-in scratch array (see
+    pagedkv.h for the size limit and the one-stream rule)."""
+    for t, n in ((out, "out"), (q, "q"), (kv_cache, "kv_cache")):
+        _require(t, torch.bfloat16, n)
+    for t, n in ((block_table, "block_table"), (seq_lens, "seq_lens"),
+                 (query_start_loc, "query_start_loc"),
+                 (num_computed_tokens, "num_computed_tokens")):
+        _require(t, torch.int32, n)
+    if not out.is_contiguous() or not block_table.is_contiguous():
+        raise ValueError("out and block_table must be contiguous")
+    if q.dim() != 3 or q.stride(2) != 1 or q.stride(1) != q.shape[2]:
+        raise ValueError("q must be [T, Hq, D] with contiguous rows")
+    _check("pkv_paged_attention_static_workspace", load().pkv_paged_attention_static_workspace(
+        _ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), _ptr(num_computed_tokens),
+        seq_lens.shape[0], q.shape[0], int(max_query_len), int(max_seq_len), q.shape[1],
+        float(scale), layout_of(kv_cache), _options(decode_warps), _stream(stream)))
+    return out

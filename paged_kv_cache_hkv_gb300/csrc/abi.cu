@@ -184,6 +184,8 @@ const char* pkv_status_string(int32_t status) {
     case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case PKV_ERR_CUDA: return "CUDA call failed (see pkv_last_cuda_error)";
     case PKV_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    case PKV_ERR_SCRATCH_LIMIT:
+      return "call needs more scratch than the built-in static workspace holds";
     default: return "unknown status";
   }
 }
