@@ -112,7 +112,7 @@ int32_t check_layout(const pkv_cache_layout& l) {
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t hdr, dec_prefix, pf_req, pf_prefix, part_ml, part_o, total;
+  size_t hdr, dec_prefix, pf_req, pf_prefix, part_ml, part_o, bound, total;
 };
 
 WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long warps) {
@@ -131,6 +131,8 @@ WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long
   off += round256(static_cast<size_t>(slots) * gw * sizeof(float2));
   w.part_o = off;
   off += round256(static_cast<size_t>(slots) * gw * head_dim * sizeof(float));
+  w.bound = off;
+  off += round256(static_cast<size_t>(warps) * sizeof(int2));
   w.total = off;
   return w;
 }
@@ -308,6 +310,7 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   ws.pf_prefix = reinterpret_cast<int32_t*>(wsb + wl.pf_prefix);
   ws.part_ml = reinterpret_cast<float2*>(wsb + wl.part_ml);
   ws.part_o = reinterpret_cast<float*>(wsb + wl.part_o);
+  ws.bound = reinterpret_cast<int2*>(wsb + wl.bound);
 
   pkv::AttnArgs a;
   a.out = static_cast<uint16_t*>(out);

@@ -75,58 +75,60 @@ __device__ __forceinline__ Int3 block_exclusive_scan(Int3 v, Int3* total) {
   return Int3{base.a + inc.a - v.a, base.b + inc.b - v.b, base.c + inc.c - v.c};
 }
 
-// One CTA of 1024 threads walks the requests once: decode blocks per
-// request (prefix), the compact list of prefill requests and their work
-// items, and length checks.
+// Counts of one request: decode blocks, is-prefill, prefill work items.
+__device__ __forceinline__ Int3 plan_counts(const AttnArgs& a, int r, int tile_q, bool flag) {
+  Int3 v{0, 0, 0};
+  const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
+  const int n = q1 - q0, L = __ldg(a.seq_lens + r), c = __ldg(a.num_computed + r);
+  bool bad = n < 0 || q0 < 0 || q1 > a.num_tokens || c < 0 || L != c + n || (r == 0 && q0 != 0);
+  const long long nblk = (static_cast<long long>(L) + kBlockSize - 1) / kBlockSize;
+  if (!bad && n > 0 && nblk > a.max_blocks) bad = true;
+  if (bad) {
+    if (flag) atomicOr(&g_errors_decode, kErrLengths);
+  } else if (n == 1) {
+    v.a = static_cast<int>(nblk);
+  } else if (n > 1) {
+    v.b = 1;
+    v.c = ((n + tile_q - 1) / tile_q) * a.num_kv_heads;
+  }
+  return v;
+}
+
+// One CTA of 1024 threads, one pass: each thread takes a run of consecutive
+// requests, counts decode blocks, prefill requests and prefill work items,
+// and after one block scan writes the prefix sums and the compact list of
+// prefill requests. Requests with inconsistent lengths are skipped and
+// flagged.
 __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, AttnWorkspace ws, int tile_q) {
   __shared__ Int3 total;
-  __shared__ int carry_dec, carry_req, carry_items;
-  if (threadIdx.x == 0) {
-    carry_dec = carry_req = carry_items = 0;
-  }
-  __syncthreads();
   const int R = a.num_reqs;
-  for (int base = 0; base < R; base += 1024) {
-    const int r = base + threadIdx.x;
-    Int3 v{0, 0, 0};
-    if (r < R) {
-      const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
-      const int n = q1 - q0, L = __ldg(a.seq_lens + r), c = __ldg(a.num_computed + r);
-      bool bad = n < 0 || q0 < 0 || q1 > a.num_tokens || c < 0 || L != c + n ||
-                 (r == 0 && q0 != 0);
-      const long long nblk = (static_cast<long long>(L) + kBlockSize - 1) / kBlockSize;
-      if (!bad && n > 0 && nblk > a.max_blocks) bad = true;
-      if (bad) {
-        atomicOr(&g_errors_decode, kErrLengths);
-      } else if (n == 1) {
-        v.a = static_cast<int>(nblk);
-      } else if (n > 1) {
-        v.b = 1;
-        v.c = ((n + tile_q - 1) / tile_q) * a.num_kv_heads;
-      }
+  const int per = (R + 1023) / 1024;
+  const int r0 = min(R, static_cast<int>(threadIdx.x) * per), r1 = min(R, r0 + per);
+  Int3 sum{0, 0, 0};
+  for (int r = r0; r < r1; ++r) {
+    const Int3 v = plan_counts(a, r, tile_q, true);
+    sum.a += v.a;
+    sum.b += v.b;
+    sum.c += v.c;
+  }
+  Int3 run = block_exclusive_scan(sum, &total);
+  for (int r = r0; r < r1; ++r) {
+    const Int3 v = plan_counts(a, r, tile_q, false);
+    ws.dec_prefix[r] = run.a;
+    if (v.b) {
+      ws.pf_req[run.b] = r;
+      ws.pf_prefix[run.b] = run.c;
     }
-    const Int3 ex = block_exclusive_scan(v, &total);
-    if (r < R) {
-      ws.dec_prefix[r] = carry_dec + ex.a;
-      if (v.b) {
-        ws.pf_req[carry_req + ex.b] = r;
-        ws.pf_prefix[carry_req + ex.b] = carry_items + ex.c;
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      carry_dec += total.a;
-      carry_req += total.b;
-      carry_items += total.c;
-    }
-    __syncthreads();
+    run.a += v.a;
+    run.b += v.b;
+    run.c += v.c;
   }
   if (threadIdx.x == 0) {
-    ws.dec_prefix[R] = carry_dec;
-    ws.pf_prefix[carry_req] = carry_items;
-    ws.hdr[kHdrDecodeBlocks] = static_cast<uint32_t>(carry_dec);
-    ws.hdr[kHdrPrefillReqs] = static_cast<uint32_t>(carry_req);
-    ws.hdr[kHdrPrefillItems] = static_cast<uint32_t>(carry_items);
+    ws.dec_prefix[R] = total.a;
+    ws.pf_prefix[total.b] = total.c;
+    ws.hdr[kHdrDecodeBlocks] = static_cast<uint32_t>(total.a);
+    ws.hdr[kHdrPrefillReqs] = static_cast<uint32_t>(total.b);
+    ws.hdr[kHdrPrefillItems] = static_cast<uint32_t>(total.c);
     ws.hdr[kHdrPrefillNext] = 0u;
   }
 }
@@ -149,6 +151,7 @@ struct DecodeParams {
   const uint32_t* hdr;
   float2* part_ml;
   float* part_o;
+  int2* bound;  // [W]: (request, virtual head) holding the first position of each warp's range
 };
 
 // Warp that owns position x of the decode stream: ranges start at
@@ -184,29 +187,33 @@ struct DecodeCfg {
 
 enum : int { kFirst = 1, kLast = 2, kInvalid = 4, kEnd = 8 };
 
-// Reduce-scatter across the LPK lanes of a sub-group: on return v[0..)
-// holds full sums for score indices (li * NV / LPK) + i.
+// Reduce-scatter across the LPK lanes of a sub-group. The caller stores at
+// register position p the partial score of logical index p ^ (li * NV / LPK)
+// (lane-dependent order of q heads and keys), so at every halving stage the
+// lower half is the one this lane keeps and the upper half the one its
+// partner keeps: no selects. On return v[0..NPL) hold full sums for logical
+// indices (li * NV / LPK) + i.
 template <int N, int OFF>
 struct ReduceScatter {
-  static __device__ __forceinline__ void run(float* v, int li) {
+  static __device__ __forceinline__ void run(float* v) {
     if constexpr (OFF >= 1) {
       if constexpr (N >= 2) {
         constexpr int H = N / 2;
-        const bool upper = (li & OFF) != 0;
 #pragma unroll
-        for (int i = 0; i < H; ++i) {
-          const float send = upper ? v[i] : v[i + H];
-          const float keep = upper ? v[i + H] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
-        }
-        ReduceScatter<H, OFF / 2>::run(v, li);
+        for (int i = 0; i < H; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + H], OFF);
+        ReduceScatter<H, OFF / 2>::run(v);
       } else {
         v[0] += __shfl_xor_sync(0xffffffffu, v[0], OFF);
-        ReduceScatter<1, OFF / 2>::run(v, li);
+        ReduceScatter<1, OFF / 2>::run(v);
       }
     }
   }
 };
+
+// The running max of a head is only moved (and o, l rescaled) when a block's
+// max exceeds it by more than this many powers of two; in between, p may
+// reach 2^8, far inside fp32 range. The result is the same softmax.
+constexpr float kRescaleLog2 = 8.f;
 
 template <int D, int GW, int S, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
@@ -225,6 +232,21 @@ __global__ void __launch_bounds__(WARPS * 32)
   if (w >= W) return;
   const long long N = static_cast<long long>(p.virt_heads) * p.hdr[kHdrDecodeBlocks];
   const long long x0 = w * N / W, x1 = (w + 1) * N / W;
+
+  // ---------------- locate position x0: (request r, virtual head vg, block)
+  int r = -1, vg = 0, blk = 0, nblk = 0, L = 0, t = 0, out_slot = -1;
+  if (x0 < N) {
+    const long long u = x0 / p.virt_heads;
+    r = upper_index(p.dec_prefix, p.num_reqs, u);
+    const int pr = __ldg(p.dec_prefix + r);
+    nblk = __ldg(p.dec_prefix + r + 1) - pr;
+    const long long rem = x0 - static_cast<long long>(p.virt_heads) * pr;
+    vg = static_cast<int>(rem / nblk);
+    blk = static_cast<int>(rem - static_cast<long long>(vg) * nblk);
+  }
+  // the combine kernel finds split pairs from these records (warps with an
+  // empty range record the pair that holds their start too)
+  if (lane == 0) p.bound[w] = make_int2(r, vg);
   if (x0 >= x1) return;
 
   if (lane == 0) {
@@ -237,19 +259,9 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   // ---------------- producer state (identical in every lane)
   long long x = x0;
-  int r, vg, blk, nblk, L = 0, t = 0, out_slot = -1;
   bool new_piece = true;
-  {
-    const long long u = x0 / p.virt_heads;
-    r = upper_index(p.dec_prefix, p.num_reqs, u);
-    const int pr = __ldg(p.dec_prefix + r);
-    nblk = __ldg(p.dec_prefix + r + 1) - pr;
-    const long long rem = x0 - static_cast<long long>(p.virt_heads) * pr;
-    vg = static_cast<int>(rem / nblk);
-    blk = static_cast<int>(rem - static_cast<long long>(vg) * nblk);
-    L = __ldg(p.seq_lens + r);
-    t = __ldg(p.qsl + r);
-  }
+  L = __ldg(p.seq_lens + r);
+  t = __ldg(p.qsl + r);
   int win_r = -1, win_base = 0, win_val = -1;
 
   auto produce = [&](int s) {
@@ -316,11 +328,14 @@ __global__ void __launch_bounds__(WARPS * 32)
   };
 
   // ---------------- consumer state
-  float2 q2[GW][4];  // q * scale * log2(e), dims li*8 .. li*8+7 as pairs
-  float2 o2[GW][4];  // unnormalised output, same dims
+  // Position p of the per-block score registers holds logical index
+  // p ^ perm: q head (p / KPL) ^ perm_h, key slot (p % KPL) ^ perm_k.
+  const int perm = (li * C::NV) / C::LPK;
+  const int perm_h = perm / C::KPL, perm_k = perm % C::KPL;
+  const int hm = perm_h;  // head of this lane's full scores after the reduction
+  float2 q2[GW][4];  // q * scale * log2(e), position order (head hp ^ perm_h)
+  float2 o2[GW][4];  // unnormalised output, logical heads, dims li*8 .. li*8+7
   float m_run = -INFINITY, l_run = 0.f;  // for head hm of this lane
-  const int idx_base = (li * C::NV) / C::LPK;
-  const int hm = idx_base / C::KPL;
 
 #pragma unroll
   for (int s = 0; s < S; ++s) produce(s);
@@ -341,18 +356,18 @@ __global__ void __launch_bounds__(WARPS * 32)
     if (m0.w & kEnd) break;
     const int4 m1 = sm.meta1[s];
     const int flags = m0.w;
-    const uint32_t kv_base = smem_u32(&sm.kv[s][0][0]);
+    const uint32_t kv_base = smem_u32(&sm.kv[s][0][0]) + li * 16;
 
     if (flags & kFirst) {
       const uint32_t qa = smem_u32(&sm.q[s][0]) + li * 16;
 #pragma unroll
-      for (int h = 0; h < GW; ++h) {
-        const uint4 qv = ld_shared_v4(qa + h * D * 2);
+      for (int hp = 0; hp < GW; ++hp) {
+        const uint4 qv = ld_shared_v4(qa + (hp ^ perm_h) * D * 2);
         const uint32_t wd[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          q2[h][e] = make_float2(bf16_lo(wd[e]) * p.scale_log2, bf16_hi(wd[e]) * p.scale_log2);
-          o2[h][e] = make_float2(0.f, 0.f);
+          q2[hp][e] = make_float2(bf16_lo(wd[e]) * p.scale_log2, bf16_hi(wd[e]) * p.scale_log2);
+          o2[hp][e] = make_float2(0.f, 0.f);
         }
       }
       m_run = -INFINITY;
@@ -361,33 +376,32 @@ __global__ void __launch_bounds__(WARPS * 32)
     const bool bvalid = !(flags & kInvalid);
     const int nvalid = m1.x;
 
-    // ---- scores: acc[h * KPL + j] for key j*KPI + sub, partial over 8 dims
+    // ---- scores, partial over this lane's 8 dims
     float acc[C::NV];
 #pragma unroll
-    for (int j = 0; j < C::KPL; ++j) {
-      const int key = j * C::KPI + sub;
-      const uint4 kv4 = ld_shared_v4(kv_base + (key * D + li * 8) * 2);
+    for (int jp = 0; jp < C::KPL; ++jp) {
+      const int key = (jp ^ perm_k) * C::KPI + sub;
+      const uint4 kv4 = ld_shared_v4(kv_base + key * D * 2);
       const uint32_t wd[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
       float2 k2[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(wd[e]), bf16_hi(wd[e]));
 #pragma unroll
-      for (int h = 0; h < GW; ++h) {
+      for (int hp = 0; hp < GW; ++hp) {
         float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) a2 = ffma2(q2[h][e], k2[e], a2);
-        acc[h * C::KPL + j] = a2.x + a2.y;
+        for (int e = 0; e < 4; ++e) a2 = ffma2(q2[hp][e], k2[e], a2);
+        acc[hp * C::KPL + jp] = a2.x + a2.y;
       }
     }
-    ReduceScatter<C::NV, C::LPK / 2>::run(acc, li);
+    ReduceScatter<C::NV, C::LPK / 2>::run(acc);
 
     // ---- online softmax for head hm
     float sc[C::NPL];
     float lmax = -INFINITY;
 #pragma unroll
     for (int i = 0; i < C::NPL; ++i) {
-      const int jj = (idx_base + i) % C::KPL;
-      const int key = jj * C::KPI + sub;
+      const int key = ((perm + i) % C::KPL) * C::KPI + sub;
       sc[i] = (bvalid && key < nvalid) ? acc[i] : -INFINITY;
       lmax = fmaxf(lmax, sc[i]);
     }
@@ -397,21 +411,31 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
     for (int off = C::LPK; off < 32; off <<= 1)
       lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
-    const float m_new = fmaxf(m_run, lmax);
-    const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+    if (__any_sync(0xffffffffu, lmax > m_run + kRescaleLog2)) {
+      const float m_new = fmaxf(m_run, lmax);
+      const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+      l_run *= alpha;
+      m_run = m_new;
+      if (sub == 0 && (li % C::LPH) == 0) sm.hs[hm].x = alpha;
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < GW; ++h) {
+        const float a = sm.hs[h].x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(o2[h][e].x * a, o2[h][e].y * a);
+      }
+    }
     float psum = 0.f;
 #pragma unroll
     for (int i = 0; i < C::NPL; ++i) {
-      const float pv = (sc[i] == -INFINITY) ? 0.f : exp2f(sc[i] - m_new);
-      sm.p[sub][idx_base + i] = pv;
+      const float pv = (sc[i] == -INFINITY || m_run == -INFINITY) ? 0.f : exp2f(sc[i] - m_run);
+      sm.p[sub][perm + i] = pv;
       psum += pv;
     }
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-    if (sub == 0 && (li % C::LPH) == 0) sm.hs[hm].x = alpha;
+    l_run += psum;
     __syncwarp();
 
-    // ---- o = o * alpha + sum_j p_j v_j
+    // ---- o += sum_j p_j v_j
     {
       float pj[C::NV];
 #pragma unroll
@@ -422,29 +446,28 @@ __global__ void __launch_bounds__(WARPS * 32)
         pj[i + 2] = f.z;
         pj[i + 3] = f.w;
       }
-#pragma unroll
-      for (int h = 0; h < GW; ++h) {
-        const float a = sm.hs[h].x;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(o2[h][e].x * a, o2[h][e].y * a);
-      }
-#pragma unroll
-      for (int j = 0; j < C::KPL; ++j) {
+      auto pv_key = [&](int j) {
         const int key = j * C::KPI + sub;
-        if (bvalid && key < nvalid) {
-          const uint4 vv = ld_shared_v4(kv_base + ((16 + key) * D + li * 8) * 2);
-          const uint32_t wd[4] = {vv.x, vv.y, vv.z, vv.w};
-          float2 v2[4];
+        const uint4 vv = ld_shared_v4(kv_base + (16 + key) * D * 2);
+        const uint32_t wd[4] = {vv.x, vv.y, vv.z, vv.w};
+        float2 v2[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) v2[e] = make_float2(bf16_lo(wd[e]), bf16_hi(wd[e]));
+        for (int e = 0; e < 4; ++e) v2[e] = make_float2(bf16_lo(wd[e]), bf16_hi(wd[e]));
 #pragma unroll
-          for (int h = 0; h < GW; ++h) {
-            const float pp = pj[h * C::KPL + j];
-            const float2 p2 = make_float2(pp, pp);
+        for (int h = 0; h < GW; ++h) {
+          const float pp = pj[h * C::KPL + j];
+          const float2 p2 = make_float2(pp, pp);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o2[h][e] = ffma2(p2, v2[e], o2[h][e]);
-          }
+          for (int e = 0; e < 4; ++e) o2[h][e] = ffma2(p2, v2[e], o2[h][e]);
         }
+      };
+      if (bvalid && nvalid == kBlockSize) {
+#pragma unroll
+        for (int j = 0; j < C::KPL; ++j) pv_key(j);
+      } else {
+#pragma unroll
+        for (int j = 0; j < C::KPL; ++j)
+          if (bvalid && j * C::KPI + sub < nvalid) pv_key(j);
       }
     }
     __syncwarp();
@@ -500,53 +523,77 @@ __global__ void __launch_bounds__(WARPS * 32)
 }
 
 // ------------------------------------------------------------------ combine
-// One warp per (request, q head) whose kv head was split between warps.
+// One CTA per warp boundary w of the decode split, one warp per q head of
+// the pair. A (request, virtual head) pair is split when a boundary falls
+// strictly inside its blocks; the first such boundary is the one right after
+// the warp that owns the pair's first block, and that boundary's CTA merges
+// the pair's partials (one per non-empty warp range that touched it):
+//   M = max_p m_p,  o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p.
+// Lanes first read the (m, l) of up to 32 pieces at once, then every lane
+// sums its dims over the pieces with independent loads.
 template <int D, int GW>
-__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int num_items) {
-  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (gw >= num_items) return;
-  const int h = gw % GW;
-  const int rv = gw / GW;
-  const int vg = rv % p.virt_heads, r = rv / p.virt_heads;
+__global__ void __launch_bounds__(GW * 32) combine_kernel(const DecodeParams p) {
+  const long long w = blockIdx.x;
+  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long W = p.warps;
+  if (w < 1 || w >= W) return;
+  const int2 rec = p.bound[w];
+  if (rec.x < 0) return;
+  const int r = rec.x, vg = rec.y;
   const int pr = __ldg(p.dec_prefix + r);
   const int nblk = __ldg(p.dec_prefix + r + 1) - pr;
-  if (nblk == 0) return;
-  const long long W = p.warps;
   const long long N = static_cast<long long>(p.virt_heads) * p.hdr[kHdrDecodeBlocks];
   const long long a = static_cast<long long>(p.virt_heads) * pr + static_cast<long long>(vg) * nblk;
-  const long long wf = owner_warp(a, N, W), wl = owner_warp(a + nblk - 1, N, W);
-  if (wf == wl) return;
+  const long long wf = owner_warp(a, N, W);
+  if (wf != w - 1) return;
+  const int npieces = static_cast<int>(owner_warp(a + nblk - 1, N, W) - wf + 1);
+  const long long base = static_cast<long long>(r) * p.virt_heads + vg + wf;  // slot of piece 0
+
+  // (m, l) of piece j; empty warp ranges wrote nothing and weigh zero
+  auto piece_ml = [&](int j) -> float2 {
+    const long long ww = wf + j;
+    if (j >= npieces || ww * N / W == (ww + 1) * N / W) return make_float2(-INFINITY, 0.f);
+    return p.part_ml[(base + j) * GW + h];
+  };
+  float M = -INFINITY;
+  for (int j0 = 0; j0 < npieces; j0 += 32) M = fmaxf(M, piece_ml(j0 + lane).x);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
   constexpr int E = D / 32;  // dims per lane
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float M = -INFINITY, Ls = 0.f;
-  const long long base = static_cast<long long>(r) * p.virt_heads + vg;
-  for (long long ww = wf; ww <= wl; ++ww) {
-    if (ww * N / W == (ww + 1) * N / W) continue;  // empty range: wrote nothing
-    const long long slot = base + ww;
-    const float2 ml = p.part_ml[slot * GW + h];
-    const float Mn = fmaxf(M, ml.x);
-    if (Mn == -INFINITY) continue;
-    const float sa = exp2f(M - Mn), sb = exp2f(ml.x - Mn);
-    Ls = Ls * sa + ml.y * sb;
-    const float* src = p.part_o + (slot * GW + h) * D + lane * E;
-    if constexpr (E == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] = acc[0] * sa + v.x * sb;
-      acc[1] = acc[1] * sa + v.y * sb;
-      acc[2] = acc[2] * sa + v.z * sb;
-      acc[3] = acc[3] * sa + v.w * sb;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      acc[0] = acc[0] * sa + v.x * sb;
-      acc[1] = acc[1] * sa + v.y * sb;
+  float Ls = 0.f;
+  for (int j0 = 0; j0 < npieces; j0 += 32) {
+    const float2 ml = piece_ml(j0 + lane);
+    const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+    Ls += wgt * ml.y;
+    const int cnt = min(32, npieces - j0);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, wgt, j);
+      if (wj == 0.f) continue;
+      const float* src = p.part_o + ((base + j0 + j) * GW + h) * D + lane * E;
+      if constexpr (E == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += wj * v.x;
+        acc[1] += wj * v.y;
+        acc[2] += wj * v.z;
+        acc[3] += wj * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += wj * v.x;
+        acc[1] += wj * v.y;
+      }
     }
-    M = Mn;
   }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
   const float inv = 1.f / Ls;
   const int row = __ldg(p.qsl + r);
-  uint16_t* dst = p.out + (static_cast<long long>(row) * p.num_q_heads + vg * GW + h) * D + lane * E;
+  uint16_t* dst =
+      p.out + (static_cast<long long>(row) * p.num_q_heads + vg * GW + h) * D + lane * E;
   if constexpr (E == 4) {
     uint2 ov;
     ov.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
@@ -558,8 +605,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
 }
 
 // ------------------------------------------------------------------ host
-constexpr int kDecodeStages = 3;
-constexpr int kDecodeWarps = 4;
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 2
+#endif
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+constexpr int kDecodeStages = PKV_DECODE_STAGES;  // smem stages per warp
+constexpr int kDecodeWarps = PKV_DECODE_WARPS;    // warps per CTA
 
 template <int D, int GW>
 constexpr size_t decode_smem_bytes() {
@@ -611,8 +664,7 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_
   e = cudaGetLastError();
   if (e == cudaSuccess && trace) e = cudaEventRecord(static_cast<cudaEvent_t>(trace[3]), stream);
   if (e != cudaSuccess) return e;
-  const int items = p.num_reqs * p.virt_heads * GW;
-  combine_kernel<D, GW><<<(items + 3) / 4, 128, 0, stream>>>(p, items);
+  combine_kernel<D, GW><<<static_cast<unsigned>(p.warps), GW * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -639,6 +691,7 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUte
   p.hdr = ws.hdr;
   p.part_ml = ws.part_ml;
   p.part_o = ws.part_o;
+  p.bound = ws.bound;
   if (a.head_dim == 128 && gw == 4) return launch_decode_t<128, 4>(p, kv_map, stream, trace);
   if (a.head_dim == 128 && gw == 2) return launch_decode_t<128, 2>(p, kv_map, stream, trace);
   if (a.head_dim == 128 && gw == 1) return launch_decode_t<128, 1>(p, kv_map, stream, trace);

@@ -16,62 +16,70 @@ namespace pkv {
 
 static __device__ uint32_t g_errors_kvwrite;
 
+// One warp per request: its lanes cover the request's new tokens. Tokens at
+// or past query_start_loc[num_reqs] (padding rows) are set to -1 by the
+// threads of the trailing blocks of the grid.
 __global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
                                     const int32_t* __restrict__ block_table, int max_blocks,
                                     const int32_t* __restrict__ qsl,
                                     const int32_t* __restrict__ num_computed, int num_reqs,
-                                    int num_tokens, int num_blocks) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= num_tokens) return;
-  const int total = __ldg(qsl + num_reqs);
-  if (t >= total || num_reqs <= 0) {
-    slots[t] = -1;
+                                    int num_tokens, int num_blocks, int req_blocks) {
+  if (static_cast<int>(blockIdx.x) >= req_blocks) {  // padding rows
+    const int t = (blockIdx.x - req_blocks) * blockDim.x + threadIdx.x;
+    if (t < num_tokens && t >= __ldg(qsl + num_reqs)) slots[t] = -1;
     return;
   }
-  if (__ldg(qsl) > t) {  // query_start_loc[0] must be 0
-    atomicOr(&g_errors_kvwrite, kErrLengths);
-    slots[t] = -1;
+  const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
+  if (r >= num_reqs) return;
+  const int q0 = __ldg(qsl + r), q1 = __ldg(qsl + r + 1);
+  const int c = __ldg(num_computed + r);
+  if (q0 < 0 || q1 < q0 || q1 > num_tokens || c < 0 || (r == 0 && q0 != 0)) {
+    if (lane == 0) atomicOr(&g_errors_kvwrite, kErrLengths);
     return;
   }
-  const int r = upper_index(qsl, num_reqs, t);
-  const long long pos = static_cast<long long>(__ldg(num_computed + r)) + (t - __ldg(qsl + r));
-  const long long lb = pos / kBlockSize;
-  if (pos < 0 || lb >= max_blocks) {
-    atomicOr(&g_errors_kvwrite, kErrLengths);
-    slots[t] = -1;
-    return;
+  const long long row = static_cast<long long>(r) * max_blocks;
+  for (int t = q0 + lane; t < q1; t += 32) {
+    const long long pos = static_cast<long long>(c) + (t - q0);
+    const long long lb = pos / kBlockSize;
+    int64_t slot = -1;
+    if (lb >= max_blocks) {
+      atomicOr(&g_errors_kvwrite, kErrLengths);
+    } else {
+      const int phys = __ldg(block_table + row + lb);
+      if (phys < 0 || phys >= num_blocks)
+        atomicOr(&g_errors_kvwrite, kErrBlockRange);
+      else
+        slot = static_cast<int64_t>(phys) * kBlockSize + (pos % kBlockSize);
+    }
+    slots[t] = slot;
   }
-  const int phys = __ldg(block_table + static_cast<long long>(r) * max_blocks + lb);
-  if (phys < 0 || phys >= num_blocks) {
-    atomicOr(&g_errors_kvwrite, kErrBlockRange);
-    slots[t] = -1;
-    return;
-  }
-  slots[t] = static_cast<int64_t>(phys) * kBlockSize + (pos % kBlockSize);
 }
 
-// One 16-byte vector per thread per iteration. vec_per_row = Hkv * D / 8.
+// One CTA per token (grid-stride over tokens): its threads copy the token's K
+// row and V row, 16 bytes each, into the pool at the token's slot.
+// vec_per_row = Hkv * D / 8.
 __global__ void kv_write_kernel(uint4* __restrict__ pool, const uint4* __restrict__ key,
                                 const uint4* __restrict__ value, long long key_stride_v,
                                 long long value_stride_v, const int64_t* __restrict__ slots,
                                 int num_tokens, int vec_per_row, long long num_slots) {
-  const long long total = static_cast<long long>(num_tokens) * 2 * vec_per_row;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    const int t = static_cast<int>(i / (2 * vec_per_row));
-    const int w = static_cast<int>(i - static_cast<long long>(t) * 2 * vec_per_row);
-    const int kv = w >= vec_per_row;
-    const int e = w - kv * vec_per_row;
+  for (int t = blockIdx.x; t < num_tokens; t += gridDim.x) {
     const long long s = __ldg(slots + t);
     if (s < 0) continue;
     if (s >= num_slots) {
-      if (e == 0 && kv == 0) atomicOr(&g_errors_kvwrite, kErrSlotRange);
+      if (threadIdx.x == 0) atomicOr(&g_errors_kvwrite, kErrSlotRange);
       continue;
     }
-    const uint4 v = kv ? __ldg(value + t * value_stride_v + e) : __ldg(key + t * key_stride_v + e);
     const long long blk = s / kBlockSize, off = s % kBlockSize;
-    pool[((blk * 2 + kv) * kBlockSize + off) * vec_per_row + e] = v;
+    uint4* kdst = pool + ((blk * 2) * kBlockSize + off) * vec_per_row;
+    uint4* vdst = kdst + static_cast<long long>(kBlockSize) * vec_per_row;
+    const uint4* ksrc = key + t * key_stride_v;
+    const uint4* vsrc = value + t * value_stride_v;
+    for (int e = threadIdx.x; e < vec_per_row; e += blockDim.x) {
+      const uint4 kv = __ldg(ksrc + e);
+      const uint4 vv = __ldg(vsrc + e);
+      kdst[e] = kv;
+      vdst[e] = vv;
+    }
   }
 }
 
@@ -80,10 +88,11 @@ cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int 
                                 int num_tokens, int num_blocks, cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
   const int threads = 256;
-  const int grid = (num_tokens + threads - 1) / threads;
-  slot_mapping_kernel<<<grid, threads, 0, stream>>>(slots, block_table, max_blocks, qsl,
-                                                    num_computed, num_reqs, num_tokens,
-                                                    num_blocks);
+  const int req_blocks = (num_reqs + threads / 32 - 1) / (threads / 32);
+  const int pad_blocks = (num_tokens + threads - 1) / threads;
+  slot_mapping_kernel<<<req_blocks + pad_blocks, threads, 0, stream>>>(
+      slots, block_table, max_blocks, qsl, num_computed, num_reqs, num_tokens, num_blocks,
+      req_blocks);
   return cudaGetLastError();
 }
 
@@ -93,12 +102,10 @@ cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long
                             cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
   const int vec_per_row = num_kv_heads * head_dim / 8;
-  const long long total = static_cast<long long>(num_tokens) * 2 * vec_per_row;
-  const int threads = 256;
-  long long grid = (total + threads - 1) / threads;
-  const long long cap = static_cast<long long>(num_sms) * 8;
-  if (grid > cap) grid = cap;
-  kv_write_kernel<<<static_cast<int>(grid), threads, 0, stream>>>(
+  const int threads = vec_per_row >= 128 ? 128 : (vec_per_row >= 64 ? 64 : 32);
+  const long long cap = static_cast<long long>(num_sms) * 16;
+  const int grid = static_cast<int>(num_tokens < cap ? num_tokens : cap);
+  kv_write_kernel<<<grid, threads, 0, stream>>>(
       static_cast<uint4*>(pool), static_cast<const uint4*>(key), static_cast<const uint4*>(value),
       key_stride / 8, value_stride / 8, slots, num_tokens, vec_per_row,
       static_cast<long long>(num_blocks) * kBlockSize);

@@ -25,6 +25,7 @@ struct AttnWorkspace {
   int32_t* pf_prefix;    // [R + 1]: prefill items before the k-th prefill request
   float2* part_ml;       // [slots][GW]: (running max in log2 units, sum)
   float* part_o;         // [slots][GW][D]: unnormalised partial outputs
+  int2* bound;           // [W]: pair holding the first position of each decode warp
 };
 
 struct AttnArgs {

@@ -127,3 +127,87 @@ def test_reduce_scatter_lane_map(D, GW):
         for i in range(NPL):
             assert abs(v[lane, i] - vals[group, base + i].sum()) < 1e-9
             assert (base + i) // KPL == li // LPH  # a lane's scores stay in one head
+
+
+@pytest.mark.parametrize("D,GW", [(64, 1), (64, 2), (64, 4), (128, 1), (128, 2), (128, 4)])
+def test_select_free_reduce_scatter_with_permuted_lanes(D, GW):
+    """The kernel stores, at register position p, the score of logical index
+    p ^ M(lane) with M = (li * NV) // LPK (q heads and keys visited in a
+    lane-dependent order). Then every halving stage is v[i] += shfl_xor(v[i+H])
+    with no select, and lane li ends with logical indices M + i."""
+    LPK = D // 8
+    KPI = 32 // LPK
+    KPL = 16 // KPI
+    NV = GW * KPL
+    NPL = NV // LPK if NV >= LPK else 1
+    rng = np.random.default_rng(7 * D + GW)
+    logical = rng.standard_normal((32, NV))  # lane's partial for logical index
+    v = np.empty_like(logical)
+    for lane in range(32):
+        li = lane % LPK
+        M = (li * NV) // LPK
+        for p in range(NV):
+            h, j = (p // KPL) ^ (M // KPL), (p % KPL) ^ (M % KPL)
+            assert h < GW and j < KPL
+            v[lane, p] = logical[lane, h * KPL + j]
+    n, off = NV, LPK // 2
+    while off >= 1:
+        new = v.copy()
+        if n >= 2:
+            H = n // 2
+            for lane in range(32):
+                for i in range(H):
+                    new[lane, i] = v[lane, i] + v[lane ^ off, i + H]
+            n = H
+        else:
+            for lane in range(32):
+                new[lane, 0] = v[lane, 0] + v[lane ^ off, 0]
+        v = new
+        off //= 2
+    for lane in range(32):
+        sub, li = lane // LPK, lane % LPK
+        M = (li * NV) // LPK
+        group = [sub * LPK + k for k in range(LPK)]
+        for i in range(NPL):
+            assert abs(v[lane, i] - logical[group, M + i].sum()) < 1e-9
+
+
+def pair_at(x, prefix, Hv):
+    """(request, virtual head) holding stream position x."""
+    u = x // Hv
+    r = max(i for i in range(len(prefix) - 1) if prefix[i] <= u)
+    nb = int(prefix[r + 1] - prefix[r])
+    return r, (x - Hv * int(prefix[r])) // nb
+
+
+@pytest.mark.parametrize("trial", range(60))
+def test_each_split_pair_is_combined_by_exactly_one_boundary(trial):
+    """Boundary warp w (1 <= w < W) reads the pair holding start(w) (empty
+    ranges included) and combines it iff the pair's first block belongs to
+    warp w - 1."""
+    rng = np.random.default_rng(1000 + trial)
+    R = int(rng.integers(1, 10))
+    nblk = rng.integers(0, 25, size=R)
+    if nblk.sum() == 0:
+        nblk[-1] = 2
+    Hv = int(rng.choice([1, 2, 4, 8]))
+    W = int(rng.integers(1, 400))
+    prefix = np.concatenate([[0], np.cumsum(nblk)]).astype(np.int64)
+    N = Hv * int(prefix[-1])
+    claimed = {}
+    for w in range(1, W):
+        x = w * N // W
+        if x >= N:
+            continue
+        r, vg = pair_at(x, prefix, Hv)
+        nb = int(prefix[r + 1] - prefix[r])
+        a = Hv * int(prefix[r]) + vg * nb
+        if owner(a, N, W) == w - 1:
+            assert (r, vg) not in claimed
+            claimed[(r, vg)] = w
+    for r in range(R):
+        nb = int(prefix[r + 1] - prefix[r])
+        for vg in range(Hv if nb else 0):
+            a = Hv * int(prefix[r]) + vg * nb
+            split = owner(a, N, W) != owner(a + nb - 1, N, W)
+            assert ((r, vg) in claimed) == split
