@@ -186,7 +186,8 @@ int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
  * max_seq_len    host hint: >= every L (like max_seqlen_k).
  * num_q_heads    multiple of num_kv_heads; num_q_heads / num_kv_heads must be
  *                1, 2, 4 or 8.
- * scale          softmax scale (1/sqrt(head_dim) on the pages' models).
+ * scale          softmax scale, positive and finite (1/sqrt(head_dim) on the
+ *                pages' models); anything else is PKV_ERR_BAD_SHAPE.
  * workspace      device buffer of at least pkv_attention_workspace_size()
  *                bytes, 256-byte aligned, private to this call while it runs
  *                (no zeroing needed).

@@ -276,7 +276,7 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   if (num_reqs < 0 || num_tokens < 0 || max_blocks_per_req < 0 || max_query_len < 0 ||
       max_seq_len < 0)
     return PKV_ERR_BAD_SHAPE;
-  if (!(scale == scale)) return PKV_ERR_BAD_SHAPE;
+  if (!(scale > 0.f) || scale > 3.0e38f) return PKV_ERR_BAD_SHAPE;  // positive and finite
   const int64_t row = static_cast<int64_t>(num_q_heads) * layout.head_dim;
   if (q_row_stride == 0) q_row_stride = row;
   if (q_row_stride < row) return PKV_ERR_BAD_SHAPE;

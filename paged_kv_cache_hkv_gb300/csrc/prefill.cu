@@ -10,16 +10,22 @@
 //
 // Work item = (request, tile of 128 query rows, kv head). The 128 rows of a
 // tile are the G = Hq/Hkv q heads of one kv head for 128/G consecutive
-// queries, so every K/V tile feeds all G heads (GQA). For each tile of 128
-// keys (8 pool blocks):
-//   S = Q K^T        tcgen05.mma M=128 N=128, A = Q (smem), B = K (smem)
-//   softmax          each thread owns one row: tcgen05.ld of S, causal
-//                    mask, running max/sum in base 2, P rounded to bf16 into
-//                    smem, O rescaled in TMEM when the max moves
-//   O += P V         tcgen05.mma M=128 N=D, A = P (smem), B = V (smem)
-// Q, K and V arrive by TMA with 128-byte swizzle (one 16-token block of one
-// kv head per copy), the layout the tensor core reads. Accumulators: S in
-// TMEM columns [0, 128), O in [128, 128 + D).
+// queries, so every K/V tile feeds all G heads (GQA). The item's key tiles
+// (128 keys = 8 pool blocks each) are split between two softmax warpgroups:
+// warpgroup w takes tiles w, w+2, ... with its own accumulators
+// (TMEM columns [256w, 256w+128) for S, [256w+128, 256w+128+D) for O).
+// One issuer thread streams K/V tiles through a 2-stage ring by TMA (128-byte
+// swizzle, one 16-token block of one kv head per copy) and issues
+//   S_w = Q K^T      tcgen05.mma M=128 N=128, A = Q (smem), B = K (smem)
+//   O_w += P_w V     tcgen05.mma M=128 N=D, A = P_w (smem), B = V (smem)
+// while the warpgroups run the softmax: each thread owns one row, reads S
+// with tcgen05.ld, applies the causal mask, keeps a base-2 running max
+// (rescaling O in TMEM only when it grows by more than 2^8) and sum, and
+// writes P as bf16 into its warpgroup's smem buffer. One warpgroup's softmax
+// runs while the tensor core works on the other's tiles; each warpgroup's
+// next K/V tile streams in by TMA while the other one computes. At the end the two
+// partial (max, sum, O) are merged and each warpgroup writes half of the
+// output columns.
 //
 // Every wait is bounded; on a timeout the kernel records
 // PKV_DEVERR_TIMEOUT, drains its copies, frees TMEM and returns.
@@ -69,12 +75,24 @@ __device__ __forceinline__ void fence_before_sync() {
 __device__ __forceinline__ void fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
+
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane (asynchronous:
+// the registers hold the data only after wait16 on them).
+__device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// 32 consecutive 32-bit columns (asynchronous, like ld16).
+__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
       "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -84,26 +102,39 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float* v) {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void st32(uint32_t taddr, const float* v) {
+// tcgen05.wait::ld pinning 32 loaded registers (see wait16).
+__device__ __forceinline__ void wait32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// tcgen05.wait::ld with the loaded registers as operands, so that no use of
+// them can be scheduled before the wait.
+__device__ __forceinline__ void wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-          taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
       : "memory");
 }
 
@@ -111,19 +142,25 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float* v) {
 
 constexpr int kTileM = 128;  // query rows (query x head) per tile
 constexpr int kTileN = 128;  // keys per tile (8 blocks)
-constexpr uint32_t kTmemCols = 256;
+constexpr int kStages = 2;   // K and V tile rings: tile kt uses slot (tiles + kt) % 2
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 352;  // 2 softmax warpgroups + MMA warp + K-copy warp + V-copy warp
+constexpr int kIssuer = 256;   // thread that issues the MMAs (warp 8, lane 0)
+constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (powers of two)
 
 template <int D>
 struct PrefillLayout {
-  static constexpr int DH = D / 64;  // 64-element (128-byte) column chunks
-  static constexpr uint32_t kChunk = kTileM * 128;  // one 128-row x 128-byte chunk: 16 KB
+  static constexpr int DH = D / 64;                 // 64-element (128-byte) column chunks
+  static constexpr uint32_t kChunk = kTileM * 128;  // 128 rows x 128 bytes = 16 KB
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + DH * kChunk;  // 2 stages
-  static constexpr uint32_t kV = kK + 2 * DH * kChunk;
-  static constexpr uint32_t kP = kV + 2 * DH * kChunk;  // 2 chunks (128 keys)
-  static constexpr uint32_t kBar = kP + 2 * kChunk;
-  static constexpr uint32_t kBytes = kBar + 128;
+  static constexpr uint32_t kTileKV = DH * kChunk;     // K (or V) of one 128-key tile
+  static constexpr uint32_t kK = kQ + DH * kChunk;     // K ring, kStages tiles
+  static constexpr uint32_t kV = kK + kStages * kTileKV;  // V ring, kStages tiles
+  static constexpr uint32_t kP = kV + kStages * kTileKV;  // P of warpgroup w: 2 chunks each
+  static constexpr uint32_t kBar = kP + 2 * 2 * kChunk;
+  static constexpr uint32_t kBytes = kBar + 256;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base
+  static_assert(kAlloc <= 232448, "shared memory");
 };
 
 struct PrefillParams {
@@ -142,17 +179,45 @@ struct PrefillParams {
 
 struct PrefillShared {
   uint64_t q_full;
-  uint64_t kv_full[2];
-  uint64_t s_full;
-  uint64_t o_full;
+  uint64_t k_full[kStages];
+  uint64_t v_full[kStages];
+  uint64_t s_full[2];   // S of warpgroup w computed
+  uint64_t p_ready[2];  // P of warpgroup w in smem, V rows cleaned (128 arrivals)
+  uint64_t pv_done[2];  // O of warpgroup w updated
+  uint64_t drain;
   uint32_t tmem;
   int item;
   int abort;
-  uint32_t mask[2];
 };
 
+// Bounded wait that also gives up once another thread has flagged an abort.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicOr(&g_errors_prefill, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Work item: (request, 128-row query tile, kv head). Two softmax warpgroups
+// split the item's key tiles (warpgroup w takes tiles w, w+2, ...), each with
+// its own S and O accumulators in TMEM and its own running max and sum; one
+// thread streams K/V tiles through a 3-stage ring by TMA and issues every
+// MMA: S_w = Q K^T into TMEM, then O_w += P_w V with P_w (bf16) read from
+// TMEM where the softmax wrote it over S_w. At the end the two partial
+// results are merged (log-sum-exp) and each warpgroup writes half of the
+// output columns.
 template <int D>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                    const PrefillParams p) {
   using Lay = PrefillLayout<D>;
@@ -162,21 +227,30 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   PrefillShared& sh = *reinterpret_cast<PrefillShared*>(gbase + Lay::kBar);
+  volatile int* abort_flag = &sh.abort;
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int wg = tid >> 7;          // 0, 1 softmax warpgroups; 2 = issuer warp
+  const int row = tid & 127;        // query row of this softmax thread (TMEM lane)
   const int G = p.group, QT = kTileM / G;
 
-  if (tid == 0) {
+  if (tid == kIssuer) {
     mbar_init(&sh.q_full, 1);
-    mbar_init(&sh.kv_full[0], 1);
-    mbar_init(&sh.kv_full[1], 1);
-    mbar_init(&sh.s_full, 1);
-    mbar_init(&sh.o_full, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sh.k_full[i], 1);
+      mbar_init(&sh.v_full[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.p_ready[i], 128);
+      mbar_init(&sh.pv_done[i], 1);
+    }
+    mbar_init(&sh.drain, 1);
     sh.abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&kv_map);
     prefetch_tensormap(&q_map);
   }
-  if (warp == 0) {
+  if (warp == 8) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&sh.tmem)),
                  "r"(kTmemCols)
@@ -187,23 +261,20 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sh.tmem;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t t_s = tmem + lane_base;         // S: columns [0, 128)
-  const uint32_t t_o = tmem + lane_base + 128u;  // O: columns [128, 128 + D)
-
   constexpr uint32_t idesc_qk = tc::idesc_bf16(kTileM, kTileN, 0);
   constexpr uint32_t idesc_pv = tc::idesc_bf16(kTileM, D, 1);
   const uint32_t n_items = p.hdr[kHdrPrefillItems];
   const int n_req = static_cast<int>(p.hdr[kHdrPrefillReqs]);
 
-  uint32_t n_q = 0, n_s = 0, n_o = 0, tiles = 0;  // completed phases per barrier
-  bool failed = false;
+  // phase counters, identical in every thread
+  uint32_t n_q = 0, tiles = 0, cnt[2] = {0, 0};
+  uint32_t drains = 0;
 
   while (true) {
-    if (tid == 0) sh.item = static_cast<int>(atomicAdd(&p.hdr[kHdrPrefillNext], 1u));
+    if (tid == kIssuer) sh.item = static_cast<int>(atomicAdd(&p.hdr[kHdrPrefillNext], 1u));
     __syncthreads();
     const int item = sh.item;
-    if (item >= static_cast<int>(n_items)) break;
+    if (item >= static_cast<int>(n_items) || sh.abort) break;
 
     // ---- which (request, tile, kv head)
     const int k = upper_index(p.pf_prefix, n_req, item);
@@ -220,214 +291,294 @@ __global__ void __launch_bounds__(128, 1)
     const int kv_len = c + i_last + 1;
     const int nkv = (kv_len + kTileN - 1) / kTileN;
     const long long bt_row = static_cast<long long>(r) * p.max_blocks;
-
-    auto issue_tile = [&](int kt, int st) {  // thread 0 only
-      const int left = kv_len - kt * kTileN;
-      const int nb = min(8, (left + kBlockSize - 1) / kBlockSize);
-      uint32_t mask = 0, bytes = 0;
-      int phys[8];
-      for (int b = 0; b < nb; ++b) {
-        phys[b] = __ldg(p.block_table + bt_row + kt * 8 + b);
-        if (phys[b] >= 0 && phys[b] < p.num_blocks) {
-          mask |= 1u << b;
-          bytes += 2u * DH * 2048u;
-        } else {
-          atomicOr(&g_errors_prefill, kErrBlockRange);
-        }
-      }
-      sh.mask[st] = mask;
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&sh.kv_full[st], bytes);
-      for (int b = 0; b < nb; ++b) {
-        if (!(mask >> b & 1u)) continue;
-#pragma unroll
-        for (int dh = 0; dh < DH; ++dh) {
-          tma_load_3d(gbase + Lay::kK + (st * DH + dh) * Lay::kChunk + b * 2048, &kv_map, dh * 64,
-                      g, phys[b] * 32, &sh.kv_full[st]);
-          tma_load_3d(gbase + Lay::kV + (st * DH + dh) * Lay::kChunk + b * 2048, &kv_map, dh * 64,
-                      g, phys[b] * 32 + 16, &sh.kv_full[st]);
-        }
-      }
+    auto stage_of = [&](int kt) { return static_cast<int>((tiles + kt) % kStages); };
+    auto stage_par = [&](int kt) { return ((tiles + kt) / kStages) & 1u; };
+    // phys id of block b of tile kt if it holds keys < kv_len and is in the pool, else -1
+    auto block_id = [&](int kt, int b) -> int {
+      if (kt * kTileN + b * kBlockSize >= kv_len) return -1;
+      const int id = __ldg(p.block_table + bt_row + kt * 8 + b);
+      return (id >= 0 && id < p.num_blocks) ? id : -1;
     };
 
-    if (tid == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&sh.q_full, DH * Lay::kChunk);
+    if (warp >= 8) {
+      // ================= producer warps, each with in-order blocking waits:
+      //   warp 9:  K(kt) TMA copies, once S(kt - 2) is done (its K slot is free)
+      //   warp 10: V(kt) TMA copies, once PV(kt - 2) is done (its V slot is free)
+      //   warp 8:  MMAs: S(kt) once K(kt) landed and softmax(kt - 2) read S_w;
+      //            PV(kt) once softmax(kt) wrote P_w and V(kt) landed
+      // Lanes 0 .. 8*DH-1 of a copy warp issue one TMA copy each; the block
+      // ids of a 32-block window sit in the lanes' registers.
+      const int ln = tid & 31;
+      auto phase = [&](int kt) { return (cnt[kt & 1] + (kt >> 1)) & 1u; };
+      bool ok = true;
+      if (warp == 9 || warp == 10) {
+        const int is_v = warp == 10;
+        if (!is_v && ln == 0) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(&sh.q_full, DH * Lay::kChunk);
 #pragma unroll
-      for (int dh = 0; dh < DH; ++dh)
-        tma_load_3d(gbase + Lay::kQ + dh * Lay::kChunk, &q_map, dh * 64, g * G, q0 + i0,
-                    &sh.q_full);
-      issue_tile(0, tiles & 1);
-      if (nkv > 1) issue_tile(1, (tiles + 1) & 1);
-    }
-
-    // this thread's row: query i0 + tid / G, head g * G + tid % G
-    const int qi = i0 + tid / G;
-    const int lim = min(c + qi, kv_len - 1);  // last key this row may see
-    float m_run = -INFINITY, l_run = 0.f;
-
-    for (int kt = 0; kt < nkv; ++kt) {
-      const uint32_t tg = tiles + kt;
-      const int st = tg & 1;
-      bool ok = mbar_wait(&sh.kv_full[st], (tg >> 1) & 1u);
-      if (kt == 0) ok = mbar_wait(&sh.q_full, n_q & 1u) && ok;
-      const uint32_t mask = sh.mask[st];
-      {  // zero the V rows of keys that are past kv_len or were not loaded
-        const int j = kt * kTileN + tid;
-        if (j >= kv_len || !(mask >> (tid >> 4) & 1u)) {
+          for (int dh = 0; dh < DH; ++dh)
+            tma_load_3d(gbase + Lay::kQ + dh * Lay::kChunk, &q_map, dh * 64, g * G, q0 + i0,
+                        &sh.q_full);
+        }
+        int win_base = -1000000, win_val = -1;
+        for (int kt = 0; ok && kt < nkv; ++kt) {
+          if (kt >= kStages) {  // the slot's previous tile (kt - 2) must be done with it
+            ok = wait_or_abort(is_v ? &sh.pv_done[kt & 1] : &sh.s_full[kt & 1], phase(kt - 2),
+                               abort_flag);
+            if (!ok) break;
+          }
+          const int st = stage_of(kt);
+          if (kt * 8 + 8 > win_base + 32) {
+            win_base = kt * 8;
+            const int lb = win_base + ln;
+            win_val = (lb * kBlockSize < kv_len) ? block_id(kt + ln / 8, ln & 7) : -1;
+            if (!is_v && lb * kBlockSize < kv_len && win_val < 0)
+              atomicOr(&g_errors_prefill, kErrBlockRange);
+          }
+          const int b = (ln / DH) & 7, dh = ln % DH;
+          const int id = __shfl_sync(0xffffffffu, win_val, kt * 8 - win_base + b);
+          const bool mine = ln < 8 * DH && id >= 0;
+          const uint32_t nops = __popc(__ballot_sync(0xffffffffu, mine));
+          uint64_t* bar = is_v ? &sh.v_full[st] : &sh.k_full[st];
+          if (ln == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, nops * 2048u);
+          }
+          __syncwarp();
+          if (mine)
+            tma_load_3d(gbase + (is_v ? Lay::kV : Lay::kK) + st * Lay::kTileKV +
+                            dh * Lay::kChunk + b * 2048,
+                        &kv_map, dh * 64, g, id * 32 + (is_v ? 16 : 0), bar);
+        }
+      } else if (warp == 8 && ln == 0) {
+        auto issue_s = [&](int kt) {  // S_w = Q K^T for tile kt
+          const int w = kt & 1, st = stage_of(kt);
+          tc::fence_after_sync();
 #pragma unroll
-          for (int dh = 0; dh < DH; ++dh) {
-            uint4* row = reinterpret_cast<uint4*>(gbase + Lay::kV + (st * DH + dh) * Lay::kChunk +
-                                                  tid * 128);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Lay::kChunk + (kk & 3) * 32;
+            const uint64_t a = tc::sw128_desc(base + Lay::kQ + off, 16, 1024);
+            const uint64_t b = tc::sw128_desc(base + Lay::kK + st * Lay::kTileKV + off, 16, 1024);
+            tc::mma_bf16(tmem + w * 256u, a, b, idesc_qk, kk > 0);
+          }
+          tc::commit(&sh.s_full[w]);
+        };
+        auto issue_pv = [&](int kt) {  // O_w += P_w V for tile kt, P_w from smem
+          const int w = kt & 1, st = stage_of(kt);
+          tc::fence_after_sync();
+          const uint32_t vbase = base + Lay::kV + st * Lay::kTileKV;
+          const uint32_t pbase = base + Lay::kP + w * 2 * Lay::kChunk;
 #pragma unroll
-            for (int x = 0; x < 8; ++x) row[x] = make_uint4(0, 0, 0, 0);
+          for (int kk = 0; kk < kTileN / 16; ++kk) {
+            const uint64_t a =
+                tc::sw128_desc(pbase + (kk >> 2) * Lay::kChunk + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = tc::sw128_desc(vbase + kk * 2048, Lay::kChunk, 1024);
+            tc::mma_bf16(tmem + w * 256u + 128u, a, b, idesc_pv, (kt >= 2 || kk > 0) ? 1u : 0u);
+          }
+          tc::commit(&sh.pv_done[w]);
+        };
+        ok = wait_or_abort(&sh.q_full, n_q & 1u, abort_flag);
+        for (int kt = 0; ok && kt < 2 && kt < nkv; ++kt) {
+          ok = wait_or_abort(&sh.k_full[stage_of(kt)], stage_par(kt), abort_flag);
+          if (ok) issue_s(kt);
+        }
+        // after softmax(kt): S(kt + 2) first (the warpgroup's next softmax
+        // waits on it), then PV(kt) (needed only before its next P write)
+        for (int kt = 0; ok && kt < nkv; ++kt) {
+          ok = wait_or_abort(&sh.p_ready[kt & 1], phase(kt), abort_flag);
+          if (ok && kt + 2 < nkv) {
+            ok = wait_or_abort(&sh.k_full[stage_of(kt + 2)], stage_par(kt + 2), abort_flag);
+            if (ok) issue_s(kt + 2);
+          }
+          if (ok) ok = wait_or_abort(&sh.v_full[stage_of(kt)], stage_par(kt), abort_flag);
+          if (!ok) break;
+          issue_pv(kt);
+        }
+        if (!ok) {  // let issued MMAs finish before anything is torn down
+          tc::commit(&sh.drain);
+          mbar_wait(&sh.drain, drains & 1u, kDrainLimitNs);
+        }
+      }
+      if (warp == 8) drains += __shfl_sync(0xffffffffu, ok ? 0u : 1u, 0);
+    } else if (wg < 2) {
+      // ================= softmax warpgroup wg: tiles wg, wg + 2, ...
+      const int qi = i0 + row / G;              // query of this row
+      const int lim = min(c + qi, kv_len - 1);  // last key this row may see
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t t_s = tmem + lane_base + wg * 256u;
+      float m_run = -INFINITY, l_run = 0.f;
+      bool ok = true;
+      int nmine = 0;
+      const int lane = tid & 31;
+      // block ids of this warpgroup's next tile, loaded one tile ahead by lanes 0..7
+      auto load_ids = [&](int kt) -> int { return (lane < 8 && kt < nkv) ? block_id(kt, lane) : -1; };
+      int next_id = load_ids(wg);
+      for (int kt = wg; ok && kt < nkv; kt += 2, ++nmine) {
+        const uint32_t ph = cnt[wg] + (kt >> 1);
+        const uint32_t mask = __ballot_sync(0xffffffffu, next_id >= 0) & 0xFFu;
+        next_id = load_ids(kt + 2);
+        ok = wait_or_abort(&sh.s_full[wg], ph & 1u, abort_flag);
+        if (!ok) break;
+        tc::fence_after_sync();
+        // a tile every row sees in full needs no mask; otherwise column j is
+        // visible iff j <= jlim and its 16-key block was loaded (chunk c of 16
+        // columns = block c of the tile)
+        const bool full = kt * kTileN + kTileN - 1 <= c + i0 && mask == 0xFFu;
+        const int jlim = lim - kt * kTileN;
+        // the whole S row in one TMEM round trip: 4 x 32 columns, one wait
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::ld32(t_s + q * 32, sr[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::wait32(sr[q]);
+        // invisible columns become -inf (block c of the tile = columns 16c .. 16c+15)
+        if (!full) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int j = q * 32 + i;
+              if (!(((mask >> (j >> 4)) & 1u) && j <= jlim)) sr[q][i] = __float_as_uint(-INFINITY);
+            }
+        }
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[q][i]));
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+        // (scale > 0 keeps the argmax)
+        // PV(kt - 2) must be done before O_wg is rescaled and P_wg rewritten
+        if (kt >= 2) {
+          ok = wait_or_abort(&sh.pv_done[wg], (ph - 1) & 1u, abort_flag);
+          if (!ok) break;
+          tc::fence_after_sync();
+        }
+        if (__any_sync(0xffffffffu, mx > m_run + kRescaleLog2)) {
+          const float m_new = fmaxf(m_run, mx);
+          const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+          if (kt >= 2) {
+#pragma unroll 1
+            for (int q = 0; q < D / 16; ++q) {
+              uint32_t o[16];
+              tc::ld16(t_s + 128u + q * 16, o);
+              tc::wait16(o);
+#pragma unroll
+              for (int x = 0; x < 16; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+              tc::st16(t_s + 128u + q * 16, o);
+            }
           }
         }
-      }
-      fence_proxy_async_smem();
-      if (!ok) sh.abort = 1;
-      __syncthreads();
-      if (sh.abort) {
-        failed = true;
-        break;
-      }
-      if (tid == 0) {  // S = Q K^T
-        tc::fence_after_sync();
+        // P = 2^(s * scale - m) as bf16 (-inf -> 0), row `row` of P_wg in smem
+        // (K-major, 128-byte swizzle: 16-byte chunk c of a row sits at c ^ (row % 8))
+        float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+        const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+        unsigned char* prow = gbase + Lay::kP + wg * 2 * Lay::kChunk + row * 128;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Lay::kChunk + (kk & 3) * 32;
-          const uint64_t a = tc::sw128_desc(base + Lay::kQ + off, 16, 1024);
-          const uint64_t b = tc::sw128_desc(base + Lay::kK + st * DH * Lay::kChunk + off, 16, 1024);
-          tc::mma_bf16(tmem, a, b, idesc_qk, kk > 0);
+        for (int c8 = 0; c8 < 16; ++c8) {  // 8 keys = one 16-byte chunk
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = c8 * 8 + 2 * e;
+            const float p0 = exp2f(__uint_as_float(sr[j >> 5][j & 31]) * p.scale_log2 - msub);
+            const float p1 = exp2f(__uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]) * p.scale_log2 - msub);
+            w[e] = pack_bf16x2(p0, p1);
+            ps4[e] += p0 + p1;
+          }
+          *reinterpret_cast<uint4*>(prow + (c8 >> 3) * Lay::kChunk + (((c8 & 7) ^ (row & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
-        tc::commit(&sh.s_full);
+        l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+        // V rows of keys past kv_len or of blocks not loaded must be zero
+        // (0 * NaN): for such a tile wait for its V copy first
+        if (kt * kTileN + kTileN > kv_len || mask != 0xFFu) {
+          ok = wait_or_abort(&sh.v_full[stage_of(kt)], stage_par(kt), abort_flag);
+          if (!ok) break;
+          const int key = kt * kTileN + row;
+          if (key >= kv_len || !(mask >> (row >> 4) & 1u)) {
+            unsigned char* vrow = gbase + Lay::kV + stage_of(kt) * Lay::kTileKV;
+#pragma unroll
+            for (int dh = 0; dh < DH; ++dh) {
+              uint4* v4 = reinterpret_cast<uint4*>(vrow + dh * Lay::kChunk + row * 128);
+#pragma unroll
+              for (int x = 0; x < 8; ++x) v4[x] = make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        tc::wait_st();
+        tc::fence_before_sync();
+        mbar_arrive(&sh.p_ready[wg]);
       }
-      ok = mbar_wait(&sh.s_full, n_s & 1u);
-      ++n_s;
+      if (ok && nmine > 0)  // this warpgroup's last PV
+        ok = wait_or_abort(&sh.pv_done[wg], (cnt[wg] + nmine - 1) & 1u, abort_flag);
       tc::fence_after_sync();
-
-      // ---- softmax over this row's 128 scores
-      float s[kTileN];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tc::ld32(t_s + q * 32, s + q * 32);
-      tc::wait_ld();
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < kTileN; ++j) {
-        const int key = kt * kTileN + j;
-        const bool vis = key <= lim && (mask >> (j >> 4) & 1u);
-        s[j] = vis ? s[j] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[j]);
-      }
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-      const float msub = (m_new == -INFINITY) ? 0.f : m_new;
-
-      if (kt > 0) {  // PV of the previous tile must be done: O and P are reused
-        ok = mbar_wait(&sh.o_full, n_o & 1u) && ok;
-        ++n_o;
-        tc::fence_after_sync();
-        if (tid == 0 && kt + 1 < nkv) issue_tile(kt + 1, (tg + 1) & 1);
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            float o[32];
-            tc::ld32(t_o + q * 32, o);
-            tc::wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] *= alpha;
-            tc::st32(t_o + q * 32, o);
-          }
-        }
-      }
-      float psum = 0.f;
-      unsigned char* prow = gbase + Lay::kP + tid * 128;
-#pragma unroll
-      for (int c8 = 0; c8 < kTileN / 8; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a0 = exp2f(s[c8 * 8 + 2 * e] - msub);
-          const float a1 = exp2f(s[c8 * 8 + 2 * e + 1] - msub);
-          w[e] = pack_bf16x2(a0, a1);
-          psum += bf16_lo(w[e]) + bf16_hi(w[e]);
-        }
-        const int chunk = c8 & 7, half = c8 >> 3;
-        *reinterpret_cast<uint4*>(prow + half * Lay::kChunk + ((chunk ^ (tid & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-      fence_proxy_async_smem();
-      tc::wait_st();
+      // ---- merge the two partial results. Each warpgroup posts its (max,
+      // sum) in its own P buffer, which no MMA reads any more (its last PV is
+      // done, or it had no tiles); Q may still be in use by the other's MMAs.
+      float2* ml_own = reinterpret_cast<float2*>(gbase + Lay::kP + wg * 2 * Lay::kChunk);
+      ml_own[row] = make_float2(m_run, l_run);
       tc::fence_before_sync();
-      if (!ok) sh.abort = 1;
-      __syncthreads();
-      if (sh.abort) {
-        failed = true;
-        break;
-      }
-      if (tid == 0) {  // O += P V
-        tc::fence_after_sync();
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      tc::fence_after_sync();
+      const float2 ml0 = reinterpret_cast<const float2*>(gbase + Lay::kP)[row];
+      const float2 ml1 = reinterpret_cast<const float2*>(gbase + Lay::kP + 2 * Lay::kChunk)[row];
+      const float M = fmaxf(ml0.x, ml1.x);
+      const float a0 = (ml0.x == -INFINITY) ? 0.f : exp2f(ml0.x - M);
+      const float a1 = (ml1.x == -INFINITY) ? 0.f : exp2f(ml1.x - M);
+      const float inv = 1.f / (ml0.y * a0 + ml1.y * a1);
+      const bool has1 = nkv > 1;
+      const bool store = ok && qi < n;
+      uint16_t* dst = p.out + (static_cast<long long>(q0 + qi) * p.num_q_heads + g * G + row % G) * D;
+      const uint32_t t_o0 = tmem + lane_base + 128u, t_o1 = tmem + lane_base + 256u + 128u;
+#pragma unroll 1
+      for (int q = 0; q < D / 32; ++q) {  // this warpgroup's D/2 columns, 16 at a time
+        const int col = wg * (D / 2) + q * 16;
+        uint32_t o0[16], o1[16];
+        tc::ld16(t_o0 + col, o0);
+        if (has1) tc::ld16(t_o1 + col, o1);
+        tc::wait16(o0);
+        if (has1) tc::wait16(o1);
+        if (store) {
+          uint32_t w[8];
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t a = tc::sw128_desc(base + Lay::kP + (kk >> 2) * Lay::kChunk + (kk & 3) * 32,
-                                            16, 1024);
-          const uint64_t b = tc::sw128_desc(base + Lay::kV + st * DH * Lay::kChunk + kk * 2048,
-                                            Lay::kChunk, 1024);
-          tc::mma_bf16(tmem + 128u, a, b, idesc_pv, (kt > 0 || kk > 0) ? 1u : 0u);
+          for (int e = 0; e < 8; ++e) {
+            float v[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int x = 2 * e + h;
+              v[h] = (__uint_as_float(o0[x]) * a0 + (has1 ? __uint_as_float(o1[x]) * a1 : 0.f)) * inv;
+            }
+            w[e] = pack_bf16x2(v[0], v[1]);
+          }
+          uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
-        tc::commit(&sh.o_full);
-      }
-    }
-    if (failed) break;
-
-    // ---- epilogue: O / l -> bf16 rows of the output
-    bool ok = mbar_wait(&sh.o_full, n_o & 1u);
-    ++n_o;
-    tc::fence_after_sync();
-    if (!ok) sh.abort = 1;
-    const float inv = 1.f / l_run;
-    const bool store = qi < n;
-    uint16_t* dst = p.out + (static_cast<long long>(q0 + qi) * p.num_q_heads + g * G + tid % G) * D;
-#pragma unroll
-    for (int q = 0; q < D / 32; ++q) {
-      float o[32];
-      tc::ld32(t_o + q * 32, o);
-      tc::wait_ld();
-      if (store) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + q * 32);
-#pragma unroll
-        for (int x = 0; x < 4; ++x)
-          d4[x] = make_uint4(pack_bf16x2(o[8 * x] * inv, o[8 * x + 1] * inv),
-                             pack_bf16x2(o[8 * x + 2] * inv, o[8 * x + 3] * inv),
-                             pack_bf16x2(o[8 * x + 4] * inv, o[8 * x + 5] * inv),
-                             pack_bf16x2(o[8 * x + 6] * inv, o[8 * x + 7] * inv));
       }
     }
     tc::fence_before_sync();
-    __syncthreads();
+    __syncthreads();  // O read, merge space reusable, next item may overwrite TMEM
+    tc::fence_after_sync();
     tiles += nkv;
+    cnt[0] += (nkv + 1) / 2;
+    cnt[1] += nkv / 2;
     ++n_q;
-    if (sh.abort) {
-      failed = true;
-      break;
-    }
   }
 
-  if (failed) {
-    if (tid == 0) {
-      atomicOr(&g_errors_prefill, kErrTimeout);
-      // let copies still in flight land before the shared memory goes away
-      mbar_wait(&sh.kv_full[0], 0, kDrainLimitNs);
-      mbar_wait(&sh.kv_full[1], 0, kDrainLimitNs);
-      mbar_wait(&sh.q_full, n_q & 1u, kDrainLimitNs);
+  if (sh.abort && tid == kIssuer) {
+    // let copies in flight land before the shared memory goes away
+    for (int st = 0; st < kStages; ++st) {
+      mbar_wait(&sh.k_full[st], 0, kDrainLimitNs);
+      mbar_wait(&sh.v_full[st], 0, kDrainLimitNs);
     }
-    __syncthreads();
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 8) {
     tc::fence_after_sync();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
@@ -442,7 +593,7 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& k
   const int smem = static_cast<int>(PrefillLayout<D>::kAlloc);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 128, smem, stream>>>(kv_map, q_map, p);
+  kern<<<grid, kThreads, smem, stream>>>(kv_map, q_map, p);
   return cudaGetLastError();
 }
 

@@ -91,6 +91,8 @@ def test_attention_rejects_bad_arguments(lib):
     assert _attn(lib, R=-1) == E("PKV_ERR_BAD_SHAPE")
     assert _attn(lib, ms=200) == E("PKV_ERR_BAD_SHAPE")        # 200 > 8 blocks * 16
     assert _attn(lib, scale=float("nan")) == E("PKV_ERR_BAD_SHAPE")
+    assert _attn(lib, scale=-0.5) == E("PKV_ERR_BAD_SHAPE")
+    assert _attn(lib, scale=float("inf")) == E("PKV_ERR_BAD_SHAPE")
     assert _attn(lib, qs=100) == E("PKV_ERR_BAD_SHAPE")        # row stride < Hq * D
     assert _attn(lib, bt=None) == E("PKV_ERR_NULL_POINTER")
     assert _attn(lib, q=MISALIGNED) == E("PKV_ERR_MISALIGNED")
