@@ -60,6 +60,27 @@ def dist_env():
     return rank, world, local
 
 
+# ------------------------------------------------------------------ ranks
+def replica_seed(base_seed, rank):
+    """Each rank runs its own replica of the workload with its own batch."""
+    return base_seed + rank
+
+
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The slowest rank's time (every rank must call it)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, max_ms_per_step):
+    """Units all ranks processed per second, over the slowest rank's time."""
+    return units_per_rank * world / (max_ms_per_step * 1e-3)
+
+
 # ------------------------------------------------------------------ work
 def step_work(step):
     """Algorithmic bytes and flops of one step.
@@ -198,7 +219,8 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    seed = args.seed if args.seed is not None else {"mixed_step": 3}.get(args.workload, 0)
+    seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3}.get(
+        args.workload, 0)
     meta = synth.WORKLOADS[args.workload](seed=seed, materialize=False)
     shape = shape_of(meta)
     per = {"decode": 4, "chunk": 8, "prefill": 4}
@@ -260,10 +282,11 @@ def run_native(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
         pg = dist
 
-    base_seed = args.seed if args.seed is not None else {"mixed_step": 3, "tiny_decode": 1,
-                                                         "llama_decode": 2, "prefix_sharing": 4,
+    base_seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3,
+                                                         "tiny_decode": 1, "llama_decode": 2,
+                                                         "prefix_sharing": 4,
                                                          "long_context": 5}[args.workload]
-    seed = base_seed + rank  # replicas: each rank its own batch
+    seed = replica_seed(base_seed, rank)
     step = synth.WORKLOADS[args.workload](seed=seed)
     ds = DeviceStep(step)
     binding.pkv_get_device_errors(clear=True)
@@ -311,12 +334,9 @@ def run_native(args):
         for i in range(binding.PKV_TRACE_EVENTS - 1):
             per_kernel[i] += ev[i].elapsed_time(ev[i + 1])
     per_kernel /= K  # ms per launch: plan, prefill, decode, combine
-    if pg is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, pg, device="cuda")
     ms_per_step = total_ms / K
-    value = work["tokens"] * world / (ms_per_step * 1e-3)
+    value = whole_job_rate(work["tokens"], world, ms_per_step)
     flags = binding.pkv_get_device_errors(clear=True)
     if flags:
         raise SystemExit(f"device error flags {flags:#x} in the timed region")
@@ -340,12 +360,8 @@ def run_native(args):
             host_out.copy_(ds.out, non_blocking=True)
         e1.record(stream)
         sync_all()
-        e2e_ms = e0.elapsed_time(e1)
-        if pg is not None:
-            t = torch.tensor([e2e_ms], device="cuda")
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": work["tokens"] * world / (e2e_ms / K * 1e-3), "unit": UNIT,
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, device="cuda")
+        e2e = {"value": whole_job_rate(work["tokens"], world, e2e_ms / K), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     # ---- roofline of the dominant kernel (decode)

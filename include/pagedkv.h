@@ -146,6 +146,34 @@ int32_t pkv_paged_kv_write(void* kv_cache, const void* key, const void* value,
                            pkv_cache_layout layout, void* stream);
 
 /*
+ * pkv_copy_blocks -- copy whole blocks (K and V of every kv head) between two
+ * pools of the same block shape:
+ *   - copy-on-write: before a new token is written into a block that other
+ *     sequences also reference, the writer gets its own copy of the block
+ *     ("vLLM 架构源码解析（一）" §4.3.2, parallel sampling), src_pool ==
+ *     dst_pool;
+ *   - swap-out / swap-in of a preempted request ("vLLM 架构源码解析（一）"
+ *     §1.1, v0 preemption by swapping the KV cache to CPU memory), one pool
+ *     on the device and the other in pinned host memory.
+ *   dst_pool[d][...] = src_pool[s][...] for every pair (s, d): a bit copy of
+ *   2 * 16 * num_kv_heads * head_dim bf16.
+ *
+ * dst_pool, src_pool  pools [num_blocks][2][16][num_kv_heads][head_dim] bf16:
+ *                     device memory, or pinned host memory the device can
+ *                     address with the same pointer (unified addressing).
+ * dst_num_blocks, src_num_blocks  pool sizes, for the range checks.
+ * block_pairs         device int32 [num_pairs][2] = (source block, destination
+ *                     block). A pair out of range is skipped and sets
+ *                     PKV_DEVERR_BLOCK_RANGE. Pairs with the same destination,
+ *                     or a destination that is another pair's source within one
+ *                     call, race (undefined contents).
+ * layout              block shape; its num_blocks field is ignored.
+ */
+int32_t pkv_copy_blocks(void* dst_pool, int32_t dst_num_blocks, const void* src_pool,
+                        int32_t src_num_blocks, const int32_t* block_pairs,
+                        int32_t num_pairs, pkv_cache_layout layout, void* stream);
+
+/*
  * pkv_attention_workspace_size -- bytes of device workspace that
  * pkv_paged_attention needs for `num_reqs` requests on the current device
  * with the given options (NULL = defaults). Returns a negative status on bad

@@ -19,6 +19,7 @@ from .paged_oracle import (  # noqa: F401
     slot_of,
     slot_mapping,
     kv_write,
+    copy_blocks,
     gather_request_kv,
     attend_rows,
     paged_attention,

@@ -111,6 +111,17 @@ def kv_write(kv_cache: np.ndarray, k: np.ndarray, v: np.ndarray,
     return out
 
 
+def copy_blocks(dst_pool: np.ndarray, src_pool: np.ndarray, pairs) -> np.ndarray:
+    """Return a copy of dst_pool with block d replaced by src_pool's block s
+    for every pair (s, d), in order: copy-on-write of a shared block before a
+    write ([P1] §4.3.2) and swap-out / swap-in of a preempted request's blocks
+    between device and host memory ([P1] §1.1)."""
+    out = dst_pool.copy()
+    for s, d in np.asarray(pairs, dtype=np.int64).reshape(-1, 2):
+        out[d] = src_pool[s]
+    return out
+
+
 def gather_request_kv(kv_cache: np.ndarray, table_row: np.ndarray,
                       seq_len: int) -> np.ndarray:
     """Logical-order copy of one request's cached K/V: uint16 [L, 2, Hkv, D].

@@ -56,6 +56,8 @@ _SIGNATURES = {
                                     c_i32, c_float, pkv_cache_layout, c_void_p, c_size_t,
                                     ctypes.POINTER(pkv_attention_options), c_void_p]),
     "pkv_get_device_errors": (c_i32, [ctypes.POINTER(c_u32), c_i32, c_void_p]),
+    "pkv_copy_blocks": (c_i32, [c_void_p, c_i32, c_void_p, c_i32, c_void_p, c_i32,
+                                pkv_cache_layout, c_void_p]),
     "pkv_paged_attention_static_workspace": (
         c_i32, [c_void_p, c_void_p, c_i64, c_void_p, c_void_p, c_i32, c_void_p, c_void_p,
                 c_void_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_float, pkv_cache_layout,
@@ -159,6 +161,25 @@ def pkv_paged_kv_write(kv_cache, key, value, slot_mapping, stream=None):
     _check("pkv_paged_kv_write", load().pkv_paged_kv_write(
         _ptr(kv_cache), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
         _ptr(slot_mapping), key.shape[0], lay, _stream(stream)))
+
+
+def pkv_copy_blocks(dst_pool, src_pool, block_pairs, stream=None):
+    """dst_pool[d] = src_pool[s] for each (s, d) row of block_pairs (int32
+    [n, 2] on the device). Pools are CUDA tensors or pinned host tensors."""
+    for t, n in ((dst_pool, "dst_pool"), (src_pool, "src_pool")):
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{n} must be bfloat16")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{n} must be a CUDA tensor or pinned host memory")
+    _require(block_pairs, torch.int32, "block_pairs")
+    if block_pairs.dim() != 2 or block_pairs.shape[1] != 2 or not block_pairs.is_contiguous():
+        raise ValueError("block_pairs must be a contiguous [n, 2] int32 tensor")
+    lay = layout_of(src_pool)
+    if tuple(dst_pool.shape[1:]) != tuple(src_pool.shape[1:]) or not dst_pool.is_contiguous():
+        raise ValueError("pools must share the block shape")
+    _check("pkv_copy_blocks", load().pkv_copy_blocks(
+        _ptr(dst_pool), dst_pool.shape[0], _ptr(src_pool), src_pool.shape[0],
+        _ptr(block_pairs), block_pairs.shape[0], lay, _stream(stream)))
 
 
 def _options(decode_warps, trace_events=None):

@@ -241,6 +241,28 @@ int32_t pkv_paged_kv_write(void* kv_cache, const void* key, const void* value,
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_write launch");
 }
 
+int32_t pkv_copy_blocks(void* dst_pool, int32_t dst_num_blocks, const void* src_pool,
+                        int32_t src_num_blocks, const int32_t* block_pairs, int32_t num_pairs,
+                        pkv_cache_layout layout, void* stream) {
+  pkv_cache_layout l = layout;
+  l.num_blocks = dst_num_blocks > 0 ? dst_num_blocks : 1;
+  int32_t st = check_layout(l);
+  if (st != PKV_OK) return st;
+  if (dst_num_blocks < 1 || src_num_blocks < 1 || num_pairs < 0) return PKV_ERR_BAD_SHAPE;
+  if (static_cast<long long>(src_num_blocks) * 32 >= (1ll << 31)) return PKV_ERR_BAD_SHAPE;
+  if (num_pairs == 0) return PKV_OK;
+  if (!dst_pool || !src_pool || !block_pairs) return PKV_ERR_NULL_POINTER;
+  if (!aligned16(dst_pool) || !aligned16(src_pool)) return PKV_ERR_MISALIGNED;
+  DeviceInfo* d;
+  st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = pkv::launch_copy_blocks(dst_pool, dst_num_blocks, src_pool, src_num_blocks,
+                                          block_pairs, num_pairs, layout.num_kv_heads,
+                                          layout.head_dim, d->num_sms,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "copy_blocks launch");
+}
+
 int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
                                      pkv_cache_layout layout,
                                      const pkv_attention_options* options) {

@@ -620,11 +620,13 @@ constexpr size_t decode_smem_bytes() {
 }
 
 template <int D, int GW>
+static std::atomic<unsigned long long> g_decode_attr_done{0};
+
+template <int D, int GW>
 static cudaError_t decode_occupancy(int* ctas_per_sm) {
   auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps>;
   const size_t smem = decode_smem_bytes<D, GW>();
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = smem_attr_once(kern, static_cast<int>(smem), g_decode_attr_done<D, GW>);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, kern, kDecodeWarps * 32, smem);
 }
@@ -656,8 +658,7 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_
                                    cudaStream_t stream, void** trace) {
   auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps>;
   const size_t smem = decode_smem_bytes<D, GW>();
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = smem_attr_once(kern, static_cast<int>(smem), g_decode_attr_done<D, GW>);
   if (e != cudaSuccess) return e;
   const long long grid = (p.warps + kDecodeWarps - 1) / kDecodeWarps;
   kern<<<static_cast<unsigned>(grid), kDecodeWarps * 32, smem, stream>>>(kv_map, p);

@@ -83,6 +83,38 @@ __global__ void kv_write_kernel(uint4* __restrict__ pool, const uint4* __restric
   }
 }
 
+// Whole-block copies between two pools of one layout (copy-on-write of a
+// shared block; swap-out / swap-in between the device pool and a pool in
+// pinned host memory). One CTA per pair: 16-byte vectors, coalesced on both
+// sides. vec_per_block = 2 * 16 * Hkv * D / 8.
+__global__ void copy_blocks_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                   const int32_t* __restrict__ pairs, int num_pairs,
+                                   int dst_num_blocks, int src_num_blocks, int vec_per_block) {
+  for (int i = blockIdx.x; i < num_pairs; i += gridDim.x) {
+    const int s = __ldg(pairs + 2 * i), d = __ldg(pairs + 2 * i + 1);
+    if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks) {
+      if (threadIdx.x == 0) atomicOr(&g_errors_kvwrite, kErrBlockRange);
+      continue;
+    }
+    const uint4* from = src + static_cast<long long>(s) * vec_per_block;
+    uint4* to = dst + static_cast<long long>(d) * vec_per_block;
+    for (int e = threadIdx.x; e < vec_per_block; e += blockDim.x) to[e] = from[e];
+  }
+}
+
+cudaError_t launch_copy_blocks(void* dst, int dst_num_blocks, const void* src, int src_num_blocks,
+                               const int32_t* pairs, int num_pairs, int num_kv_heads,
+                               int head_dim, int num_sms, cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  const int vec_per_block = 2 * kBlockSize * num_kv_heads * head_dim / 8;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  const int grid = static_cast<int>(num_pairs < cap ? num_pairs : cap);
+  copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(dst),
+                                               static_cast<const uint4*>(src), pairs, num_pairs,
+                                               dst_num_blocks, src_num_blocks, vec_per_block);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int max_blocks,
                                 const int32_t* qsl, const int32_t* num_computed, int num_reqs,
                                 int num_tokens, int num_blocks, cudaStream_t stream) {

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace pkv {
 
 // Header words at the start of the attention workspace (written by the plan
@@ -43,6 +45,21 @@ struct AttnArgs {
   float scale;
 };
 
+// Raise a kernel's dynamic shared memory limit once per device: `done` is a
+// per-kernel bit mask of devices already set up, so later launches (also
+// those recorded into a CUDA graph) make no attribute call.
+template <typename Kernel>
+inline cudaError_t smem_attr_once(Kernel kern, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 // Heads handled together by one decode warp, and head groups per kv head.
 inline int decode_heads_per_warp(int group) { return group < 4 ? group : 4; }
 
@@ -59,6 +76,10 @@ cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long
                             long long value_stride, const int64_t* slots, int num_tokens,
                             int num_blocks, int num_kv_heads, int head_dim, int num_sms,
                             cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* dst, int dst_num_blocks, const void* src, int src_num_blocks,
+                               const int32_t* pairs, int num_pairs, int num_kv_heads,
+                               int head_dim, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream);
 

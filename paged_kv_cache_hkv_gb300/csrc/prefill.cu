@@ -591,7 +591,8 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& k
                                     const CUtensorMap& q_map, int grid, cudaStream_t stream) {
   auto kern = prefill_kernel<D>;
   const int smem = static_cast<int>(PrefillLayout<D>::kAlloc);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = smem_attr_once(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, stream>>>(kv_map, q_map, p);
   return cudaGetLastError();

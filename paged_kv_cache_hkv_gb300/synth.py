@@ -341,6 +341,12 @@ def mixed_step(seed: int = 3, num_decodes: int = 1280, **kw) -> PagedStep:
     return make_step(mixed_step_specs(seed, num_decodes), seed=seed, **LLAMA, **kw)
 
 
+def prefill_rows(seed: int = 3, **kw) -> PagedStep:
+    """The mixed step's prefill requests alone: the 512-token chunk over 1536
+    cached tokens and the 8 fresh 64-token prefills."""
+    return make_step(mixed_step_specs(seed, num_decodes=0), seed=seed, **LLAMA, **kw)
+
+
 def prefix_sharing(seed: int = 4, **kw) -> PagedStep:
     """128 decodes sharing a 1024-token (64-block) prefix, private suffixes of
     16..256 tokens."""
@@ -361,6 +367,7 @@ WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama_decode": llama_decode,
     "mixed_step": mixed_step,
+    "prefill_rows": prefill_rows,
     "prefix_sharing": prefix_sharing,
     "long_context": long_context,
 }

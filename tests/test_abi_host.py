@@ -114,6 +114,17 @@ def test_slot_mapping_and_errors_reject_bad_arguments(lib):
     assert lib.pkv_get_device_errors(None, 0, None) == E("PKV_ERR_NULL_POINTER")
 
 
+def test_copy_blocks_rejects_bad_arguments(lib):
+    E = header_define
+    C = lib.pkv_copy_blocks
+    assert C(FAKE, 4, FAKE, 4, FAKE, 2, _layout(bs=8), None) == E("PKV_ERR_UNSUPPORTED")
+    assert C(FAKE, 0, FAKE, 4, FAKE, 2, _layout(), None) == E("PKV_ERR_BAD_SHAPE")
+    assert C(FAKE, 4, FAKE, 4, FAKE, -1, _layout(), None) == E("PKV_ERR_BAD_SHAPE")
+    assert C(FAKE, 4, None, 4, FAKE, 2, _layout(), None) == E("PKV_ERR_NULL_POINTER")
+    assert C(FAKE, 4, MISALIGNED, 4, FAKE, 2, _layout(), None) == E("PKV_ERR_MISALIGNED")
+    assert C(None, 4, None, 4, None, 0, _layout(), None) == E("PKV_OK")
+
+
 def test_no_gpu_means_an_error_not_a_fallback(lib):
     import torch
     if torch.cuda.is_available():

@@ -231,3 +231,80 @@ def test_mixed_batch_order_independence():
     run_and_check(step)
     rev = make_step(specs[::-1], num_q_heads=32, num_kv_heads=8, head_dim=128, seed=61)
     run_and_check(rev, decode_warps=9)
+
+
+# ---------------------------------------------------------------- block copies
+def _rand_pool(nb, hkv=8, d=128, seed=0, device="cuda", pinned=False):
+    g = torch.Generator().manual_seed(seed)
+    t = torch.randn((nb, 2, 16, hkv, d), generator=g).to(torch.bfloat16)
+    if pinned:
+        return t.pin_memory()
+    return t.to(device)
+
+
+def _host_bits(t):
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_copy_blocks_copy_on_write_in_pool():
+    import oracle
+    pool = _rand_pool(300, seed=1)
+    before = _host_bits(pool)
+    rng = np.random.default_rng(5)
+    ids = rng.permutation(300)
+    pairs = np.stack([ids[:60], ids[60:120]], axis=1).astype(np.int32)  # disjoint src / dst
+    binding.pkv_copy_blocks(pool, pool, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_errors(clear=True) == 0
+    assert np.array_equal(_host_bits(pool), oracle.copy_blocks(before, before, pairs))
+
+
+def test_copy_blocks_swap_out_and_in_with_pinned_host_pool():
+    import oracle
+    dev = _rand_pool(200, hkv=4, d=64, seed=2)
+    host = _rand_pool(50, hkv=4, d=64, seed=3, pinned=True)
+    dev_bits, host_bits = _host_bits(dev), _host_bits(host)
+    out_pairs = np.array([[17, 0], [150, 1], [3, 49], [199, 20]], np.int32)
+    binding.pkv_copy_blocks(host, dev, torch.from_numpy(out_pairs).cuda())
+    torch.cuda.synchronize()
+    host_after = oracle.copy_blocks(host_bits, dev_bits, out_pairs)
+    assert np.array_equal(_host_bits(host), host_after)
+    in_pairs = np.array([[0, 5], [49, 6], [20, 7]], np.int32)
+    binding.pkv_copy_blocks(dev, host, torch.from_numpy(in_pairs).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(_host_bits(dev), oracle.copy_blocks(dev_bits, host_after, in_pairs))
+    assert binding.pkv_get_device_errors(clear=True) == 0
+
+
+def test_copy_blocks_out_of_range_pair_is_skipped_and_flagged():
+    pool = _rand_pool(10, hkv=2, d=64, seed=4)
+    before = _host_bits(pool)
+    pairs = torch.tensor([[2, 10], [-1, 3]], dtype=torch.int32, device="cuda")
+    binding.pkv_copy_blocks(pool, pool, pairs)
+    assert binding.pkv_get_device_errors(clear=True) & binding.DEVERR_BLOCK_RANGE
+    assert np.array_equal(_host_bits(pool), before)
+
+
+# ---------------------------------------------------------------- CUDA graphs
+def test_mixed_step_replays_in_a_cuda_graph():
+    specs = [RequestSpec(300, 45), RequestSpec(0, 17), RequestSpec(1000, 1), RequestSpec(63, 1),
+             RequestSpec(4000, 1)]
+    step = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=131)
+    ds = DeviceStep(step)
+    ds.run()
+    torch.cuda.synchronize()
+    eager = ds.out_host().copy()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ds.run()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ds.run()
+    for _ in range(2):
+        ds.out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(ds.out_host(), eager)
+    assert binding.pkv_get_device_errors(clear=True) == 0

@@ -411,3 +411,48 @@ def test_planted_slot_mistake_is_caught(monkeypatch):
     g = _load("slot_mapping_worked_example.json")
     bt = np.array(g["block_table"], np.int32)
     assert any(po.slot_of(bt[e["request"]], e["pos"]) != e["slot"] for e in g["slots"])
+
+
+# ---------------------------------------------------------------------------
+# block copies (copy-on-write, swap)
+# ---------------------------------------------------------------------------
+
+def test_copy_blocks_moves_whole_blocks_only():
+    rng = np.random.default_rng(41)
+    src = rand_bits(rng, (9, 2, 16, 2, 8))
+    dst = rand_bits(rng, (7, 2, 16, 2, 8))
+    pairs = [(3, 0), (8, 6), (3, 2)]
+    out = oracle.copy_blocks(dst, src, pairs)
+    for s_, d in pairs:
+        assert np.array_equal(out[d], src[s_])
+    for d in (1, 3, 4, 5):
+        assert np.array_equal(out[d], dst[d])
+
+
+def test_copy_on_write_keeps_the_sharer_intact():
+    """Two sequences share a partly filled block; the one that writes first
+    gets its own copy ([P1] §4.3.2). Afterwards the other one still sees the
+    original block and the writer sees its copy plus its new token, exactly
+    as if it had owned private blocks from the start."""
+    rng = np.random.default_rng(42)
+    B, Hkv, D, Hq = 16, 2, 8, 4
+    prefix = rand_bits(rng, (24, 2, Hkv, D))  # 1.5 blocks: the second block is shared and partial
+    pool = np.full((10, 2, B, Hkv, D), BF16_NAN, np.uint16)
+    scatter(pool, [4, 7], prefix)
+    new_kv = rand_bits(rng, (1, 2, Hkv, D))
+    pool_cow = oracle.copy_blocks(pool, pool, [(7, 9)])  # the writer's copy of block 7
+    slot = oracle.slot_of(np.array([4, 9]), 24)
+    pool_cow = oracle.kv_write(pool_cow, new_kv[:, 0], new_kv[:, 1], np.array([slot]))
+    assert np.array_equal(pool_cow[7], pool[7])  # the sharer's block is untouched
+    q = rand_bits(rng, (2, Hq, D))
+    bt = np.array([[4, 7, -1], [4, 9, -1]], np.int32)
+    out = oracle.paged_attention(q, pool_cow, bt, np.array([24, 25], np.int32),
+                                 np.array([0, 1, 2], np.int32), np.array([23, 24], np.int32), 0.3)
+    # reference: the sharer alone, and the writer with private blocks from the start
+    ref_pool = np.full_like(pool, BF16_NAN)
+    scatter(ref_pool, [1, 2], np.concatenate([prefix, new_kv]))
+    scatter(ref_pool, [5, 6], prefix)
+    ref = oracle.paged_attention(q, ref_pool, np.array([[5, 6, -1], [1, 2, -1]], np.int32),
+                                 np.array([24, 25], np.int32), np.array([0, 1, 2], np.int32),
+                                 np.array([23, 24], np.int32), 0.3)
+    assert np.array_equal(out, ref)
