@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", default="mixed_step", choices=sorted(synth.WORKLOADS))
     p.add_argument("--seed", type=int, default=None)
+    p.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32],
+                   help="tokens per cache block")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -104,6 +106,30 @@ def step_work(step):
         "write_bytes": 2 * step.num_tokens * Hkv * D * 2 * 2,
         "tokens": step.num_tokens,
     }
+
+
+def block_tradeoff(step):
+    """The block-size trade-off of one step's cache: slots allocated but
+    holding no token (internal fragmentation of last blocks) and the block
+    table entries the attention reads.
+
+    Blocks shared by several requests count once; a block's stored tokens
+    are the most any request keeps in it."""
+    B = step.block_size
+    fill = {}
+    entries = 0
+    for r in range(step.num_reqs):
+        L = int(step.seq_lens[r])
+        n = -(-L // B)
+        entries += n
+        for j in range(n):
+            blk = int(step.block_table[r, j])
+            fill[blk] = max(fill.get(blk, 0), min(B, L - j * B))
+    allocated = len(fill) * B
+    stored = sum(fill.values())
+    return {"table_entries_read": entries, "blocks_in_use": len(fill),
+            "slots_allocated": allocated,
+            "slots_wasted_frac": (allocated - stored) / allocated if allocated else 0.0}
 
 
 def kernels_per_step(step):
@@ -199,7 +225,8 @@ def time_oracle_sample(step_specs, shape, seed, per_class):
         pos = {i: k for k, i in enumerate(reqs)}
         sel = [int(sub.query_start_loc[pos[i]]) + j for i, j in rows]
         t0 = time.perf_counter()
-        slots = oracle.slot_mapping(sub.block_table, sub.query_start_loc, sub.num_computed)
+        slots = oracle.slot_mapping(sub.block_table, sub.query_start_loc, sub.num_computed,
+                                    sub.block_size)
         pool = oracle.kv_write(sub.kv_cache, sub.k, sub.v, slots)
         oracle.paged_attention(sub.q, pool, sub.block_table, sub.seq_lens, sub.query_start_loc,
                                sub.num_computed, sub.scale, rows=sel)
@@ -211,7 +238,7 @@ def time_oracle_sample(step_specs, shape, seed, per_class):
 
 def shape_of(step):
     return dict(num_q_heads=step.num_q_heads, num_kv_heads=step.num_kv_heads,
-                head_dim=step.head_dim)
+                head_dim=step.head_dim, block_size=step.block_size)
 
 
 # ------------------------------------------------------------------ reference arm
@@ -221,7 +248,8 @@ def run_reference(args):
         return 0
     seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3}.get(
         args.workload, 0)
-    meta = synth.WORKLOADS[args.workload](seed=seed, materialize=False)
+    meta = synth.WORKLOADS[args.workload](seed=seed, materialize=False,
+                                          block_size=args.block_size)
     shape = shape_of(meta)
     per = {"decode": 4, "chunk": 8, "prefill": 4}
     for w in range(args.warmup):
@@ -238,7 +266,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "tokens_per_step": meta.num_tokens},
+        "config": {"workload": args.workload, "tokens_per_step": meta.num_tokens,
+                   "block_size": args.block_size},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "per step: " + desc + " (step time extrapolated by class)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -287,7 +316,7 @@ def run_native(args):
                                                          "prefix_sharing": 4,
                                                          "long_context": 5}[args.workload]
     seed = replica_seed(base_seed, rank)
-    step = synth.WORKLOADS[args.workload](seed=seed)
+    step = synth.WORKLOADS[args.workload](seed=seed, block_size=args.block_size)
     ds = DeviceStep(step)
     binding.pkv_get_device_errors(clear=True)
     work = step_work(step)
@@ -373,8 +402,11 @@ def run_native(args):
         hbm_peak, peak_src = 6800.0, "fallback"
     dec_ms = per_kernel[2]
     dec_gbs = work["decode_kv_bytes"] / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
-    traffic = traffic_from_profile(os.path.join(ROOT, "paged_kv_cache_hkv_gb300", "csrc",
-                                                "decode.cu"))
+    # the committed counters cover the default mixed step only
+    traffic = None
+    if args.workload == "mixed_step" and args.block_size == 16 and args.seed is None:
+        traffic = traffic_from_profile(os.path.join(ROOT, "paged_kv_cache_hkv_gb300", "csrc",
+                                                    "decode.cu"))
     roofline = {"kernel": "decode_kernel", "bound": "hbm", "achieved": dec_gbs,
                 "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
                 "frac": dec_gbs / hbm_peak if dec_gbs else None, "traffic": traffic,
@@ -406,6 +438,7 @@ def run_native(args):
                    "decode_kv_bytes_per_step": work["decode_kv_bytes"],
                    "prefill_flops_per_step": work["prefill_flops"],
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "block_tradeoff": block_tradeoff(step),
         "decode_kv_read_gbs": dec_gbs,
         "kernel_ms": {"plan": per_kernel[0], "prefill": per_kernel[1],
                       "decode": per_kernel[2], "combine": per_kernel[3]},

@@ -24,8 +24,11 @@
  * Pool layout (the pages' physical KV cache, "vllm v1 源码精读（三）", §3.3):
  *   kv_cache[num_blocks][2][block_size][num_kv_heads][head_dim], bf16,
  *   contiguous; index 0 of the second dimension holds K, 1 holds V.
- *   block_size must be 16 (the pages' default, "vLLM 架构源码解析（一）" §1.1,
- *   §5.1); head_dim must be 64 or 128.
+ *   block_size (B) is 8, 16 or 32 tokens: 16 is the pages' default and 8
+ *   and 32 the two other points of "vLLM 架构源码解析（一）" §5.1 (less
+ *   last-block waste vs fewer block-table entries); other sizes return
+ *   PKV_ERR_UNSUPPORTED. num_blocks * 2 * B must stay below 2^31.
+ *   head_dim must be 64 or 128.
  */
 #ifndef PAGEDKV_H_
 #define PAGEDKV_H_
@@ -66,7 +69,7 @@ extern "C" {
 /* Shape of the physical pool. */
 typedef struct pkv_cache_layout {
   int32_t num_blocks;   /* physical blocks in the pool, >= 1                  */
-  int32_t block_size;   /* tokens per block; must be 16                       */
+  int32_t block_size;   /* tokens per block: 8, 16 or 32                       */
   int32_t num_kv_heads; /* kv heads per token                                 */
   int32_t head_dim;     /* 64 or 128                                          */
 } pkv_cache_layout;
@@ -118,6 +121,7 @@ const char* pkv_last_cuda_error(void);
  * query_start_loc     device int32 [num_reqs + 1], non-decreasing, [0] = 0.
  * num_computed_tokens device int32 [num_reqs].
  * num_blocks          pool size, for the range check.
+ * block_size          tokens per block: 8, 16 or 32 (else PKV_ERR_UNSUPPORTED).
  */
 int32_t pkv_slot_mapping(int64_t* slot_mapping, const int32_t* block_table,
                          int32_t max_blocks_per_req,
@@ -130,9 +134,10 @@ int32_t pkv_slot_mapping(int64_t* slot_mapping, const int32_t* block_table,
  * pkv_paged_kv_write -- reshape_and_cache: store each new token's K and V rows
  * into the pool at its slot ("vLLM 架构源码解析（一）" §3.3.3 step 2;
  * "vllm v1 源码精读（三）" §3.4, reshape_and_cache_flash). A bit copy:
- *   kv_cache[s / 16][0][s % 16][:][:] = key[t],  [..][1][..] = value[t]
- * for every t with s = slot_mapping[t] >= 0. Negative slots are skipped;
- * slots >= num_blocks * 16 are skipped and set PKV_DEVERR_SLOT_RANGE. Two
+ *   kv_cache[s / B][0][s % B][:][:] = key[t],  [..][1][..] = value[t]
+ * for every t with s = slot_mapping[t] >= 0 (B = layout.block_size).
+ * Negative slots are skipped; slots >= num_blocks * B are skipped and set
+ * PKV_DEVERR_SLOT_RANGE. Two
  * tokens with the same slot race (undefined which wins).
  *
  * kv_cache      in/out, device bf16 pool (layout above).
@@ -156,9 +161,9 @@ int32_t pkv_paged_kv_write(void* kv_cache, const void* key, const void* value,
  *     §1.1, v0 preemption by swapping the KV cache to CPU memory), one pool
  *     on the device and the other in pinned host memory.
  *   dst_pool[d][...] = src_pool[s][...] for every pair (s, d): a bit copy of
- *   2 * 16 * num_kv_heads * head_dim bf16.
+ *   2 * B * num_kv_heads * head_dim bf16.
  *
- * dst_pool, src_pool  pools [num_blocks][2][16][num_kv_heads][head_dim] bf16:
+ * dst_pool, src_pool  pools [num_blocks][2][B][num_kv_heads][head_dim] bf16:
  *                     device memory, or pinned host memory the device can
  *                     address with the same pointer (unified addressing).
  * dst_num_blocks, src_num_blocks  pool sizes, for the range checks.
@@ -197,7 +202,7 @@ int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
  * (batch row query_start_loc[r] + i, absolute position c + i) and q head h
  * attend keys j = 0 .. c + i of kv head h / (num_q_heads / num_kv_heads):
  *   out = sum_j softmax_j(scale * q . k_j) v_j,
- * key j read from block block_table[r][j / 16], offset j % 16.
+ * key j read from block block_table[r][j / B], offset j % B.
  * Rows with n == 1 run on the split-KV decode kernels (+ combine); rows of
  * requests with n > 1 run on the tensor-core prefill kernel.
  *
@@ -207,7 +212,8 @@ int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
  *                q + t * q_row_stride (0 = num_q_heads * head_dim).
  * kv_cache       device bf16 pool (layout above), read only.
  * block_table    device int32 [num_reqs][max_blocks_per_req], -1 = unused;
- *                entries from ceil(L / 16) on are never read.
+ *                entries from ceil(L / B) on are never read;
+ *                max_seq_len <= max_blocks_per_req * B.
  * seq_lens, query_start_loc, num_computed_tokens: device int32 as above.
  * num_tokens     rows of q / out (>= query_start_loc[num_reqs]).
  * max_query_len  host hint: >= every n (like max_seqlen_q).

@@ -24,7 +24,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct DeviceInfo {
   int num_sms = 0;
   bool ok = false;
-  int full_wave_warps[2][4] = {};  // [D==128][log2 heads per warp]
+  int full_wave_warps[2][3][3] = {};  // [D==128][log2 heads per warp][log2 B - 3]
 };
 
 constexpr int kMaxDevices = 64;
@@ -100,12 +100,18 @@ int32_t make_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, u
   return PKV_OK;
 }
 
+bool block_size_ok(int32_t b) { return b == 8 || b == 16 || b == 32; }
+
+int block_shift_of(int32_t b) { return b == 8 ? 3 : (b == 16 ? 4 : 5); }
+
 int32_t check_layout(const pkv_cache_layout& l) {
   if (l.num_blocks < 1 || l.num_kv_heads < 1 || l.head_dim < 1 || l.block_size < 1)
     return PKV_ERR_BAD_SHAPE;
-  if (l.block_size != 16) return PKV_ERR_UNSUPPORTED;
+  if (!block_size_ok(l.block_size)) return PKV_ERR_UNSUPPORTED;
   if (l.head_dim != 64 && l.head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (static_cast<long long>(l.num_blocks) * 32 >= (1ll << 31)) return PKV_ERR_BAD_SHAPE;
+  // pool rows (block * 2 + k|v) * B + offset are 32-bit TMA coordinates
+  if (static_cast<long long>(l.num_blocks) * 2 * l.block_size >= (1ll << 31))
+    return PKV_ERR_BAD_SHAPE;
   return PKV_OK;
 }
 
@@ -137,7 +143,7 @@ WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long
   return w;
 }
 
-int32_t decode_warps_for(DeviceInfo* d, int head_dim, int group,
+int32_t decode_warps_for(DeviceInfo* d, int head_dim, int group, int block_size,
                          const pkv_attention_options* opt, long long* warps) {
   if (opt) {
     for (int i = 0; i < 7; ++i)
@@ -152,10 +158,11 @@ int32_t decode_warps_for(DeviceInfo* d, int head_dim, int group,
   const int gw = pkv::decode_heads_per_warp(group);
   const int gi = gw == 4 ? 2 : (gw == 2 ? 1 : 0);
   std::lock_guard<std::mutex> lock(g_mu);
-  int& cached = d->full_wave_warps[di][gi];
+  const int sh = block_shift_of(block_size);
+  int& cached = d->full_wave_warps[di][gi][sh - 3];
   if (cached == 0) {
     int w = 0;
-    cudaError_t e = pkv::decode_full_wave_warps(head_dim, group, d->num_sms, &w);
+    cudaError_t e = pkv::decode_full_wave_warps(head_dim, group, sh, d->num_sms, &w);
     if (e != cudaSuccess) return cuda_fail(e, "decode occupancy");
     cached = w;
   }
@@ -201,7 +208,8 @@ int32_t pkv_slot_mapping(int64_t* slot_mapping, const int32_t* block_table,
                          void* stream) {
   if (num_tokens < 0 || num_reqs < 0 || max_blocks_per_req < 0 || num_blocks < 1)
     return PKV_ERR_BAD_SHAPE;
-  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  if (block_size < 1) return PKV_ERR_BAD_SHAPE;
+  if (!block_size_ok(block_size)) return PKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PKV_OK;
   if (!slot_mapping || !query_start_loc) return PKV_ERR_NULL_POINTER;
   if (num_reqs > 0 && (!block_table || !num_computed_tokens)) return PKV_ERR_NULL_POINTER;
@@ -210,7 +218,7 @@ int32_t pkv_slot_mapping(int64_t* slot_mapping, const int32_t* block_table,
   if (st != PKV_OK) return st;
   cudaError_t e = pkv::launch_slot_mapping(slot_mapping, block_table, max_blocks_per_req,
                                            query_start_loc, num_computed_tokens, num_reqs,
-                                           num_tokens, num_blocks,
+                                           num_tokens, num_blocks, block_size,
                                            static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "slot_mapping launch");
 }
@@ -236,7 +244,8 @@ int32_t pkv_paged_kv_write(void* kv_cache, const void* key, const void* value,
   if (st != PKV_OK) return st;
   cudaError_t e = pkv::launch_kv_write(kv_cache, key, value, key_row_stride, value_row_stride,
                                        slot_mapping, num_tokens, layout.num_blocks,
-                                       layout.num_kv_heads, layout.head_dim, d->num_sms,
+                                       layout.block_size, layout.num_kv_heads, layout.head_dim,
+                                       d->num_sms,
                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_write launch");
 }
@@ -249,7 +258,8 @@ int32_t pkv_copy_blocks(void* dst_pool, int32_t dst_num_blocks, const void* src_
   int32_t st = check_layout(l);
   if (st != PKV_OK) return st;
   if (dst_num_blocks < 1 || src_num_blocks < 1 || num_pairs < 0) return PKV_ERR_BAD_SHAPE;
-  if (static_cast<long long>(src_num_blocks) * 32 >= (1ll << 31)) return PKV_ERR_BAD_SHAPE;
+  if (static_cast<long long>(src_num_blocks) * 2 * layout.block_size >= (1ll << 31))
+    return PKV_ERR_BAD_SHAPE;
   if (num_pairs == 0) return PKV_OK;
   if (!dst_pool || !src_pool || !block_pairs) return PKV_ERR_NULL_POINTER;
   if (!aligned16(dst_pool) || !aligned16(src_pool)) return PKV_ERR_MISALIGNED;
@@ -257,8 +267,8 @@ int32_t pkv_copy_blocks(void* dst_pool, int32_t dst_num_blocks, const void* src_
   st = device_info(&d);
   if (st != PKV_OK) return st;
   cudaError_t e = pkv::launch_copy_blocks(dst_pool, dst_num_blocks, src_pool, src_num_blocks,
-                                          block_pairs, num_pairs, layout.num_kv_heads,
-                                          layout.head_dim, d->num_sms,
+                                          block_pairs, num_pairs, layout.block_size,
+                                          layout.num_kv_heads, layout.head_dim, d->num_sms,
                                           static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "copy_blocks launch");
 }
@@ -276,7 +286,7 @@ int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
   if (st != PKV_OK) return st;
   const int group = num_q_heads / layout.num_kv_heads;
   long long warps = 0;
-  st = decode_warps_for(d, layout.head_dim, group, options, &warps);
+  st = decode_warps_for(d, layout.head_dim, group, layout.block_size, options, &warps);
   if (st != PKV_OK) return st;
   const int gw = pkv::decode_heads_per_warp(group);
   const int virt = layout.num_kv_heads * (group / gw);
@@ -303,7 +313,8 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   if (q_row_stride == 0) q_row_stride = row;
   if (q_row_stride < row) return PKV_ERR_BAD_SHAPE;
   if (num_reqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
-  if (static_cast<long long>(max_seq_len) > static_cast<long long>(max_blocks_per_req) * 16)
+  if (static_cast<long long>(max_seq_len) >
+      static_cast<long long>(max_blocks_per_req) * layout.block_size)
     return PKV_ERR_BAD_SHAPE;
   if (!out || !q || !kv_cache || !block_table || !seq_lens || !query_start_loc ||
       !num_computed_tokens)
@@ -317,7 +328,7 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   if (st != PKV_OK) return st;
   const int group = num_q_heads / layout.num_kv_heads;
   long long warps = 0;
-  st = decode_warps_for(d, layout.head_dim, group, options, &warps);
+  st = decode_warps_for(d, layout.head_dim, group, layout.block_size, options, &warps);
   if (st != PKV_OK) return st;
   const int gw = pkv::decode_heads_per_warp(group);
   const int virt = layout.num_kv_heads * (group / gw);
@@ -352,14 +363,21 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   a.num_kv_heads = layout.num_kv_heads;
   a.head_dim = layout.head_dim;
   a.num_blocks = layout.num_blocks;
+  a.block_shift = block_shift_of(layout.block_size);
   a.scale = scale;
 
   const int D = layout.head_dim, Hkv = layout.num_kv_heads;
   const uint64_t row_bytes = static_cast<uint64_t>(Hkv) * D * 2;
-  // pool as rows of one kv head: {d, kv head, (block*2 + k|v)*16 + offset}
+  // pool as rows of one kv head: {d, kv head, (block*2 + k|v)*B + offset}.
+  // A decode copy is a block's 32 K and V rows (B = 16), 16 rows (half of the
+  // K or V rows of a 32-token block) or the 16 K and V rows of an 8-token
+  // block.
+  const int B = layout.block_size;
+  const uint64_t pool_rows = static_cast<uint64_t>(layout.num_blocks) * 2 * B;
+  const uint32_t dec_box = B == 16 ? 32u : 16u;
   CUtensorMap kv_map;
-  st = make_map(&kv_map, kv_cache, D, Hkv, static_cast<uint64_t>(layout.num_blocks) * 32,
-                static_cast<uint64_t>(D) * 2, row_bytes, D, 1, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+  st = make_map(&kv_map, kv_cache, D, Hkv, pool_rows, static_cast<uint64_t>(D) * 2, row_bytes, D,
+                1, dec_box, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != PKV_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -372,11 +390,11 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   if (max_query_len > 1) {
-    // pool for the tensor-core path: 64-element (128-byte) swizzled rows
+    // pool for the tensor-core path: 64-element (128-byte) swizzled rows,
+    // 16 rows per copy (8 for 8-token blocks)
     CUtensorMap kv_map_sw, q_map;
-    st = make_map(&kv_map_sw, kv_cache, D, Hkv, static_cast<uint64_t>(layout.num_blocks) * 32,
-                  static_cast<uint64_t>(D) * 2, row_bytes, 64, 1, 16,
-                  CU_TENSOR_MAP_SWIZZLE_128B);
+    st = make_map(&kv_map_sw, kv_cache, D, Hkv, pool_rows, static_cast<uint64_t>(D) * 2,
+                  row_bytes, 64, 1, B == 8 ? 8u : 16u, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != PKV_OK) return st;
     st = make_map(&q_map, q, D, num_q_heads, num_tokens, static_cast<uint64_t>(D) * 2,
                   static_cast<uint64_t>(q_row_stride) * 2, 64, group, 128 / group,

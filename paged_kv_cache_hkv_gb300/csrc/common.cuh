@@ -13,7 +13,10 @@ constexpr uint32_t kErrBlockRange = 0x2u;
 constexpr uint32_t kErrLengths = 0x4u;
 constexpr uint32_t kErrTimeout = 0x8u;
 
-constexpr int kBlockSize = 16;
+// The attention kernels move keys in chunks of 16 (one decode stage, one
+// MMA K step). A cache block holds 8, 16 or 32 tokens, so a chunk is two
+// 8-token blocks, one 16-token block or half of a 32-token block.
+constexpr int kChunkKeys = 16;
 // An on-chip wait that has not completed after this long is treated as lost.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s, when cleaning up

@@ -17,11 +17,16 @@
 // (request, kv head) that falls inside one warp's range is finished there
 // and written straight to the output.
 //
-// Inside a warp: a ring of S shared-memory stages, each holding one block's
-// 16 K rows and 16 V rows of one kv head (one 3-D TMA copy, 2*16*D*2 bytes)
-// plus, on the first block of a piece, the G query rows (one bulk copy).
-// Lane 0 issues the copies S-1 blocks ahead of the block being computed.
-// Online softmax runs in base 2 with q pre-scaled by scale*log2(e).
+// The unit of the stream is a chunk of 16 keys, whatever the cache's block
+// size B: a 16-token block, half of a 32-token block or two 8-token blocks.
+// Inside a warp: a ring of S shared-memory stages, each holding one chunk's
+// 16 K rows and 16 V rows of one kv head (2*16*D*2 bytes; one 3-D TMA copy
+// for B = 16, where K and V of a block are 32 consecutive pool rows; two of
+// 16 rows for B = 32 (half the K rows, half the V rows) and for B = 8 (the
+// 8 K and 8 V rows of each block)) plus, on the first chunk of a piece, the G
+// query rows (one bulk copy). Lane 0 issues the copies S-1 chunks ahead of
+// the chunk being computed. Online softmax runs in base 2 with q pre-scaled
+// by scale*log2(e).
 #include "common.cuh"
 #include "launch.h"
 
@@ -75,14 +80,15 @@ __device__ __forceinline__ Int3 block_exclusive_scan(Int3 v, Int3* total) {
   return Int3{base.a + inc.a - v.a, base.b + inc.b - v.b, base.c + inc.c - v.c};
 }
 
-// Counts of one request: decode blocks, is-prefill, prefill work items.
+// Counts of one request: decode 16-key chunks, is-prefill, prefill work items.
 __device__ __forceinline__ Int3 plan_counts(const AttnArgs& a, int r, int tile_q, bool flag) {
   Int3 v{0, 0, 0};
   const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
   const int n = q1 - q0, L = __ldg(a.seq_lens + r), c = __ldg(a.num_computed + r);
   bool bad = n < 0 || q0 < 0 || q1 > a.num_tokens || c < 0 || L != c + n || (r == 0 && q0 != 0);
-  const long long nblk = (static_cast<long long>(L) + kBlockSize - 1) / kBlockSize;
-  if (!bad && n > 0 && nblk > a.max_blocks) bad = true;
+  const long long nblk = (static_cast<long long>(L) + kChunkKeys - 1) / kChunkKeys;
+  const long long nent = (static_cast<long long>(L) + (1 << a.block_shift) - 1) >> a.block_shift;
+  if (!bad && n > 0 && nent > a.max_blocks) bad = true;
   if (bad) {
     if (flag) atomicOr(&g_errors_decode, kErrLengths);
   } else if (n == 1) {
@@ -169,13 +175,13 @@ struct DecodeCfg {
   static constexpr int NPL = NV >= LPK ? NV / LPK : 1;  // full scores per lane
   static constexpr int DUP = NV >= LPK ? 1 : LPK / NV;  // lanes holding the same score
   static constexpr int LPH = LPK / GW;                  // lanes per head in a sub-group
-  static constexpr uint32_t kKvBytes = 32u * D * 2u;
+  static constexpr uint32_t kKvBytes = 32u * D * 2u;  // K and V rows of one chunk
   static constexpr uint32_t kQBytes = GW * D * 2u;
   static_assert(KPL * KPI == 16, "block of 16 keys");
   static_assert(KPL % NPL == 0, "a lane's scores stay in one head");
 
   struct alignas(128) WarpSmem {
-    uint16_t kv[S][32][D];  // rows 0..15 K, 16..31 V of one kv head
+    uint16_t kv[S][32][D];  // K and V rows of one kv head and chunk (see k_row, v_row)
     uint16_t q[S][GW * D];
     int4 meta0[S];  // r, virtual head, block, flags
     int4 meta1[S];  // valid keys, token row, output slot (-1 = final)
@@ -186,6 +192,17 @@ struct DecodeCfg {
 };
 
 enum : int { kFirst = 1, kLast = 2, kInvalid = 4, kEnd = 8 };
+
+// Stage rows of key j (0..15) of a chunk, SH = log2(B). 8-token blocks land
+// as [K 0..7 | V 0..7 | K 8..15 | V 8..15], the others as [K 0..15 | V 0..15].
+template <int SH>
+__device__ __forceinline__ int k_row(int j) {
+  return SH == 3 ? (j & 7) + ((j >> 3) << 4) : j;
+}
+template <int SH>
+__device__ __forceinline__ int v_row(int j) {
+  return SH == 3 ? (j & 7) + ((j >> 3) << 4) + 8 : 16 + j;
+}
 
 // Reduce-scatter across the LPK lanes of a sub-group. The caller stores at
 // register position p the partial score of logical index p ^ (li * NV / LPK)
@@ -215,7 +232,7 @@ struct ReduceScatter {
 // reach 2^8, far inside fp32 range. The result is the same softmax.
 constexpr float kRescaleLog2 = 8.f;
 
-template <int D, int GW, int S, int WARPS>
+template <int D, int GW, int S, int WARPS, int SH>
 __global__ void __launch_bounds__(WARPS * 32)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
   using C = DecodeCfg<D, GW, S>;
@@ -258,10 +275,14 @@ __global__ void __launch_bounds__(WARPS * 32)
   __syncwarp();
 
   // ---------------- producer state (identical in every lane)
+  // blk counts 16-key chunks; the block table is read through a window of 32
+  // entries held one per lane
+  constexpr int sh = SH;
   long long x = x0;
   bool new_piece = true;
   L = __ldg(p.seq_lens + r);
   t = __ldg(p.qsl + r);
+  int nent = (L + (1 << sh) - 1) >> sh;  // table entries the request uses
   int win_r = -1, win_base = 0, win_val = -1;
 
   auto produce = [&](int s) {
@@ -278,27 +299,51 @@ __global__ void __launch_bounds__(WARPS * 32)
       const long long wf = owner_warp(a, N, W), wl = owner_warp(a + nblk - 1, N, W);
       out_slot = (wf == wl) ? -1 : static_cast<int>(static_cast<long long>(r) * p.virt_heads + vg + w);
     }
-    if (r != win_r || blk < win_base || blk >= win_base + 32) {
+    // table entries of chunk blk: e0, and e0 + 1 for 8-token blocks
+    const int e0 = (sh == 4) ? blk : (sh == 5 ? blk >> 1 : 2 * blk);
+    const int e_hi = (sh == 3) ? e0 + 1 : e0;  // (constant-folded per block size)
+    if (r != win_r || e0 < win_base || e_hi >= win_base + 32) {
       win_r = r;
-      win_base = blk;
-      const int j = blk + lane;
-      win_val = (j < nblk) ? __ldg(p.block_table + static_cast<long long>(r) * p.max_blocks + j) : -1;
+      win_base = e0;
+      const int j = e0 + lane;
+      win_val = (j < nent) ? __ldg(p.block_table + static_cast<long long>(r) * p.max_blocks + j) : -1;
     }
-    const int phys = __shfl_sync(0xffffffffu, win_val, blk - win_base);
-    const bool valid = phys >= 0 && phys < p.num_blocks;
+    const int phys = __shfl_sync(0xffffffffu, win_val, e0 - win_base);
+    const int nvalid = min(kChunkKeys, L - blk * kChunkKeys);
+    bool valid = phys >= 0 && phys < p.num_blocks;
+    bool second = false;  // 8-token blocks: the chunk's keys 8..15 exist
+    int phys1 = -1;
+    if constexpr (sh == 3) {
+      phys1 = __shfl_sync(0xffffffffu, win_val, e_hi - win_base);
+      second = nvalid > 8;
+      if (second) valid = valid && phys1 >= 0 && phys1 < p.num_blocks;
+    }
     int flags = (new_piece ? kFirst : 0) | ((blk == nblk - 1 || x == x1 - 1) ? kLast : 0) |
                 (valid ? 0 : kInvalid);
-    const int nvalid = min(kBlockSize, L - blk * kBlockSize);
     if (lane == 0) {
       sm.meta0[s] = make_int4(r, vg, blk, flags);
       sm.meta1[s] = make_int4(nvalid, t, out_slot, 0);
-      const uint32_t tx = (valid ? C::kKvBytes : 0u) + (new_piece ? C::kQBytes : 0u);
+      const uint32_t kv_tx = (sh == 3 && !second) ? C::kKvBytes / 2 : C::kKvBytes;
+      const uint32_t tx = (valid ? kv_tx : 0u) + (new_piece ? C::kQBytes : 0u);
       if (!valid) atomicOr(&g_errors_decode, kErrBlockRange);
       if (tx) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&sm.full[s], tx);
-        if (valid)
-          tma_load_3d(&sm.kv[s][0][0], &kv_map, 0, vg / p.head_groups, phys * 32, &sm.full[s]);
+        if (valid) {
+          // pool rows of one kv head: (block * 2 + k|v) * B + offset
+          const int hk = vg / p.head_groups;
+          uint16_t* dst = &sm.kv[s][0][0];
+          if constexpr (sh == 4) {  // K and V of the block: 32 consecutive rows
+            tma_load_3d(dst, &kv_map, 0, hk, phys * 32, &sm.full[s]);
+          } else if constexpr (sh == 5) {  // half (blk & 1) of the block's K rows and V rows
+            const int row = phys * 64 + (blk & 1) * 16;
+            tma_load_3d(dst, &kv_map, 0, hk, row, &sm.full[s]);
+            tma_load_3d(dst + 16 * D, &kv_map, 0, hk, row + 32, &sm.full[s]);
+          } else {  // two blocks of 8, each its 16 consecutive K and V rows
+            tma_load_3d(dst, &kv_map, 0, hk, phys * 16, &sm.full[s]);
+            if (second) tma_load_3d(dst + 16 * D, &kv_map, 0, hk, phys1 * 16, &sm.full[s]);
+          }
+        }
         if (new_piece)
           bulk_load(&sm.q[s][0], p.q + static_cast<long long>(t) * p.q_stride + vg * GW * D,
                     C::kQBytes, &sm.full[s]);
@@ -322,6 +367,7 @@ __global__ void __launch_bounds__(WARPS * 32)
           } while (nblk == 0);
           L = __ldg(p.seq_lens + r);
           t = __ldg(p.qsl + r);
+          nent = (L + (1 << sh) - 1) >> sh;
         }
       }
     }
@@ -381,7 +427,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
     for (int jp = 0; jp < C::KPL; ++jp) {
       const int key = (jp ^ perm_k) * C::KPI + sub;
-      const uint4 kv4 = ld_shared_v4(kv_base + key * D * 2);
+      const uint4 kv4 = ld_shared_v4(kv_base + k_row<SH>(key) * D * 2);
       const uint32_t wd[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
       float2 k2[4];
 #pragma unroll
@@ -448,7 +494,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
       auto pv_key = [&](int j) {
         const int key = j * C::KPI + sub;
-        const uint4 vv = ld_shared_v4(kv_base + (16 + key) * D * 2);
+        const uint4 vv = ld_shared_v4(kv_base + v_row<SH>(key) * D * 2);
         const uint32_t wd[4] = {vv.x, vv.y, vv.z, vv.w};
         float2 v2[4];
 #pragma unroll
@@ -461,7 +507,7 @@ __global__ void __launch_bounds__(WARPS * 32)
           for (int e = 0; e < 4; ++e) o2[h][e] = ffma2(p2, v2[e], o2[h][e]);
         }
       };
-      if (bvalid && nvalid == kBlockSize) {
+      if (bvalid && nvalid == kChunkKeys) {
 #pragma unroll
         for (int j = 0; j < C::KPL; ++j) pv_key(j);
       } else {
@@ -619,29 +665,74 @@ constexpr size_t decode_smem_bytes() {
   return sizeof(typename DecodeCfg<D, GW, kDecodeStages>::WarpSmem) * kDecodeWarps + 128;
 }
 
-template <int D, int GW>
+template <int D, int GW, int SH>
 static std::atomic<unsigned long long> g_decode_attr_done{0};
 
-template <int D, int GW>
+template <int D, int GW, int SH>
 static cudaError_t decode_occupancy(int* ctas_per_sm) {
-  auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps>;
+  auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps, SH>;
   const size_t smem = decode_smem_bytes<D, GW>();
-  cudaError_t e = smem_attr_once(kern, static_cast<int>(smem), g_decode_attr_done<D, GW>);
+  cudaError_t e = smem_attr_once(kern, static_cast<int>(smem), g_decode_attr_done<D, GW, SH>);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, kern, kDecodeWarps * 32, smem);
 }
 
-cudaError_t decode_full_wave_warps(int head_dim, int group, int num_sms, int* warps) {
-  const int gw = decode_heads_per_warp(group);
-  int ctas = 0;
-  cudaError_t e = cudaErrorInvalidValue;
-  if (head_dim == 128 && gw == 4) e = decode_occupancy<128, 4>(&ctas);
-  if (head_dim == 128 && gw == 2) e = decode_occupancy<128, 2>(&ctas);
-  if (head_dim == 128 && gw == 1) e = decode_occupancy<128, 1>(&ctas);
-  if (head_dim == 64 && gw == 4) e = decode_occupancy<64, 4>(&ctas);
-  if (head_dim == 64 && gw == 2) e = decode_occupancy<64, 2>(&ctas);
-  if (head_dim == 64 && gw == 1) e = decode_occupancy<64, 1>(&ctas);
+template <int D, int GW, int SH>
+static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_map,
+                                   cudaStream_t stream, void** trace) {
+  auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps, SH>;
+  const size_t smem = decode_smem_bytes<D, GW>();
+  cudaError_t e = smem_attr_once(kern, static_cast<int>(smem), g_decode_attr_done<D, GW, SH>);
   if (e != cudaSuccess) return e;
+  const long long grid = (p.warps + kDecodeWarps - 1) / kDecodeWarps;
+  kern<<<static_cast<unsigned>(grid), kDecodeWarps * 32, smem, stream>>>(kv_map, p);
+  e = cudaGetLastError();
+  if (e == cudaSuccess && trace) e = cudaEventRecord(static_cast<cudaEvent_t>(trace[3]), stream);
+  if (e != cudaSuccess) return e;
+  combine_kernel<D, GW><<<static_cast<unsigned>(p.warps), GW * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Calls F<D, GW, SH>::run(args...) for the instantiated shapes: head_dim 64 or
+// 128, 1, 2 or 4 heads per warp, blocks of 8, 16 or 32 tokens.
+template <template <int, int, int> class F, typename... A>
+static cudaError_t decode_dispatch(int head_dim, int gw, int sh, A&&... args) {
+#define PKV_DECODE_CASE(D_, GW_, SH_) \
+  if (head_dim == D_ && gw == GW_ && sh == SH_) return F<D_, GW_, SH_>::run(args...);
+#define PKV_DECODE_SH(D_, GW_) \
+  PKV_DECODE_CASE(D_, GW_, 3) PKV_DECODE_CASE(D_, GW_, 4) PKV_DECODE_CASE(D_, GW_, 5)
+  PKV_DECODE_SH(128, 4) PKV_DECODE_SH(128, 2) PKV_DECODE_SH(128, 1)
+  PKV_DECODE_SH(64, 4) PKV_DECODE_SH(64, 2) PKV_DECODE_SH(64, 1)
+#undef PKV_DECODE_SH
+#undef PKV_DECODE_CASE
+  return cudaErrorInvalidValue;
+}
+
+template <int D, int GW, int SH>
+struct OccupancyOp {
+  static cudaError_t run(int* ctas) { return decode_occupancy<D, GW, SH>(ctas); }
+};
+
+template <int D, int GW, int SH>
+struct LaunchOp {
+  static cudaError_t run(const DecodeParams& p, const CUtensorMap& m, cudaStream_t s, void** t) {
+    return launch_decode_t<D, GW, SH>(p, m, s, t);
+  }
+};
+
+// At most this many decode CTAs per SM in the default split, even where
+// registers and shared memory would fit a third: on the 1280-decode mixed
+// step (d = 128, 32 q / 8 kv heads) 2 CTAs of 4 warps per SM streamed at
+// 0.98 of the copy peak and 3 at 0.93 (shorter warp ranges, more partials).
+constexpr int kDecodeMaxCtasPerSm = 2;
+
+cudaError_t decode_full_wave_warps(int head_dim, int group, int block_shift, int num_sms,
+                                   int* warps) {
+  int ctas = 0;
+  cudaError_t e = decode_dispatch<OccupancyOp>(head_dim, decode_heads_per_warp(group),
+                                               block_shift, &ctas);
+  if (e != cudaSuccess) return e;
+  if (ctas > kDecodeMaxCtasPerSm) ctas = kDecodeMaxCtasPerSm;
   if (ctas < 1) ctas = 1;
   *warps = num_sms * ctas * kDecodeWarps;
   return cudaSuccess;
@@ -650,22 +741,6 @@ cudaError_t decode_full_wave_warps(int head_dim, int group, int num_sms, int* wa
 cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream) {
   const int group = a.num_q_heads / a.num_kv_heads;
   plan_kernel<<<1, 1024, 0, stream>>>(a, ws, 128 / group);
-  return cudaGetLastError();
-}
-
-template <int D, int GW>
-static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_map,
-                                   cudaStream_t stream, void** trace) {
-  auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps>;
-  const size_t smem = decode_smem_bytes<D, GW>();
-  cudaError_t e = smem_attr_once(kern, static_cast<int>(smem), g_decode_attr_done<D, GW>);
-  if (e != cudaSuccess) return e;
-  const long long grid = (p.warps + kDecodeWarps - 1) / kDecodeWarps;
-  kern<<<static_cast<unsigned>(grid), kDecodeWarps * 32, smem, stream>>>(kv_map, p);
-  e = cudaGetLastError();
-  if (e == cudaSuccess && trace) e = cudaEventRecord(static_cast<cudaEvent_t>(trace[3]), stream);
-  if (e != cudaSuccess) return e;
-  combine_kernel<D, GW><<<static_cast<unsigned>(p.warps), GW * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -693,13 +768,7 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUte
   p.part_ml = ws.part_ml;
   p.part_o = ws.part_o;
   p.bound = ws.bound;
-  if (a.head_dim == 128 && gw == 4) return launch_decode_t<128, 4>(p, kv_map, stream, trace);
-  if (a.head_dim == 128 && gw == 2) return launch_decode_t<128, 2>(p, kv_map, stream, trace);
-  if (a.head_dim == 128 && gw == 1) return launch_decode_t<128, 1>(p, kv_map, stream, trace);
-  if (a.head_dim == 64 && gw == 4) return launch_decode_t<64, 4>(p, kv_map, stream, trace);
-  if (a.head_dim == 64 && gw == 2) return launch_decode_t<64, 2>(p, kv_map, stream, trace);
-  if (a.head_dim == 64 && gw == 1) return launch_decode_t<64, 1>(p, kv_map, stream, trace);
-  return cudaErrorInvalidValue;
+  return decode_dispatch<LaunchOp>(a.head_dim, gw, a.block_shift, p, kv_map, stream, trace);
 }
 
 cudaError_t read_errors_decode(uint32_t* out, bool clear) {

@@ -1,9 +1,11 @@
 // Slot mapping and the cache write (reshape_and_cache) for sm_103a.
 //
-// Slot of a new token ("vllm v1 源码精读（三）", §3.4):
-//   slot = block_table[r][pos / 16] * 16 + pos % 16,  pos = num_computed[r] + i.
+// Slot of a new token ("vllm v1 源码精读（三）", §3.4), B tokens per block:
+//   slot = block_table[r][pos / B] * B + pos % B,  pos = num_computed[r] + i.
 // Write ("vLLM 架构源码解析（一）" §3.3.3; same page §3.4 of the v1 walk-through):
-//   kv_cache[slot / 16][0|1][slot % 16][:][:] = key[t] | value[t].
+//   kv_cache[slot / B][0|1][slot % B][:][:] = key[t] | value[t].
+// B is 8, 16 or 32 ("vLLM 架构源码解析（一）" §5.1 weighs the choice), passed
+// as its log2 so that / and % are a shift and a mask.
 //
 // Both are memory moves. The write copies 16-byte vectors: a K or V row of
 // one token is num_kv_heads * head_dim bf16 contiguous in the source and in
@@ -23,7 +25,7 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
                                     const int32_t* __restrict__ block_table, int max_blocks,
                                     const int32_t* __restrict__ qsl,
                                     const int32_t* __restrict__ num_computed, int num_reqs,
-                                    int num_tokens, int num_blocks, int req_blocks) {
+                                    int num_tokens, int num_blocks, int shift, int req_blocks) {
   if (static_cast<int>(blockIdx.x) >= req_blocks) {  // padding rows
     const int t = (blockIdx.x - req_blocks) * blockDim.x + threadIdx.x;
     if (t < num_tokens && t >= __ldg(qsl + num_reqs)) slots[t] = -1;
@@ -40,7 +42,7 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
   const long long row = static_cast<long long>(r) * max_blocks;
   for (int t = q0 + lane; t < q1; t += 32) {
     const long long pos = static_cast<long long>(c) + (t - q0);
-    const long long lb = pos / kBlockSize;
+    const long long lb = pos >> shift;
     int64_t slot = -1;
     if (lb >= max_blocks) {
       atomicOr(&g_errors_kvwrite, kErrLengths);
@@ -49,7 +51,7 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
       if (phys < 0 || phys >= num_blocks)
         atomicOr(&g_errors_kvwrite, kErrBlockRange);
       else
-        slot = static_cast<int64_t>(phys) * kBlockSize + (pos % kBlockSize);
+        slot = (static_cast<int64_t>(phys) << shift) + (pos & ((1 << shift) - 1));
     }
     slots[t] = slot;
   }
@@ -57,11 +59,11 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
 
 // One CTA per token (grid-stride over tokens): its threads copy the token's K
 // row and V row, 16 bytes each, into the pool at the token's slot.
-// vec_per_row = Hkv * D / 8.
+// vec_per_row = Hkv * D / 8; shift = log2(B).
 __global__ void kv_write_kernel(uint4* __restrict__ pool, const uint4* __restrict__ key,
                                 const uint4* __restrict__ value, long long key_stride_v,
                                 long long value_stride_v, const int64_t* __restrict__ slots,
-                                int num_tokens, int vec_per_row, long long num_slots) {
+                                int num_tokens, int vec_per_row, int shift, long long num_slots) {
   for (int t = blockIdx.x; t < num_tokens; t += gridDim.x) {
     const long long s = __ldg(slots + t);
     if (s < 0) continue;
@@ -69,9 +71,9 @@ __global__ void kv_write_kernel(uint4* __restrict__ pool, const uint4* __restric
       if (threadIdx.x == 0) atomicOr(&g_errors_kvwrite, kErrSlotRange);
       continue;
     }
-    const long long blk = s / kBlockSize, off = s % kBlockSize;
-    uint4* kdst = pool + ((blk * 2) * kBlockSize + off) * vec_per_row;
-    uint4* vdst = kdst + static_cast<long long>(kBlockSize) * vec_per_row;
+    const long long blk = s >> shift, off = s & ((1 << shift) - 1);
+    uint4* kdst = pool + (((blk * 2) << shift) + off) * vec_per_row;
+    uint4* vdst = kdst + (static_cast<long long>(vec_per_row) << shift);
     const uint4* ksrc = key + t * key_stride_v;
     const uint4* vsrc = value + t * value_stride_v;
     for (int e = threadIdx.x; e < vec_per_row; e += blockDim.x) {
@@ -86,7 +88,7 @@ __global__ void kv_write_kernel(uint4* __restrict__ pool, const uint4* __restric
 // Whole-block copies between two pools of one layout (copy-on-write of a
 // shared block; swap-out / swap-in between the device pool and a pool in
 // pinned host memory). One CTA per pair: 16-byte vectors, coalesced on both
-// sides. vec_per_block = 2 * 16 * Hkv * D / 8.
+// sides. vec_per_block = 2 * B * Hkv * D / 8.
 __global__ void copy_blocks_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
                                    const int32_t* __restrict__ pairs, int num_pairs,
                                    int dst_num_blocks, int src_num_blocks, int vec_per_block) {
@@ -103,10 +105,10 @@ __global__ void copy_blocks_kernel(uint4* __restrict__ dst, const uint4* __restr
 }
 
 cudaError_t launch_copy_blocks(void* dst, int dst_num_blocks, const void* src, int src_num_blocks,
-                               const int32_t* pairs, int num_pairs, int num_kv_heads,
-                               int head_dim, int num_sms, cudaStream_t stream) {
+                               const int32_t* pairs, int num_pairs, int block_size,
+                               int num_kv_heads, int head_dim, int num_sms, cudaStream_t stream) {
   if (num_pairs == 0) return cudaSuccess;
-  const int vec_per_block = 2 * kBlockSize * num_kv_heads * head_dim / 8;
+  const int vec_per_block = 2 * block_size * num_kv_heads * head_dim / 8;
   const long long cap = static_cast<long long>(num_sms) * 8;
   const int grid = static_cast<int>(num_pairs < cap ? num_pairs : cap);
   copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(dst),
@@ -117,21 +119,22 @@ cudaError_t launch_copy_blocks(void* dst, int dst_num_blocks, const void* src, i
 
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int max_blocks,
                                 const int32_t* qsl, const int32_t* num_computed, int num_reqs,
-                                int num_tokens, int num_blocks, cudaStream_t stream) {
+                                int num_tokens, int num_blocks, int block_size,
+                                cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
   const int threads = 256;
   const int req_blocks = (num_reqs + threads / 32 - 1) / (threads / 32);
   const int pad_blocks = (num_tokens + threads - 1) / threads;
   slot_mapping_kernel<<<req_blocks + pad_blocks, threads, 0, stream>>>(
       slots, block_table, max_blocks, qsl, num_computed, num_reqs, num_tokens, num_blocks,
-      req_blocks);
+      __builtin_ctz(static_cast<unsigned>(block_size)), req_blocks);
   return cudaGetLastError();
 }
 
 cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long long key_stride,
                             long long value_stride, const int64_t* slots, int num_tokens,
-                            int num_blocks, int num_kv_heads, int head_dim, int num_sms,
-                            cudaStream_t stream) {
+                            int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                            int num_sms, cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
   const int vec_per_row = num_kv_heads * head_dim / 8;
   const int threads = vec_per_row >= 128 ? 128 : (vec_per_row >= 64 ? 64 : 32);
@@ -140,7 +143,8 @@ cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long
   kv_write_kernel<<<grid, threads, 0, stream>>>(
       static_cast<uint4*>(pool), static_cast<const uint4*>(key), static_cast<const uint4*>(value),
       key_stride / 8, value_stride / 8, slots, num_tokens, vec_per_row,
-      static_cast<long long>(num_blocks) * kBlockSize);
+      __builtin_ctz(static_cast<unsigned>(block_size)),
+      static_cast<long long>(num_blocks) * block_size);
   return cudaGetLastError();
 }
 

@@ -12,7 +12,7 @@ namespace pkv {
 // Header words at the start of the attention workspace (written by the plan
 // kernel every call).
 enum : int {
-  kHdrDecodeBlocks = 0,  // sum of ceil(L/16) over decode requests
+  kHdrDecodeBlocks = 0,  // sum of ceil(L/16) (16-key chunks) over decode requests
   kHdrPrefillReqs = 1,   // requests with query_len > 1
   kHdrPrefillItems = 2,  // prefill work items (tile x kv head)
   kHdrPrefillNext = 3,   // work counter of the persistent prefill kernel
@@ -22,7 +22,7 @@ enum : int {
 // Device pointers into the attention workspace.
 struct AttnWorkspace {
   uint32_t* hdr;         // [kHdrWords]
-  int32_t* dec_prefix;   // [R + 1]: decode blocks before request r
+  int32_t* dec_prefix;   // [R + 1]: decode 16-key chunks before request r
   int32_t* pf_req;       // [R]: request id of the k-th prefill request
   int32_t* pf_prefix;    // [R + 1]: prefill items before the k-th prefill request
   float2* part_ml;       // [slots][GW]: (running max in log2 units, sum)
@@ -42,6 +42,7 @@ struct AttnArgs {
   const int32_t* num_computed;
   int num_reqs, num_tokens, max_query_len, max_seq_len;
   int num_q_heads, num_kv_heads, head_dim, num_blocks;
+  int block_shift;  // log2 of the tokens per cache block (3, 4 or 5)
   float scale;
 };
 
@@ -70,21 +71,23 @@ inline long long decode_partial_slots(int num_reqs, int virt_heads, long long wa
 
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int max_blocks,
                                 const int32_t* qsl, const int32_t* num_computed, int num_reqs,
-                                int num_tokens, int num_blocks, cudaStream_t stream);
+                                int num_tokens, int num_blocks, int block_size,
+                                cudaStream_t stream);
 
 cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long long key_stride,
                             long long value_stride, const int64_t* slots, int num_tokens,
-                            int num_blocks, int num_kv_heads, int head_dim, int num_sms,
-                            cudaStream_t stream);
+                            int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                            int num_sms, cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* dst, int dst_num_blocks, const void* src, int src_num_blocks,
-                               const int32_t* pairs, int num_pairs, int num_kv_heads,
-                               int head_dim, int num_sms, cudaStream_t stream);
+                               const int32_t* pairs, int num_pairs, int block_size,
+                               int num_kv_heads, int head_dim, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream);
 
 // Decode warps in one full wave on this device for the given shape.
-cudaError_t decode_full_wave_warps(int head_dim, int group, int num_sms, int* warps);
+cudaError_t decode_full_wave_warps(int head_dim, int group, int block_shift, int num_sms,
+                                   int* warps);
 
 // trace: NULL or the caller's event array; event [3] is recorded between the
 // decode and the combine kernel.

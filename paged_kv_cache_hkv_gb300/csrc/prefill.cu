@@ -11,11 +11,13 @@
 // Work item = (request, tile of 128 query rows, kv head). The 128 rows of a
 // tile are the G = Hq/Hkv q heads of one kv head for 128/G consecutive
 // queries, so every K/V tile feeds all G heads (GQA). The item's key tiles
-// (128 keys = 8 pool blocks each) are split between two softmax warpgroups:
+// (128 keys = 8 chunks of 16 keys: 8 blocks of 16 tokens, 4 of 32 or 16 of
+// 8) are split between two softmax warpgroups:
 // warpgroup w takes tiles w, w+2, ... with its own accumulators
 // (TMEM columns [256w, 256w+128) for S, [256w+128, 256w+128+D) for O).
-// One issuer thread streams K/V tiles through a 2-stage ring by TMA (128-byte
-// swizzle, one 16-token block of one kv head per copy) and issues
+// Two copy warps stream K and V tiles through a 2-stage ring by TMA (128-byte
+// swizzle, one 16-key chunk of one kv head per copy, two copies of 8 rows
+// for 8-token blocks) and one MMA thread issues
 //   S_w = Q K^T      tcgen05.mma M=128 N=128, A = Q (smem), B = K (smem)
 //   O_w += P_w V     tcgen05.mma M=128 N=D, A = P_w (smem), B = V (smem)
 // while the warpgroups run the softmax: each thread owns one row, reads S
@@ -171,6 +173,7 @@ struct PrefillParams {
   const int32_t* qsl;
   const int32_t* num_computed;
   int num_q_heads, num_kv_heads, group, num_blocks;
+  int block_shift;  // log2 of the tokens per cache block (3, 4 or 5)
   float scale_log2;
   uint32_t* hdr;
   const int32_t* pf_req;
@@ -293,11 +296,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long bt_row = static_cast<long long>(r) * p.max_blocks;
     auto stage_of = [&](int kt) { return static_cast<int>((tiles + kt) % kStages); };
     auto stage_par = [&](int kt) { return ((tiles + kt) / kStages) & 1u; };
-    // phys id of block b of tile kt if it holds keys < kv_len and is in the pool, else -1
-    auto block_id = [&](int kt, int b) -> int {
-      if (kt * kTileN + b * kBlockSize >= kv_len) return -1;
-      const int id = __ldg(p.block_table + bt_row + kt * 8 + b);
+    // block table entry e of the request if it holds keys < kv_len and its id
+    // is in the pool, else -1
+    const int bsh = p.block_shift;
+    auto entry_id = [&](int e) -> int {
+      if ((e << bsh) >= kv_len) return -1;
+      const int id = __ldg(p.block_table + bt_row + e);
       return (id >= 0 && id < p.num_blocks) ? id : -1;
+    };
+    // chunk b (keys 16b .. 16b+15) of tile kt holds keys < kv_len, all of
+    // them in blocks of the pool
+    auto chunk_ok = [&](int kt, int b) -> bool {
+      const int k0 = kt * kTileN + b * kChunkKeys;
+      if (k0 >= kv_len) return false;
+      if (bsh == 4) return entry_id(k0 >> 4) >= 0;
+      if (bsh == 5) return entry_id(k0 >> 5) >= 0;
+      return entry_id(k0 >> 3) >= 0 && (k0 + 8 >= kv_len || entry_id((k0 >> 3) + 1) >= 0);
     };
 
     if (warp >= 8) {
@@ -306,8 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       //   warp 10: V(kt) TMA copies, once PV(kt - 2) is done (its V slot is free)
       //   warp 8:  MMAs: S(kt) once K(kt) landed and softmax(kt - 2) read S_w;
       //            PV(kt) once softmax(kt) wrote P_w and V(kt) landed
-      // Lanes 0 .. 8*DH-1 of a copy warp issue one TMA copy each; the block
-      // ids of a 32-block window sit in the lanes' registers.
+      // Lane (chunk b, d half dh), lanes 0 .. 8*DH-1, issues the copies of
+      // that chunk (one of 16 rows, or two of 8 rows for 8-token blocks); the
+      // block ids of a 32-entry window of the block table sit in the lanes'
+      // registers.
       const int ln = tid & 31;
       auto phase = [&](int kt) { return (cnt[kt & 1] + (kt >> 1)) & 1u; };
       bool ok = true;
@@ -329,27 +345,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
           }
           const int st = stage_of(kt);
-          if (kt * 8 + 8 > win_base + 32) {
-            win_base = kt * 8;
-            const int lb = win_base + ln;
-            win_val = (lb * kBlockSize < kv_len) ? block_id(kt + ln / 8, ln & 7) : -1;
-            if (!is_v && lb * kBlockSize < kv_len && win_val < 0)
+          const int E = kTileN >> bsh;  // table entries per tile
+          if (kt * E + E > win_base + 32) {
+            win_base = kt * E;
+            const int e = win_base + ln;
+            win_val = entry_id(e);
+            if (!is_v && (e << bsh) < kv_len && win_val < 0)
               atomicOr(&g_errors_prefill, kErrBlockRange);
           }
           const int b = (ln / DH) & 7, dh = ln % DH;
-          const int id = __shfl_sync(0xffffffffu, win_val, kt * 8 - win_base + b);
-          const bool mine = ln < 8 * DH && id >= 0;
-          const uint32_t nops = __popc(__ballot_sync(0xffffffffu, mine));
+          // pool rows of one kv head: (block * 2 + k|v) * B + offset
+          int id0, id1 = -1, row0, row1 = 0;
+          if (bsh == 4) {
+            id0 = __shfl_sync(0xffffffffu, win_val, kt * 8 + b - win_base);
+            row0 = id0 * 32 + (is_v ? 16 : 0);
+          } else if (bsh == 5) {
+            id0 = __shfl_sync(0xffffffffu, win_val, kt * 4 + (b >> 1) - win_base);
+            row0 = id0 * 64 + (b & 1) * 16 + (is_v ? 32 : 0);
+          } else {
+            id0 = __shfl_sync(0xffffffffu, win_val, kt * 16 + 2 * b - win_base);
+            id1 = __shfl_sync(0xffffffffu, win_val, kt * 16 + 2 * b + 1 - win_base);
+            row0 = id0 * 16 + (is_v ? 8 : 0);
+            row1 = id1 * 16 + (is_v ? 8 : 0);
+          }
+          const bool mine0 = ln < 8 * DH && id0 >= 0;
+          const bool mine1 = ln < 8 * DH && id1 >= 0;
+          const uint32_t bytes = bsh == 3 ? (mine0 ? 1024u : 0u) + (mine1 ? 1024u : 0u)
+                                         : (mine0 ? 2048u : 0u);
+          const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes);
           uint64_t* bar = is_v ? &sh.v_full[st] : &sh.k_full[st];
           if (ln == 0) {
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, nops * 2048u);
+            mbar_arrive_expect_tx(bar, tx);
           }
           __syncwarp();
-          if (mine)
-            tma_load_3d(gbase + (is_v ? Lay::kV : Lay::kK) + st * Lay::kTileKV +
-                            dh * Lay::kChunk + b * 2048,
-                        &kv_map, dh * 64, g, id * 32 + (is_v ? 16 : 0), bar);
+          unsigned char* dst = gbase + (is_v ? Lay::kV : Lay::kK) + st * Lay::kTileKV +
+                               dh * Lay::kChunk + b * 2048;
+          if (mine0) tma_load_3d(dst, &kv_map, dh * 64, g, row0, bar);
+          if (mine1) tma_load_3d(dst + 1024, &kv_map, dh * 64, g, row1, bar);
         }
       } else if (warp == 8 && ln == 0) {
         auto issue_s = [&](int kt) {  // S_w = Q K^T for tile kt
@@ -412,7 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nmine = 0;
       const int lane = tid & 31;
       // block ids of this warpgroup's next tile, loaded one tile ahead by lanes 0..7
-      auto load_ids = [&](int kt) -> int { return (lane < 8 && kt < nkv) ? block_id(kt, lane) : -1; };
+      auto load_ids = [&](int kt) -> int {
+        return (lane < 8 && kt < nkv && chunk_ok(kt, lane)) ? 1 : -1;
+      };
       int next_id = load_ids(wg);
       for (int kt = wg; ok && kt < nkv; kt += 2, ++nmine) {
         const uint32_t ph = cnt[wg] + (kt >> 1);
@@ -422,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc::fence_after_sync();
         // a tile every row sees in full needs no mask; otherwise column j is
-        // visible iff j <= jlim and its 16-key block was loaded (chunk c of 16
-        // columns = block c of the tile)
+        // visible iff j <= jlim and its 16-key chunk was loaded (chunk c =
+        // columns 16c .. 16c+15)
         const bool full = kt * kTileN + kTileN - 1 <= c + i0 && mask == 0xFFu;
         const int jlim = lim - kt * kTileN;
         // the whole S row in one TMEM round trip: 4 x 32 columns, one wait
@@ -432,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) tc::ld32(t_s + q * 32, sr[q]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) tc::wait32(sr[q]);
-        // invisible columns become -inf (block c of the tile = columns 16c .. 16c+15)
+        // invisible columns become -inf
         if (!full) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -492,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(w[0], w[1], w[2], w[3]);
         }
         l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-        // V rows of keys past kv_len or of blocks not loaded must be zero
+        // V rows of keys past kv_len or of chunks not loaded must be zero
         // (0 * NaN): for such a tile wait for its V copy first
         if (kt * kTileN + kTileN > kv_len || mask != 0xFFu) {
           ok = wait_or_abort(&sh.v_full[stage_of(kt)], stage_par(kt), abort_flag);
@@ -611,6 +646,7 @@ cudaError_t launch_prefill(const AttnArgs& a, const AttnWorkspace& ws, const CUt
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_q_heads / a.num_kv_heads;
   p.num_blocks = a.num_blocks;
+  p.block_shift = a.block_shift;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.hdr = ws.hdr;
   p.pf_req = ws.pf_req;

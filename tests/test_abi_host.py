@@ -60,7 +60,11 @@ def test_write_rejects_bad_arguments(lib):
     ok = header_define("PKV_OK")
     assert ok == 0
     W = lib.pkv_paged_kv_write
-    assert W(FAKE, FAKE, FAKE, 0, 0, FAKE, 4, _layout(bs=8), None) == header_define("PKV_ERR_UNSUPPORTED")
+    for bs in (4, 24, 64):   # blocks of 8, 16 or 32 tokens only
+        assert W(FAKE, FAKE, FAKE, 0, 0, FAKE, 4, _layout(bs=bs), None) == header_define("PKV_ERR_UNSUPPORTED")
+    for bs in (8, 32):       # accepted: the next check (a null pointer) decides
+        assert W(None, FAKE, FAKE, 0, 0, FAKE, 4, _layout(bs=bs), None) == header_define("PKV_ERR_NULL_POINTER")
+    assert W(FAKE, FAKE, FAKE, 0, 0, FAKE, 4, _layout(bs=0), None) == header_define("PKV_ERR_BAD_SHAPE")
     assert W(FAKE, FAKE, FAKE, 0, 0, FAKE, 4, _layout(d=96), None) == header_define("PKV_ERR_UNSUPPORTED")
     assert W(FAKE, FAKE, FAKE, 0, 0, FAKE, -1, _layout(), None) == header_define("PKV_ERR_BAD_SHAPE")
     assert W(FAKE, FAKE, FAKE, 0, 0, FAKE, 4, _layout(nb=0), None) == header_define("PKV_ERR_BAD_SHAPE")
@@ -90,6 +94,11 @@ def test_attention_rejects_bad_arguments(lib):
     assert _attn(lib, lay=_layout(d=80)) == E("PKV_ERR_UNSUPPORTED")
     assert _attn(lib, R=-1) == E("PKV_ERR_BAD_SHAPE")
     assert _attn(lib, ms=200) == E("PKV_ERR_BAD_SHAPE")        # 200 > 8 blocks * 16
+    assert _attn(lib, ms=100, lay=_layout(bs=8)) == E("PKV_ERR_BAD_SHAPE")   # 100 > 8 * 8
+    assert _attn(lib, ms=200, lay=_layout(bs=32), bt=None) == E("PKV_ERR_NULL_POINTER")  # 200 <= 8 * 32
+    assert _attn(lib, lay=_layout(bs=12)) == E("PKV_ERR_UNSUPPORTED")
+    # pool rows (block * 2 + k|v) * B must stay below 2^31
+    assert _attn(lib, lay=_layout(nb=1 << 25, bs=32)) == E("PKV_ERR_BAD_SHAPE")
     assert _attn(lib, scale=float("nan")) == E("PKV_ERR_BAD_SHAPE")
     assert _attn(lib, scale=-0.5) == E("PKV_ERR_BAD_SHAPE")
     assert _attn(lib, scale=float("inf")) == E("PKV_ERR_BAD_SHAPE")
@@ -107,7 +116,10 @@ def test_attention_rejects_bad_arguments(lib):
 def test_slot_mapping_and_errors_reject_bad_arguments(lib):
     E = header_define
     S = lib.pkv_slot_mapping
-    assert S(FAKE, FAKE, 4, FAKE, FAKE, 2, 3, 10, 8, None) == E("PKV_ERR_UNSUPPORTED")
+    assert S(FAKE, FAKE, 4, FAKE, FAKE, 2, 3, 10, 12, None) == E("PKV_ERR_UNSUPPORTED")
+    assert S(FAKE, FAKE, 4, FAKE, FAKE, 2, 3, 10, 0, None) == E("PKV_ERR_BAD_SHAPE")
+    for bs in (8, 32):
+        assert S(None, FAKE, 4, FAKE, FAKE, 2, 3, 10, bs, None) == E("PKV_ERR_NULL_POINTER")
     assert S(FAKE, FAKE, 4, FAKE, FAKE, 2, -3, 10, 16, None) == E("PKV_ERR_BAD_SHAPE")
     assert S(None, FAKE, 4, FAKE, FAKE, 2, 3, 10, 16, None) == E("PKV_ERR_NULL_POINTER")
     assert S(None, None, 4, None, None, 2, 0, 10, 16, None) == E("PKV_OK")
@@ -117,7 +129,8 @@ def test_slot_mapping_and_errors_reject_bad_arguments(lib):
 def test_copy_blocks_rejects_bad_arguments(lib):
     E = header_define
     C = lib.pkv_copy_blocks
-    assert C(FAKE, 4, FAKE, 4, FAKE, 2, _layout(bs=8), None) == E("PKV_ERR_UNSUPPORTED")
+    assert C(FAKE, 4, FAKE, 4, FAKE, 2, _layout(bs=48), None) == E("PKV_ERR_UNSUPPORTED")
+    assert C(FAKE, 4, None, 4, FAKE, 2, _layout(bs=8), None) == E("PKV_ERR_NULL_POINTER")
     assert C(FAKE, 0, FAKE, 4, FAKE, 2, _layout(), None) == E("PKV_ERR_BAD_SHAPE")
     assert C(FAKE, 4, FAKE, 4, FAKE, -1, _layout(), None) == E("PKV_ERR_BAD_SHAPE")
     assert C(FAKE, 4, None, 4, FAKE, 2, _layout(), None) == E("PKV_ERR_NULL_POINTER")

@@ -1,0 +1,50 @@
+"""Host-side figures the bench reports, checked on small hand-made cases."""
+
+import os
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import bench  # noqa: E402
+from paged_kv_cache_hkv_gb300.synth import RequestSpec, make_step  # noqa: E402
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_block_tradeoff_counts_last_block_waste(B):
+    # contexts 1, B, B + 1 and 3B: last blocks hold 1, B, 1 and B tokens
+    lens = [1, B, B + 1, 3 * B]
+    step = make_step([RequestSpec(L - 1, 1) for L in lens], num_q_heads=4, num_kv_heads=2,
+                     head_dim=64, block_size=B, seed=1, materialize=False)
+    t = bench.block_tradeoff(step)
+    blocks = 1 + 1 + 2 + 3
+    assert t["table_entries_read"] == blocks
+    assert t["blocks_in_use"] == blocks
+    assert t["slots_allocated"] == blocks * B
+    wasted = (B - 1) + 0 + (B - 1) + 0
+    assert t["slots_wasted_frac"] == pytest.approx(wasted / (blocks * B))
+
+
+def test_block_tradeoff_counts_a_shared_block_once():
+    # two requests over one shared 32-token prefix (2 blocks of 16), each
+    # with 5 private tokens in a block of its own
+    specs = [RequestSpec(36, 1, shares_prefix=True), RequestSpec(36, 1, shares_prefix=True)]
+    step = make_step(specs, num_q_heads=4, num_kv_heads=2, head_dim=64, prefix_tokens=32,
+                     seed=2, materialize=False)
+    t = bench.block_tradeoff(step)
+    assert t["table_entries_read"] == 2 * 3
+    assert t["blocks_in_use"] == 2 + 2
+    assert t["slots_allocated"] == 4 * 16
+    assert t["slots_wasted_frac"] == pytest.approx(2 * 11 / 64)
+
+
+def test_step_work_bytes_do_not_depend_on_block_size():
+    works = []
+    for B in (8, 16, 32):
+        step = make_step([RequestSpec(99, 1), RequestSpec(20, 30)], num_q_heads=8,
+                         num_kv_heads=2, head_dim=128, block_size=B, seed=3, materialize=False)
+        works.append(bench.step_work(step))
+    assert works[0] == works[1] == works[2]
+    assert works[0]["decode_kv_bytes"] == 100 * 2 * 128 * 2 * 2
+    assert works[0]["prefill_flops"] == 4 * 128 * 8 * (30 * 20 + 30 * 31 // 2)

@@ -233,10 +233,66 @@ def test_mixed_batch_order_independence():
     run_and_check(rev, decode_warps=9)
 
 
+# ---------------------------------------------------------------- block sizes
+# Lengths around every multiple of 8 up to 33 (a chunk of 16 keys ends inside
+# an 8-token block, on a block edge, in the first or second half of a
+# 32-token block), long contexts, fresh prefills, chunks over a cached prefix
+# and a chunk shorter than one block.
+BLOCK_SPECS = ([RequestSpec(L - 1, 1) for L in (1, 7, 8, 9, 15, 16, 17, 24, 25, 31, 32, 33,
+                                               100, 1000, 3001)]
+               + [RequestSpec(0, 37), RequestSpec(41, 200), RequestSpec(500, 129),
+                  RequestSpec(9, 8), RequestSpec(24, 300)])
+
+
+@pytest.mark.parametrize("B", [8, 32])
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (8, 4, 64), (16, 2, 64)])
+def test_block_sizes_mixed_step(B, Hq, Hkv, D):
+    step = make_step(BLOCK_SPECS, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=B,
+                     seed=B * 10 + Hq + D)
+    run_and_check(step)
+    run_and_check(step, decode_warps=29)
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_block_size_leaves_the_result_unchanged_on_gpu(B):
+    """One logical batch stored with 8-, 16- or 32-token blocks: the same
+    output rows (the pool layout is the only difference)."""
+    specs = [RequestSpec(700, 1), RequestSpec(33, 1), RequestSpec(120, 90), RequestSpec(0, 1)]
+    step = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=B, seed=88)
+    ds = DeviceStep(step)
+    ds.run()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_errors(clear=True) == 0
+    ref16 = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=88)
+    assert np.array_equal(step.q, ref16.q)
+    _, _, ref = oracle_step(ref16)
+    assert_close(ds.out_host(), ref)
+
+
+@pytest.mark.parametrize("B", [8, 32])
+def test_block_sizes_mixed_workload(B):
+    run_and_check(synth.mixed_step(block_size=B, num_decodes=200), rows=None)
+
+
+@pytest.mark.parametrize("B", [8, 32])
+def test_block_sizes_bad_block_id_is_masked_and_flagged(B):
+    specs = [RequestSpec(60, 1), RequestSpec(100, 1), RequestSpec(40, 30)]
+    step = make_step(specs, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=B, seed=3)
+    # an entry inside the used range of request 1 points past the pool
+    step.block_table[1, 1] = step.num_blocks + 5
+    ds = DeviceStep(step)
+    ds.run()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_errors(clear=True) & binding.DEVERR_BLOCK_RANGE
+    # the other requests are untouched by it
+    _, _, ref = oracle_step(step, rows=[0] + list(range(2, step.num_tokens)))
+    assert_close(ds.out_host(), ref, rows=[0] + list(range(2, step.num_tokens)))
+
+
 # ---------------------------------------------------------------- block copies
-def _rand_pool(nb, hkv=8, d=128, seed=0, device="cuda", pinned=False):
+def _rand_pool(nb, hkv=8, d=128, seed=0, device="cuda", pinned=False, block_size=16):
     g = torch.Generator().manual_seed(seed)
-    t = torch.randn((nb, 2, 16, hkv, d), generator=g).to(torch.bfloat16)
+    t = torch.randn((nb, 2, block_size, hkv, d), generator=g).to(torch.bfloat16)
     if pinned:
         return t.pin_memory()
     return t.to(device)
@@ -253,6 +309,18 @@ def test_copy_blocks_copy_on_write_in_pool():
     rng = np.random.default_rng(5)
     ids = rng.permutation(300)
     pairs = np.stack([ids[:60], ids[60:120]], axis=1).astype(np.int32)  # disjoint src / dst
+    binding.pkv_copy_blocks(pool, pool, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_errors(clear=True) == 0
+    assert np.array_equal(_host_bits(pool), oracle.copy_blocks(before, before, pairs))
+
+
+@pytest.mark.parametrize("B", [8, 32])
+def test_copy_blocks_other_block_sizes(B):
+    import oracle
+    pool = _rand_pool(100, hkv=4, d=128, seed=6, block_size=B)
+    before = _host_bits(pool)
+    pairs = np.array([[3, 90], [50, 7], [99, 0]], np.int32)
     binding.pkv_copy_blocks(pool, pool, torch.from_numpy(pairs).cuda())
     torch.cuda.synchronize()
     assert binding.pkv_get_device_errors(clear=True) == 0

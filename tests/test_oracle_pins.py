@@ -148,41 +148,49 @@ def test_block_arithmetic_values():
     assert per_block == b["bytes_per_block_all_layers"]
 
 
-def test_last_block_fill_matches_walk():
+# block sizes the pages weigh against each other (vLLM 架构源码解析（一）, §5.1)
+BLOCK_SIZES = [8, 16, 32]
+
+
+@pytest.mark.parametrize("B", BLOCK_SIZES)
+def test_last_block_fill_matches_walk(B):
     for n in range(1, 200):
-        places = walk_places(list(range(100)), n)
+        places = walk_places(list(range(100)), n, B)
         nblocks = len({p[0] for p in places})
-        assert int(oracle.blocks_for_tokens(n)) == nblocks
-        assert int(oracle.last_block_fill(n)) == sum(1 for p in places if p[0] == places[-1][0])
+        assert int(oracle.blocks_for_tokens(n, B)) == nblocks
+        assert int(oracle.last_block_fill(n, B)) == sum(1 for p in places if p[0] == places[-1][0])
 
 
-def test_slot_of_equals_table_walk():
+@pytest.mark.parametrize("B", BLOCK_SIZES)
+def test_slot_of_equals_table_walk(B):
     rng = np.random.default_rng(11)
     for _ in range(20):
         row = rng.permutation(500)[:40]
-        n = int(rng.integers(1, 40 * 16))
-        for pos, (blk, off) in enumerate(walk_places(row, n)):
-            assert oracle.slot_of(row, pos) == blk * 16 + off
+        n = int(rng.integers(1, 40 * B))
+        for pos, (blk, off) in enumerate(walk_places(row, n, B)):
+            assert oracle.slot_of(row, pos, B) == blk * B + off
 
 
-def test_slot_mapping_varlen_batch():
+@pytest.mark.parametrize("B", BLOCK_SIZES)
+def test_slot_mapping_varlen_batch(B):
     rng = np.random.default_rng(12)
-    case = build_case(rng, [1, 7, 33, 1], [40, 0, 17, 15], 4, 2, 8)
-    sm = oracle.slot_mapping(case["bt"], case["qsl"], case["nc"])
+    case = build_case(rng, [1, 7, 33, 1], [40, 0, 17, 15], 4, 2, 8, B=B)
+    sm = oracle.slot_mapping(case["bt"], case["qsl"], case["nc"], B)
     for r in range(len(case["nc"])):
-        places = walk_places(case["bt"][r], int(case["sl"][r]))
+        places = walk_places(case["bt"][r], int(case["sl"][r]), B)
         for i, t in enumerate(range(case["qsl"][r], case["qsl"][r + 1])):
             blk, off = places[int(case["nc"][r]) + i]
-            assert sm[t] == blk * 16 + off
+            assert sm[t] == blk * B + off
 
 
 # ---------------------------------------------------------------------------
 # the write
 # ---------------------------------------------------------------------------
 
-def test_kv_write_roundtrip_and_untouched():
+@pytest.mark.parametrize("B", BLOCK_SIZES)
+def test_kv_write_roundtrip_and_untouched(B):
     rng = np.random.default_rng(13)
-    NB, B, Hkv, D = 12, 16, 2, 8
+    NB, Hkv, D = 12, 2, 8
     pool = rand_bits(rng, (NB, 2, B, Hkv, D))
     N = 30
     slots = rng.permutation(NB * B)[:N].astype(np.int64)
@@ -224,11 +232,12 @@ def _oracle_out(case, scale, pool=None, bt=None):
                                   case["qsl"], case["nc"], scale)
 
 
-@pytest.mark.parametrize("Hq,Hkv,D", [(4, 2, 8), (4, 4, 4), (8, 2, 6)])
-def test_attention_equals_textbook_on_contiguous(Hq, Hkv, D):
+@pytest.mark.parametrize("Hq,Hkv,D,B", [(4, 2, 8, 16), (4, 4, 4, 16), (8, 2, 6, 16),
+                                        (4, 2, 8, 8), (8, 2, 6, 32)])
+def test_attention_equals_textbook_on_contiguous(Hq, Hkv, D, B):
     rng = np.random.default_rng(100 + Hq + D)
     lens_q, lens_c = [1, 5, 1, 3], [19, 0, 4, 30]
-    case = build_case(rng, lens_q, lens_c, Hq, Hkv, D)
+    case = build_case(rng, lens_q, lens_c, Hq, Hkv, D, B=B)
     scale = 1.0 / math.sqrt(D)
     got = _oracle_out(case, scale)
     for r in range(len(lens_q)):
@@ -257,6 +266,18 @@ def test_paging_independence_identity_vs_permuted():
     assert not np.array_equal(bt2, case["bt"])
     moved = _oracle_out(case, scale, pool=pool2, bt=bt2)
     assert np.array_equal(ident, moved)  # bit for bit
+
+
+def test_block_size_does_not_change_the_result():
+    """The block size decides only where a token's K/V sits, never what is
+    computed: one logical batch stored with 8-, 16- and 32-token blocks gives
+    the same output bit for bit."""
+    lens_q, lens_c = [1, 12, 1], [45, 9, 80]
+    outs = []
+    for B in BLOCK_SIZES:
+        case = build_case(np.random.default_rng(31), lens_q, lens_c, 4, 2, 8, NB=40, B=B)
+        outs.append(_oracle_out(case, 0.3))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
 
 
 def test_shared_prefix_equals_private_copies():
