@@ -64,6 +64,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Same, with the A operand (M rows x 16 K elements) in tensor memory: lane i
+// holds row i, 32-bit column c holds K elements 2c (low half) and 2c + 1.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -140,14 +151,42 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&v)[16]) {
       : "memory");
 }
 
+__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
 }  // namespace tc
 
-constexpr int kTileM = 128;  // query rows (query x head) per tile
-constexpr int kTileN = 128;  // keys per tile (8 blocks)
-constexpr int kStages = 2;   // K and V tile rings: tile kt uses slot (tiles + kt) % 2
+// OR of `v` over the 256 softmax threads (named barrier 1): every thread gets
+// the same answer.
+__device__ __forceinline__ bool softmax_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+constexpr int kTileM = 128;    // query rows (query x head) per tile
+constexpr int kTileN = 128;    // keys per tile (8 chunks of 16)
+constexpr int kKStages = 3;    // K ring: global tile T uses slot T % 3
+constexpr int kVStages = 2;    // V ring: global tile T uses slot T % 2
 constexpr uint32_t kTmemCols = 512;
+constexpr int kItemQ = 4;      // claimed work items in flight between the roles
+constexpr int kMetaReqs = 128;  // prefill requests whose metadata a CTA keeps in shared memory
 constexpr int kThreads = 352;  // 2 softmax warpgroups + MMA warp + K-copy warp + V-copy warp
-constexpr int kIssuer = 256;   // thread that issues the MMAs (warp 8, lane 0)
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (powers of two)
 
 template <int D>
@@ -155,12 +194,15 @@ struct PrefillLayout {
   static constexpr int DH = D / 64;                 // 64-element (128-byte) column chunks
   static constexpr uint32_t kChunk = kTileM * 128;  // 128 rows x 128 bytes = 16 KB
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kTileKV = DH * kChunk;     // K (or V) of one 128-key tile
-  static constexpr uint32_t kK = kQ + DH * kChunk;     // K ring, kStages tiles
-  static constexpr uint32_t kV = kK + kStages * kTileKV;  // V ring, kStages tiles
-  static constexpr uint32_t kP = kV + kStages * kTileKV;  // P of warpgroup w: 2 chunks each
-  static constexpr uint32_t kBar = kP + 2 * 2 * kChunk;
-  static constexpr uint32_t kBytes = kBar + 256;
+  static constexpr uint32_t kTileKV = DH * kChunk;         // K (or V) of one 128-key tile
+  static constexpr uint32_t kK = kQ + DH * kChunk;         // K ring
+  static constexpr uint32_t kV = kK + kKStages * kTileKV;  // V ring
+  static constexpr uint32_t kML = kV + kVStages * kTileKV; // float2 [item parity][warpgroup][row]
+  // request metadata: int4 (request, cached, first row, new tokens) [kMetaReqs],
+  // then the item prefix int [kMetaReqs + 1]
+  static constexpr uint32_t kMeta = kML + 2 * 2 * kTileM * 8;
+  static constexpr uint32_t kBar = kMeta + kMetaReqs * 16 + (kMetaReqs + 1) * 4 + 124;
+  static constexpr uint32_t kBytes = kBar + 512;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base
   static_assert(kAlloc <= 232448, "shared memory");
 };
@@ -180,18 +222,28 @@ struct PrefillParams {
   const int32_t* pf_prefix;
 };
 
+// mbarriers. "commit" ones are arrived on by tcgen05.commit of the MMA thread.
 struct PrefillShared {
-  uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t s_full[2];   // S of warpgroup w computed
-  uint64_t p_ready[2];  // P of warpgroup w in smem, V rows cleaned (128 arrivals)
-  uint64_t pv_done[2];  // O of warpgroup w updated
+  uint64_t q_full;               // Q tile of the item landed (TMA)
+  uint64_t q_free;               // commit: the item's last S read Q
+  uint64_t k_full[kKStages];     // K tile landed (TMA)
+  uint64_t k_free[kKStages];     // commit: the S that read the K slot is done
+  uint64_t v_full[kVStages];     // V tile landed (TMA)
+  uint64_t v_free[kVStages];     // commit: the PV that read the V slot is done
+  uint64_t s_full[2];            // commit: S of warpgroup w in TMEM
+  uint64_t p_ready[2];           // 128 arrivals: P of warpgroup w in TMEM, O rescaled, V cleaned
+  uint64_t o_full;               // commit: every PV of the item done
+  uint64_t o_free;               // 256 arrivals: both warpgroups have read O and the (m, l) pairs
   uint64_t drain;
+  uint64_t iq_full[kItemQ];      // item id j published in item_q[j % kItemQ]
+  uint64_t iq_free[kItemQ];      // 10 arrivals: every role has read it
+  int item_q[kItemQ];
   uint32_t tmem;
-  int item;
   int abort;
 };
+static_assert(sizeof(PrefillShared) <= 512, "barrier area");
+
+
 
 // Bounded wait that also gives up once another thread has flagged an abort.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -211,14 +263,106 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-// Work item: (request, 128-row query tile, kv head). Two softmax warpgroups
-// split the item's key tiles (warpgroup w takes tiles w, w+2, ...), each with
-// its own S and O accumulators in TMEM and its own running max and sum; one
-// thread streams K/V tiles through a 3-stage ring by TMA and issues every
-// MMA: S_w = Q K^T into TMEM, then O_w += P_w V with P_w (bf16) read from
-// TMEM where the softmax wrote it over S_w. At the end the two partial
-// results are merged (log-sum-exp) and each warpgroup writes half of the
-// output columns.
+// Consumers of the item queue (the MMA thread, the V-copy warp, each softmax
+// warp): item id number j of this CTA, or -1 after an abort. The calling
+// warp's lane 0 releases the slot once every lane has read it.
+__device__ __forceinline__ int take_item(PrefillShared& sh, int j, volatile int* abort,
+                                         bool whole_warp) {
+  const int slot = j % kItemQ;
+  if (!wait_or_abort(&sh.iq_full[slot], (j / kItemQ) & 1u, abort)) return -1;
+  const int item = *reinterpret_cast<volatile int*>(&sh.item_q[slot]);
+  if (whole_warp) __syncwarp();
+  if (!whole_warp || (threadIdx.x & 31) == 0) mbar_arrive(&sh.iq_free[slot]);
+  return item;
+}
+
+// One work item: (request, 128-row query tile, kv head).
+struct PrefillItem {
+  int g;       // kv head
+  int c;       // cached tokens of the request
+  int q0;      // batch row of the request's first query
+  int n;       // new tokens of the request
+  int i0;      // first query of the tile (within the request)
+  int kv_len;  // keys the tile's last query sees
+  int nkv;     // key tiles
+  long long bt_row;  // offset of the request's block table row
+};
+
+// Items of the k-th prefill request are numbered tile-major, longest tile
+// first: local index l -> kv head l % Hkv, tile ntile - 1 - l / Hkv. The
+// request's metadata comes from the CTA's shared-memory copy when it holds
+// every prefill request (meta != nullptr), else from global memory.
+__device__ __forceinline__ PrefillItem prefill_item(const PrefillParams& p, int n_req, int item,
+                                                    int QT, const int4* meta,
+                                                    const int* meta_prefix) {
+  PrefillItem m;
+  int r, local;
+  if (meta) {
+    int lo = 0, hi = n_req;  // meta_prefix[lo] <= item < meta_prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (meta_prefix[mid] <= item) lo = mid; else hi = mid;
+    }
+    const int4 v = meta[lo];
+    r = v.x;
+    m.c = v.y;
+    m.q0 = v.z;
+    m.n = v.w;
+    local = item - meta_prefix[lo];
+  } else {
+    const int k = upper_index(p.pf_prefix, n_req, item);
+    r = __ldg(p.pf_req + k);
+    local = item - __ldg(p.pf_prefix + k);
+    m.c = __ldg(p.num_computed + r);
+    m.q0 = __ldg(p.qsl + r);
+    m.n = __ldg(p.qsl + r + 1) - m.q0;
+  }
+  m.g = local % p.num_kv_heads;
+  const int ntile = (m.n + QT - 1) / QT;
+  const int mt = ntile - 1 - local / p.num_kv_heads;
+  m.i0 = mt * QT;
+  const int i_last = min(m.i0 + QT, m.n) - 1;
+  m.kv_len = m.c + i_last + 1;
+  m.nkv = (m.kv_len + kTileN - 1) / kTileN;
+  m.bt_row = static_cast<long long>(r) * p.max_blocks;
+  return m;
+}
+
+// Block table entry e of the item's request if it holds keys < kv_len and its
+// id is in the pool, else -1.
+__device__ __forceinline__ int entry_id(const PrefillParams& p, const PrefillItem& m, int e) {
+  if ((e << p.block_shift) >= m.kv_len) return -1;
+  const int id = __ldg(p.block_table + m.bt_row + e);
+  return (id >= 0 && id < p.num_blocks) ? id : -1;
+}
+
+// Chunk b (keys 16b .. 16b+15) of tile kt holds keys < kv_len, all of them in
+// blocks of the pool.
+__device__ __forceinline__ bool chunk_ok(const PrefillParams& p, const PrefillItem& m, int kt, int b) {
+  const int k0 = kt * kTileN + b * kChunkKeys;
+  if (k0 >= m.kv_len) return false;
+  const int bsh = p.block_shift;
+  if (bsh == 4) return entry_id(p, m, k0 >> 4) >= 0;
+  if (bsh == 5) return entry_id(p, m, k0 >> 5) >= 0;
+  return entry_id(p, m, k0 >> 3) >= 0 && (k0 + 8 >= m.kv_len || entry_id(p, m, (k0 >> 3) + 1) >= 0);
+}
+
+// Persistent CTAs; CTA b takes items b, b + gridDim.x, ... (items come
+// longest first within a request). Every role walks that list on its own and
+// the roles meet only at mbarriers, so the next item's Q/K/V copies and first
+// S MMAs overlap the current item's last tiles and epilogue.
+//   warp 9:  Q copy (once the previous item's last S is done) and K tiles
+//            into a 3-slot ring (a slot is refilled once its S is done);
+//   warp 10: V tiles into a 2-slot ring (refilled once its PV is done);
+//   warp 8, lane 0: every MMA, in the order S(0), S(1), PV(0), S(2), PV(1),
+//            S(3), ...: S_w = Q K^T into TMEM columns [256w, 256w+128), and
+//            O_w += P_w V with P_w read from TMEM, where softmax w wrote it
+//            over S_w (bf16 pairs, one pair per 32-bit column). MMAs run in
+//            issue order, so S(kt+2) overwrites P_w only after PV(kt) read it.
+//   warpgroups 0 and 1: softmax of tiles w, w+2, ... with their own running
+//            max and sum and their own O_w at TMEM columns [256w+128, 256w+128+D);
+//            at the end of the item the two partials are merged (log-sum-exp)
+//            and each warpgroup writes half of the output columns.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
@@ -232,27 +376,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   PrefillShared& sh = *reinterpret_cast<PrefillShared*>(gbase + Lay::kBar);
   volatile int* abort_flag = &sh.abort;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int wg = tid >> 7;          // 0, 1 softmax warpgroups; 2 = issuer warp
-  const int row = tid & 127;        // query row of this softmax thread (TMEM lane)
   const int G = p.group, QT = kTileM / G;
 
-  if (tid == kIssuer) {
+  if (tid == 0) {
     mbar_init(&sh.q_full, 1);
-    for (int i = 0; i < kStages; ++i) {
+    mbar_init(&sh.q_free, 1);
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&sh.k_full[i], 1);
+      mbar_init(&sh.k_free[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&sh.v_full[i], 1);
+      mbar_init(&sh.v_free[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_ready[i], 128);
-      mbar_init(&sh.pv_done[i], 1);
     }
+    mbar_init(&sh.o_full, 1);
+    mbar_init(&sh.o_free, 256);
     mbar_init(&sh.drain, 1);
+    for (int i = 0; i < kItemQ; ++i) {
+      mbar_init(&sh.iq_full[i], 1);
+      mbar_init(&sh.iq_free[i], 10);
+    }
     sh.abort = 0;
     fence_barrier_init();
+  }
+  if (tid == 32 * 9) {
     prefetch_tensormap(&kv_map);
     prefetch_tensormap(&q_map);
   }
+  const int n_items = static_cast<int>(p.hdr[kHdrPrefillItems]);
+  const int n_req = static_cast<int>(p.hdr[kHdrPrefillReqs]);
+  int4* meta_s = reinterpret_cast<int4*>(gbase + Lay::kMeta);
+  int* meta_prefix_s = reinterpret_cast<int*>(gbase + Lay::kMeta + kMetaReqs * 16);
+  if (n_req <= kMetaReqs) {
+    for (int i = tid; i <= n_req; i += kThreads) {
+      meta_prefix_s[i] = __ldg(p.pf_prefix + i);
+      if (i < n_req) {
+        const int r = __ldg(p.pf_req + i);
+        const int q0 = __ldg(p.qsl + r);
+        meta_s[i] = make_int4(r, __ldg(p.num_computed + r), q0, __ldg(p.qsl + r + 1) - q0);
+      }
+    }
+  }
+  // the first work item is claimed while the CTA sets up
+  int first_claim = 0;
+  if (tid == 32 * 9) first_claim = static_cast<int>(atomicAdd(&p.hdr[kHdrPrefillNext], 1u));
   if (warp == 8) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&sh.tmem)),
@@ -264,202 +435,219 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sh.tmem;
-  constexpr uint32_t idesc_qk = tc::idesc_bf16(kTileM, kTileN, 0);
-  constexpr uint32_t idesc_pv = tc::idesc_bf16(kTileM, D, 1);
-  const uint32_t n_items = p.hdr[kHdrPrefillItems];
-  const int n_req = static_cast<int>(p.hdr[kHdrPrefillReqs]);
+  const int4* meta = n_req <= kMetaReqs ? meta_s : nullptr;
+  const int* meta_prefix = meta_prefix_s;
+  auto valid = [&](int item) { return item >= 0 && item < n_items; };
 
-  // phase counters, identical in every thread
-  uint32_t n_q = 0, tiles = 0, cnt[2] = {0, 0};
-  uint32_t drains = 0;
-
-  while (true) {
-    if (tid == kIssuer) sh.item = static_cast<int>(atomicAdd(&p.hdr[kHdrPrefillNext], 1u));
-    __syncthreads();
-    const int item = sh.item;
-    if (item >= static_cast<int>(n_items) || sh.abort) break;
-
-    // ---- which (request, tile, kv head)
-    const int k = upper_index(p.pf_prefix, n_req, item);
-    const int r = __ldg(p.pf_req + k);
-    const int local = item - __ldg(p.pf_prefix + k);
-    const int g = local % p.num_kv_heads;
-    const int c = __ldg(p.num_computed + r);
-    const int q0 = __ldg(p.qsl + r);
-    const int n = __ldg(p.qsl + r + 1) - q0;
-    const int ntile = (n + QT - 1) / QT;
-    const int mt = ntile - 1 - local / p.num_kv_heads;  // longest tiles first
-    const int i0 = mt * QT;
-    const int i_last = min(i0 + QT, n) - 1;
-    const int kv_len = c + i_last + 1;
-    const int nkv = (kv_len + kTileN - 1) / kTileN;
-    const long long bt_row = static_cast<long long>(r) * p.max_blocks;
-    auto stage_of = [&](int kt) { return static_cast<int>((tiles + kt) % kStages); };
-    auto stage_par = [&](int kt) { return ((tiles + kt) / kStages) & 1u; };
-    // block table entry e of the request if it holds keys < kv_len and its id
-    // is in the pool, else -1
+  if (warp == 9 || warp == 10) {
+    // ================= copy warps. Lane (chunk b, d half dh), lanes
+    // 0 .. 8*DH-1, issues the copies of that chunk (one of 16 rows, or two of
+    // 8 rows for 8-token blocks); the block ids of a 32-entry window of the
+    // block table sit in the lanes' registers.
+    const int ln = tid & 31;
+    const bool is_v = warp == 10;
+    const int S = is_v ? kVStages : kKStages;
+    uint64_t* full = is_v ? sh.v_full : sh.k_full;
+    uint64_t* empty = is_v ? sh.v_free : sh.k_free;
+    const uint32_t ring = is_v ? Lay::kV : Lay::kK;
     const int bsh = p.block_shift;
-    auto entry_id = [&](int e) -> int {
-      if ((e << bsh) >= kv_len) return -1;
-      const int id = __ldg(p.block_table + bt_row + e);
-      return (id >= 0 && id < p.num_blocks) ? id : -1;
-    };
-    // chunk b (keys 16b .. 16b+15) of tile kt holds keys < kv_len, all of
-    // them in blocks of the pool
-    auto chunk_ok = [&](int kt, int b) -> bool {
-      const int k0 = kt * kTileN + b * kChunkKeys;
-      if (k0 >= kv_len) return false;
-      if (bsh == 4) return entry_id(k0 >> 4) >= 0;
-      if (bsh == 5) return entry_id(k0 >> 5) >= 0;
-      return entry_id(k0 >> 3) >= 0 && (k0 + 8 >= kv_len || entry_id((k0 >> 3) + 1) >= 0);
-    };
-
-    if (warp >= 8) {
-      // ================= producer warps, each with in-order blocking waits:
-      //   warp 9:  K(kt) TMA copies, once S(kt - 2) is done (its K slot is free)
-      //   warp 10: V(kt) TMA copies, once PV(kt - 2) is done (its V slot is free)
-      //   warp 8:  MMAs: S(kt) once K(kt) landed and softmax(kt - 2) read S_w;
-      //            PV(kt) once softmax(kt) wrote P_w and V(kt) landed
-      // Lane (chunk b, d half dh), lanes 0 .. 8*DH-1, issues the copies of
-      // that chunk (one of 16 rows, or two of 8 rows for 8-token blocks); the
-      // block ids of a 32-entry window of the block table sit in the lanes'
-      // registers.
-      const int ln = tid & 31;
-      auto phase = [&](int kt) { return (cnt[kt & 1] + (kt >> 1)) & 1u; };
-      bool ok = true;
-      if (warp == 9 || warp == 10) {
-        const int is_v = warp == 10;
-        if (!is_v && ln == 0) {
+    const int E = kTileN >> bsh;  // table entries per tile
+    uint32_t T = 0;               // tiles issued so far (all items)
+    bool ok = true;
+    int q_loads = 0;
+    for (int it = 0; ok; ++it) {
+      int item;
+      if (!is_v) {
+        // the Q buffer is free once the previous item's last S is done; only
+        // then is the next item claimed (work counter), so that items go to
+        // the CTAs that are about to be idle
+        if (it > 0) ok = wait_or_abort(&sh.q_free, (it - 1) & 1u, abort_flag);
+        if (!ok) break;
+        item = n_items;
+        if (ln == 0) {
+          const int slot = it % kItemQ;
+          if (it >= kItemQ) ok = wait_or_abort(&sh.iq_free[slot], ((it - kItemQ) / kItemQ) & 1u, abort_flag);
+          if (ok) item = it == 0 ? first_claim : static_cast<int>(atomicAdd(&p.hdr[kHdrPrefillNext], 1u));
+          sh.item_q[slot] = item;
+          mbar_arrive(&sh.iq_full[slot]);
+        }
+        item = __shfl_sync(0xffffffffu, item, 0);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      } else {
+        item = take_item(sh, it, abort_flag, true);
+        if (item < 0) ok = false;
+      }
+      if (!ok || !valid(item)) break;
+      const PrefillItem m = prefill_item(p, n_req, item, QT, meta, meta_prefix);
+      if (!is_v) {
+        if (ln == 0) {
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(&sh.q_full, DH * Lay::kChunk);
 #pragma unroll
           for (int dh = 0; dh < DH; ++dh)
-            tma_load_3d(gbase + Lay::kQ + dh * Lay::kChunk, &q_map, dh * 64, g * G, q0 + i0,
+            tma_load_3d(gbase + Lay::kQ + dh * Lay::kChunk, &q_map, dh * 64, m.g * G, m.q0 + m.i0,
                         &sh.q_full);
         }
-        int win_base = -1000000, win_val = -1;
-        for (int kt = 0; ok && kt < nkv; ++kt) {
-          if (kt >= kStages) {  // the slot's previous tile (kt - 2) must be done with it
-            ok = wait_or_abort(is_v ? &sh.pv_done[kt & 1] : &sh.s_full[kt & 1], phase(kt - 2),
-                               abort_flag);
-            if (!ok) break;
-          }
-          const int st = stage_of(kt);
-          const int E = kTileN >> bsh;  // table entries per tile
-          if (kt * E + E > win_base + 32) {
-            win_base = kt * E;
-            const int e = win_base + ln;
-            win_val = entry_id(e);
-            if (!is_v && (e << bsh) < kv_len && win_val < 0)
-              atomicOr(&g_errors_prefill, kErrBlockRange);
-          }
-          const int b = (ln / DH) & 7, dh = ln % DH;
-          // pool rows of one kv head: (block * 2 + k|v) * B + offset
-          int id0, id1 = -1, row0, row1 = 0;
-          if (bsh == 4) {
-            id0 = __shfl_sync(0xffffffffu, win_val, kt * 8 + b - win_base);
-            row0 = id0 * 32 + (is_v ? 16 : 0);
-          } else if (bsh == 5) {
-            id0 = __shfl_sync(0xffffffffu, win_val, kt * 4 + (b >> 1) - win_base);
-            row0 = id0 * 64 + (b & 1) * 16 + (is_v ? 32 : 0);
-          } else {
-            id0 = __shfl_sync(0xffffffffu, win_val, kt * 16 + 2 * b - win_base);
-            id1 = __shfl_sync(0xffffffffu, win_val, kt * 16 + 2 * b + 1 - win_base);
-            row0 = id0 * 16 + (is_v ? 8 : 0);
-            row1 = id1 * 16 + (is_v ? 8 : 0);
-          }
-          const bool mine0 = ln < 8 * DH && id0 >= 0;
-          const bool mine1 = ln < 8 * DH && id1 >= 0;
-          const uint32_t bytes = bsh == 3 ? (mine0 ? 1024u : 0u) + (mine1 ? 1024u : 0u)
-                                         : (mine0 ? 2048u : 0u);
-          const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes);
-          uint64_t* bar = is_v ? &sh.v_full[st] : &sh.k_full[st];
-          if (ln == 0) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, tx);
-          }
-          __syncwarp();
-          unsigned char* dst = gbase + (is_v ? Lay::kV : Lay::kK) + st * Lay::kTileKV +
-                               dh * Lay::kChunk + b * 2048;
-          if (mine0) tma_load_3d(dst, &kv_map, dh * 64, g, row0, bar);
-          if (mine1) tma_load_3d(dst + 1024, &kv_map, dh * 64, g, row1, bar);
+        ++q_loads;
+      }
+      int win_base = -1000000, win_val = -1;
+      for (int kt = 0; kt < m.nkv; ++kt) {
+        const int slot = static_cast<int>(T % S);
+        if (T >= static_cast<uint32_t>(S)) {
+          ok = wait_or_abort(&empty[slot], ((T - S) / S) & 1u, abort_flag);
+          if (!ok) break;
         }
-      } else if (warp == 8 && ln == 0) {
-        auto issue_s = [&](int kt) {  // S_w = Q K^T for tile kt
-          const int w = kt & 1, st = stage_of(kt);
+        if (kt * E + E > win_base + 32) {
+          win_base = kt * E;
+          const int e = win_base + ln;
+          win_val = entry_id(p, m, e);
+          if (!is_v && (e << bsh) < m.kv_len && win_val < 0)
+            atomicOr(&g_errors_prefill, kErrBlockRange);
+        }
+        const int b = (ln / DH) & 7, dh = ln % DH;
+        // pool rows of one kv head: (block * 2 + k|v) * B + offset
+        int id0, id1 = -1, row0, row1 = 0;
+        if (bsh == 4) {
+          id0 = __shfl_sync(0xffffffffu, win_val, kt * 8 + b - win_base);
+          row0 = id0 * 32 + (is_v ? 16 : 0);
+        } else if (bsh == 5) {
+          id0 = __shfl_sync(0xffffffffu, win_val, kt * 4 + (b >> 1) - win_base);
+          row0 = id0 * 64 + (b & 1) * 16 + (is_v ? 32 : 0);
+        } else {
+          id0 = __shfl_sync(0xffffffffu, win_val, kt * 16 + 2 * b - win_base);
+          id1 = __shfl_sync(0xffffffffu, win_val, kt * 16 + 2 * b + 1 - win_base);
+          row0 = id0 * 16 + (is_v ? 8 : 0);
+          row1 = id1 * 16 + (is_v ? 8 : 0);
+        }
+        const bool mine0 = ln < 8 * DH && id0 >= 0;
+        const bool mine1 = ln < 8 * DH && id1 >= 0;
+        const uint32_t bytes = bsh == 3 ? (mine0 ? 1024u : 0u) + (mine1 ? 1024u : 0u)
+                                        : (mine0 ? 2048u : 0u);
+        const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes);
+        if (ln == 0) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(&full[slot], tx);
+        }
+        __syncwarp();
+        unsigned char* dst = gbase + ring + slot * Lay::kTileKV + dh * Lay::kChunk + b * 2048;
+        if (mine0) tma_load_3d(dst, &kv_map, dh * 64, m.g, row0, &full[slot]);
+        if (mine1) tma_load_3d(dst + 1024, &kv_map, dh * 64, m.g, row1, &full[slot]);
+        ++T;
+      }
+    }
+    if (!ok) {  // let the copies in flight land before the shared memory goes away
+      for (int s = 0; s < S; ++s)
+        if (T > static_cast<uint32_t>(s)) {
+          const uint32_t last = s + S * ((T - 1 - s) / S);
+          mbar_wait(&full[s], (last / S) & 1u, kDrainLimitNs);
+        }
+      if (!is_v && q_loads > 0) mbar_wait(&sh.q_full, (q_loads - 1) & 1u, kDrainLimitNs);
+    }
+  } else if (warp == 8) {
+    // ================= MMA thread
+    if ((tid & 31) == 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_bf16(kTileM, kTileN, 0);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16(kTileM, D, 1);
+      uint32_t T = 0, np[2] = {0, 0};
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int item = take_item(sh, it, abort_flag, false);
+        if (item < 0) ok = false;
+        if (!ok || !valid(item)) break;
+        const PrefillItem m = prefill_item(p, n_req, item, QT, meta, meta_prefix);
+        const int nkv = m.nkv;
+        auto issue_s = [&](int kt) -> bool {  // S_w = Q K^T for tile kt
+          const int w = kt & 1;
+          const uint32_t Tk = T + kt;
+          const int slot = static_cast<int>(Tk % kKStages);
+          if (!wait_or_abort(&sh.k_full[slot], (Tk / kKStages) & 1u, abort_flag)) return false;
           tc::fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Lay::kChunk + (kk & 3) * 32;
             const uint64_t a = tc::sw128_desc(base + Lay::kQ + off, 16, 1024);
-            const uint64_t b = tc::sw128_desc(base + Lay::kK + st * Lay::kTileKV + off, 16, 1024);
+            const uint64_t b = tc::sw128_desc(base + Lay::kK + slot * Lay::kTileKV + off, 16, 1024);
             tc::mma_bf16(tmem + w * 256u, a, b, idesc_qk, kk > 0);
           }
           tc::commit(&sh.s_full[w]);
+          tc::commit(&sh.k_free[slot]);
+          if (kt == nkv - 1) tc::commit(&sh.q_free);
+          return true;
         };
-        auto issue_pv = [&](int kt) {  // O_w += P_w V for tile kt, P_w from smem
-          const int w = kt & 1, st = stage_of(kt);
+        auto issue_pv = [&](int kt) -> bool {  // O_w += P_w V for tile kt, P_w from TMEM
+          const int w = kt & 1;
+          const uint32_t Tv = T + kt;
+          const int slot = static_cast<int>(Tv % kVStages);
+          if (!wait_or_abort(&sh.v_full[slot], (Tv / kVStages) & 1u, abort_flag)) return false;
           tc::fence_after_sync();
-          const uint32_t vbase = base + Lay::kV + st * Lay::kTileKV;
-          const uint32_t pbase = base + Lay::kP + w * 2 * Lay::kChunk;
+          const uint32_t vbase = base + Lay::kV + slot * Lay::kTileKV;
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk) {
-            const uint64_t a =
-                tc::sw128_desc(pbase + (kk >> 2) * Lay::kChunk + (kk & 3) * 32, 16, 1024);
             const uint64_t b = tc::sw128_desc(vbase + kk * 2048, Lay::kChunk, 1024);
-            tc::mma_bf16(tmem + w * 256u + 128u, a, b, idesc_pv, (kt >= 2 || kk > 0) ? 1u : 0u);
+            tc::mma_bf16_ts(tmem + w * 256u + 128u, tmem + w * 256u + kk * 8u, b, idesc_pv,
+                            (kt >= 2 || kk > 0) ? 1u : 0u);
           }
-          tc::commit(&sh.pv_done[w]);
+          tc::commit(&sh.v_free[slot]);
+          if (kt == nkv - 1) tc::commit(&sh.o_full);
+          return true;
         };
-        ok = wait_or_abort(&sh.q_full, n_q & 1u, abort_flag);
-        for (int kt = 0; ok && kt < 2 && kt < nkv; ++kt) {
-          ok = wait_or_abort(&sh.k_full[stage_of(kt)], stage_par(kt), abort_flag);
-          if (ok) issue_s(kt);
-        }
-        // after softmax(kt): S(kt + 2) first (the warpgroup's next softmax
-        // waits on it), then PV(kt) (needed only before its next P write)
+        ok = wait_or_abort(&sh.q_full, it & 1u, abort_flag);
+        if (ok) ok = issue_s(0);
+        if (ok && nkv > 1) ok = issue_s(1);
         for (int kt = 0; ok && kt < nkv; ++kt) {
-          ok = wait_or_abort(&sh.p_ready[kt & 1], phase(kt), abort_flag);
-          if (ok && kt + 2 < nkv) {
-            ok = wait_or_abort(&sh.k_full[stage_of(kt + 2)], stage_par(kt + 2), abort_flag);
-            if (ok) issue_s(kt + 2);
-          }
-          if (ok) ok = wait_or_abort(&sh.v_full[stage_of(kt)], stage_par(kt), abort_flag);
-          if (!ok) break;
-          issue_pv(kt);
+          const int w = kt & 1;
+          ok = wait_or_abort(&sh.p_ready[w], np[w] & 1u, abort_flag);
+          ++np[w];
+          // the previous item's O must have been read before PV(0) overwrites it
+          if (ok && kt == 0 && it > 0) ok = wait_or_abort(&sh.o_free, (it - 1) & 1u, abort_flag);
+          if (ok) ok = issue_pv(kt);
+          if (ok && kt + 2 < nkv) ok = issue_s(kt + 2);
         }
-        if (!ok) {  // let issued MMAs finish before anything is torn down
-          tc::commit(&sh.drain);
-          mbar_wait(&sh.drain, drains & 1u, kDrainLimitNs);
-        }
+        T += nkv;
       }
-      if (warp == 8) drains += __shfl_sync(0xffffffffu, ok ? 0u : 1u, 0);
-    } else if (wg < 2) {
-      // ================= softmax warpgroup wg: tiles wg, wg + 2, ...
-      const int qi = i0 + row / G;              // query of this row
-      const int lim = min(c + qi, kv_len - 1);  // last key this row may see
-      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const uint32_t t_s = tmem + lane_base + wg * 256u;
+      // every MMA (and the arrivals of its commits) done before teardown
+      tc::commit(&sh.drain);
+      mbar_wait(&sh.drain, 0, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ================= softmax warpgroup wg: tiles wg, wg + 2, ... of each item
+    const int wg = tid >> 7;
+    const int row = tid & 127;  // query row of this thread (TMEM lane)
+    const int lane = tid & 31;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + wg * 256u;  // S_wg, then P_wg
+    const uint32_t t_o = t_s + 128u;                     // O_wg
+    uint32_t T = 0, ns = 0;
+    bool ok = true;
+    // the two warpgroups take every decision to stop together (softmax_any)
+    int item = take_item(sh, 0, abort_flag, true);
+    bool stop = softmax_any(!valid(item));
+    // chunk validity of tile kt of item m (lanes 0..7), read one tile ahead
+    auto load_ids = [&](const PrefillItem& mm, int kt) -> int {
+      return (lane < 8 && kt < mm.nkv && chunk_ok(p, mm, kt, lane)) ? 1 : -1;
+    };
+    PrefillItem m{};
+    int next_id = -1;
+    if (!stop) {
+      m = prefill_item(p, n_req, item, QT, meta, meta_prefix);
+      next_id = load_ids(m, wg);
+    }
+    for (int it = 0; !stop; ++it) {
+      const int nkv = m.nkv;
+      const int qi = m.i0 + row / G;                    // query of this row
+      const int lim = min(m.c + qi, m.kv_len - 1);      // last key this row may see
       float m_run = -INFINITY, l_run = 0.f;
-      bool ok = true;
-      int nmine = 0;
-      const int lane = tid & 31;
-      // block ids of this warpgroup's next tile, loaded one tile ahead by lanes 0..7
-      auto load_ids = [&](int kt) -> int {
-        return (lane < 8 && kt < nkv && chunk_ok(kt, lane)) ? 1 : -1;
-      };
-      int next_id = load_ids(wg);
-      for (int kt = wg; ok && kt < nkv; kt += 2, ++nmine) {
-        const uint32_t ph = cnt[wg] + (kt >> 1);
+      for (int kt = wg, nmine = 0; kt < nkv; kt += 2, ++nmine) {
         const uint32_t mask = __ballot_sync(0xffffffffu, next_id >= 0) & 0xFFu;
-        next_id = load_ids(kt + 2);
-        ok = wait_or_abort(&sh.s_full[wg], ph & 1u, abort_flag);
+        ok = wait_or_abort(&sh.s_full[wg], ns & 1u, abort_flag);
+        ++ns;
         if (!ok) break;
         tc::fence_after_sync();
         // a tile every row sees in full needs no mask; otherwise column j is
         // visible iff j <= jlim and its 16-key chunk was loaded (chunk c =
         // columns 16c .. 16c+15)
-        const bool full = kt * kTileN + kTileN - 1 <= c + i0 && mask == 0xFFu;
+        const bool full = kt * kTileN + kTileN - 1 <= m.c + m.i0 && mask == 0xFFu;
         const int jlim = lim - kt * kTileN;
         // the whole S row in one TMEM round trip: 4 x 32 columns, one wait
         uint32_t sr[4][32];
@@ -467,8 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) tc::ld32(t_s + q * 32, sr[q]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) tc::wait32(sr[q]);
-        // invisible columns become -inf
-        if (!full) {
+        if (!full) {  // invisible columns become -inf
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -482,59 +669,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q)
 #pragma unroll
           for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[q][i]));
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
         // (scale > 0 keeps the argmax)
-        // PV(kt - 2) must be done before O_wg is rescaled and P_wg rewritten
-        if (kt >= 2) {
-          ok = wait_or_abort(&sh.pv_done[wg], (ph - 1) & 1u, abort_flag);
-          if (!ok) break;
-          tc::fence_after_sync();
-        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
         if (__any_sync(0xffffffffu, mx > m_run + kRescaleLog2)) {
           const float m_new = fmaxf(m_run, mx);
           const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
           l_run *= alpha;
           m_run = m_new;
-          if (kt >= 2) {
+          // O_wg holds PV of this warpgroup's earlier tiles (all done: S(kt)
+          // was issued after them)
+          if (nmine > 0) {
 #pragma unroll 1
             for (int q = 0; q < D / 16; ++q) {
               uint32_t o[16];
-              tc::ld16(t_s + 128u + q * 16, o);
+              tc::ld16(t_o + q * 16, o);
               tc::wait16(o);
 #pragma unroll
               for (int x = 0; x < 16; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-              tc::st16(t_s + 128u + q * 16, o);
+              tc::st16(t_o + q * 16, o);
             }
           }
         }
-        // P = 2^(s * scale - m) as bf16 (-inf -> 0), row `row` of P_wg in smem
-        // (K-major, 128-byte swizzle: 16-byte chunk c of a row sits at c ^ (row % 8))
+        // P = 2^(s * scale - m) as bf16 (-inf -> 0) over S_wg: column j of the
+        // row holds keys 2j (low half) and 2j+1
         float ps4[4] = {0.f, 0.f, 0.f, 0.f};
         const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-        unsigned char* prow = gbase + Lay::kP + wg * 2 * Lay::kChunk + row * 128;
 #pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8) {  // 8 keys = one 16-byte chunk
-          uint32_t w[4];
+        for (int q = 0; q < 4; ++q) {  // keys 32q .. 32q+31 -> columns 16q .. 16q+15
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = c8 * 8 + 2 * e;
-            const float p0 = exp2f(__uint_as_float(sr[j >> 5][j & 31]) * p.scale_log2 - msub);
-            const float p1 = exp2f(__uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]) * p.scale_log2 - msub);
-            w[e] = pack_bf16x2(p0, p1);
-            ps4[e] += p0 + p1;
+          for (int j = 0; j < 16; ++j) {
+            const float p0 = exp2f(__uint_as_float(sr[q][2 * j]) * p.scale_log2 - msub);
+            const float p1 = exp2f(__uint_as_float(sr[q][2 * j + 1]) * p.scale_log2 - msub);
+            pk[j] = pack_bf16x2(p0, p1);
+            ps4[j & 3] += p0 + p1;
           }
-          *reinterpret_cast<uint4*>(prow + (c8 >> 3) * Lay::kChunk + (((c8 & 7) ^ (row & 7)) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+          tc::st16(t_s + 16 * q, pk);
         }
         l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
         // V rows of keys past kv_len or of chunks not loaded must be zero
         // (0 * NaN): for such a tile wait for its V copy first
-        if (kt * kTileN + kTileN > kv_len || mask != 0xFFu) {
-          ok = wait_or_abort(&sh.v_full[stage_of(kt)], stage_par(kt), abort_flag);
+        if (kt * kTileN + kTileN > m.kv_len || mask != 0xFFu) {
+          const uint32_t Tv = T + kt;
+          const int slot = static_cast<int>(Tv % kVStages);
+          ok = wait_or_abort(&sh.v_full[slot], (Tv / kVStages) & 1u, abort_flag);
           if (!ok) break;
           const int key = kt * kTileN + row;
-          if (key >= kv_len || !(mask >> (row >> 4) & 1u)) {
-            unsigned char* vrow = gbase + Lay::kV + stage_of(kt) * Lay::kTileKV;
+          if (key >= m.kv_len || !(mask >> (row >> 4) & 1u)) {
+            unsigned char* vrow = gbase + Lay::kV + slot * Lay::kTileKV;
 #pragma unroll
             for (int dh = 0; dh < DH; ++dh) {
               uint4* v4 = reinterpret_cast<uint4*>(vrow + dh * Lay::kChunk + row * 128);
@@ -542,35 +724,44 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int x = 0; x < 8; ++x) v4[x] = make_uint4(0, 0, 0, 0);
             }
           }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         tc::wait_st();
         tc::fence_before_sync();
         mbar_arrive(&sh.p_ready[wg]);
+        next_id = load_ids(m, kt + 2);  // its latency hides under the next S wait
       }
-      if (ok && nmine > 0)  // this warpgroup's last PV
-        ok = wait_or_abort(&sh.pv_done[wg], (cnt[wg] + nmine - 1) & 1u, abort_flag);
+      // ---- the next item's id and metadata, while the last PVs run
+      const int item_n = ok ? take_item(sh, it + 1, abort_flag, true) : -1;
+      if (item_n < 0) ok = false;  // aborted: both warpgroups learn it below
+      PrefillItem m_next{};
+      if (valid(item_n)) {
+        m_next = prefill_item(p, n_req, item_n, QT, meta, meta_prefix);
+        next_id = load_ids(m_next, wg);  // first tile of the next item
+      }
+      // ---- merge the two partial results of the item
+      if (ok) ok = wait_or_abort(&sh.o_full, it & 1u, abort_flag);
       tc::fence_after_sync();
-      // ---- merge the two partial results. Each warpgroup posts its (max,
-      // sum) in its own P buffer, which no MMA reads any more (its last PV is
-      // done, or it had no tiles); Q may still be in use by the other's MMAs.
-      float2* ml_own = reinterpret_cast<float2*>(gbase + Lay::kP + wg * 2 * Lay::kChunk);
-      ml_own[row] = make_float2(m_run, l_run);
-      tc::fence_before_sync();
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      tc::fence_after_sync();
-      const float2 ml0 = reinterpret_cast<const float2*>(gbase + Lay::kP)[row];
-      const float2 ml1 = reinterpret_cast<const float2*>(gbase + Lay::kP + 2 * Lay::kChunk)[row];
+      float2* ml = reinterpret_cast<float2*>(gbase + Lay::kML) + (it & 1) * 2 * kTileM;
+      ml[wg * kTileM + row] = make_float2(m_run, l_run);
+      // (also the barrier that publishes ml) both warpgroups stop together:
+      // on a failure, or when the next item is the end marker (the same
+      // queue slot for both)
+      const bool failed = softmax_any(!ok || *abort_flag);
+      stop = failed || !valid(item_n);
+      const float2 ml0 = ml[row];
+      const float2 ml1 = ml[kTileM + row];
       const float M = fmaxf(ml0.x, ml1.x);
       const float a0 = (ml0.x == -INFINITY) ? 0.f : exp2f(ml0.x - M);
       const float a1 = (ml1.x == -INFINITY) ? 0.f : exp2f(ml1.x - M);
       const float inv = 1.f / (ml0.y * a0 + ml1.y * a1);
       const bool has1 = nkv > 1;
-      const bool store = ok && qi < n;
-      uint16_t* dst = p.out + (static_cast<long long>(q0 + qi) * p.num_q_heads + g * G + row % G) * D;
+      const bool store = !failed && qi < m.n;
+      uint16_t* dst =
+          p.out + (static_cast<long long>(m.q0 + qi) * p.num_q_heads + m.g * G + row % G) * D;
       const uint32_t t_o0 = tmem + lane_base + 128u, t_o1 = tmem + lane_base + 256u + 128u;
 #pragma unroll 1
-      for (int q = 0; q < D / 32; ++q) {  // this warpgroup's D/2 columns, 16 at a time
+      for (int q = 0; q < D / 32; ++q) {
         const int col = wg * (D / 2) + q * 16;
         uint32_t o0[16], o1[16];
         tc::ld16(t_o0 + col, o0);
@@ -594,23 +785,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
+      tc::fence_before_sync();
+      mbar_arrive(&sh.o_free);
+      T += nkv;
+      m = m_next;
     }
-    tc::fence_before_sync();
-    __syncthreads();  // O read, merge space reusable, next item may overwrite TMEM
-    tc::fence_after_sync();
-    tiles += nkv;
-    cnt[0] += (nkv + 1) / 2;
-    cnt[1] += nkv / 2;
-    ++n_q;
   }
 
-  if (sh.abort && tid == kIssuer) {
-    // let copies in flight land before the shared memory goes away
-    for (int st = 0; st < kStages; ++st) {
-      mbar_wait(&sh.k_full[st], 0, kDrainLimitNs);
-      mbar_wait(&sh.v_full[st], 0, kDrainLimitNs);
-    }
-  }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 8) {
