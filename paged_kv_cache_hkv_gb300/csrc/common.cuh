@@ -21,6 +21,16 @@ constexpr int kChunkKeys = 16;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s, when cleaning up
 
+// Programmatic dependent launch. Every kernel of the step lets the next one
+// launch as soon as it starts (its CTAs then run their prologue while this
+// grid finishes), and waits for the previous grid -- its completion and the
+// visibility of its memory -- before touching anything that grid wrote. Both
+// are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

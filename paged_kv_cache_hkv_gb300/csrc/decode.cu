@@ -107,6 +107,8 @@ __device__ __forceinline__ Int3 plan_counts(const AttnArgs& a, int r, int tile_q
 // flagged.
 __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, AttnWorkspace ws, int tile_q) {
   __shared__ Int3 total;
+  pdl_trigger();
+  pdl_wait();
   const int R = a.num_reqs;
   const int per = (R + 1023) / 1024;
   const int r0 = min(R, static_cast<int>(threadIdx.x) * per), r1 = min(R, r0 + per);
@@ -243,6 +245,9 @@ __global__ void __launch_bounds__(WARPS * 32)
   unsigned char* smem_base = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   Smem& sm = reinterpret_cast<Smem*>(smem_base)[warp];
   const int sub = lane / C::LPK, li = lane % C::LPK;
+  // no early trigger here: the combine kernel's CTAs, resident next to these
+  // for the whole decode while they wait for it, slow the decode warps down
+  pdl_wait();
 
   const long long W = p.warps;
   const long long w = static_cast<long long>(blockIdx.x) * WARPS + warp;
@@ -582,6 +587,8 @@ __global__ void __launch_bounds__(GW * 32) combine_kernel(const DecodeParams p) 
   const long long w = blockIdx.x;
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long W = p.warps;
+  pdl_trigger();
+  pdl_wait();
   if (w < 1 || w >= W) return;
   const int2 rec = p.bound[w];
   if (rec.x < 0) return;
@@ -660,9 +667,21 @@ __global__ void __launch_bounds__(GW * 32) combine_kernel(const DecodeParams p) 
 constexpr int kDecodeStages = PKV_DECODE_STAGES;  // smem stages per warp
 constexpr int kDecodeWarps = PKV_DECODE_WARPS;    // warps per CTA
 
+// At most this many decode CTAs per SM in the default split, even where
+// registers would fit a third: on the 1280-decode mixed
+// step (d = 128, 32 q / 8 kv heads) 2 CTAs of 4 warps per SM streamed at
+// 0.98 of the copy peak and 3 at 0.93 (shorter warp ranges, more partials).
+constexpr int kDecodeMaxCtasPerSm = 2;
+
 template <int D, int GW>
 constexpr size_t decode_smem_bytes() {
-  return sizeof(typename DecodeCfg<D, GW, kDecodeStages>::WarpSmem) * kDecodeWarps + 128;
+  // At least a third of an SM's shared memory (228 KB), so that no SM ever
+  // holds more than kDecodeMaxCtasPerSm CTAs -- also when the grid is
+  // launched early (programmatic dependent launch) and its first CTAs land
+  // on the few SMs the previous kernel has already left.
+  constexpr size_t used = sizeof(typename DecodeCfg<D, GW, kDecodeStages>::WarpSmem) * kDecodeWarps + 128;
+  constexpr size_t third = 228u * 1024u / 3u + 1024u;
+  return used > third ? used : third;
 }
 
 template <int D, int GW, int SH>
@@ -685,12 +704,12 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_
   cudaError_t e = smem_attr_once(kern, static_cast<int>(smem), g_decode_attr_done<D, GW, SH>);
   if (e != cudaSuccess) return e;
   const long long grid = (p.warps + kDecodeWarps - 1) / kDecodeWarps;
-  kern<<<static_cast<unsigned>(grid), kDecodeWarps * 32, smem, stream>>>(kv_map, p);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kDecodeWarps * 32), smem, stream,
+                 kv_map, p);
   if (e == cudaSuccess && trace) e = cudaEventRecord(static_cast<cudaEvent_t>(trace[3]), stream);
   if (e != cudaSuccess) return e;
-  combine_kernel<D, GW><<<static_cast<unsigned>(p.warps), GW * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel<D, GW>, dim3(static_cast<unsigned>(p.warps)), dim3(GW * 32), 0,
+                    stream, p);
 }
 
 // Calls F<D, GW, SH>::run(args...) for the instantiated shapes: head_dim 64 or
@@ -720,11 +739,6 @@ struct LaunchOp {
   }
 };
 
-// At most this many decode CTAs per SM in the default split, even where
-// registers and shared memory would fit a third: on the 1280-decode mixed
-// step (d = 128, 32 q / 8 kv heads) 2 CTAs of 4 warps per SM streamed at
-// 0.98 of the copy peak and 3 at 0.93 (shorter warp ranges, more partials).
-constexpr int kDecodeMaxCtasPerSm = 2;
 
 cudaError_t decode_full_wave_warps(int head_dim, int group, int block_shift, int num_sms,
                                    int* warps) {
@@ -740,8 +754,7 @@ cudaError_t decode_full_wave_warps(int head_dim, int group, int block_shift, int
 
 cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream) {
   const int group = a.num_q_heads / a.num_kv_heads;
-  plan_kernel<<<1, 1024, 0, stream>>>(a, ws, 128 / group);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, a, ws, 128 / group);
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,

@@ -26,6 +26,8 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
                                     const int32_t* __restrict__ qsl,
                                     const int32_t* __restrict__ num_computed, int num_reqs,
                                     int num_tokens, int num_blocks, int shift, int req_blocks) {
+  pdl_trigger();
+  pdl_wait();
   if (static_cast<int>(blockIdx.x) >= req_blocks) {  // padding rows
     const int t = (blockIdx.x - req_blocks) * blockDim.x + threadIdx.x;
     if (t < num_tokens && t >= __ldg(qsl + num_reqs)) slots[t] = -1;
@@ -64,6 +66,8 @@ __global__ void kv_write_kernel(uint4* __restrict__ pool, const uint4* __restric
                                 const uint4* __restrict__ value, long long key_stride_v,
                                 long long value_stride_v, const int64_t* __restrict__ slots,
                                 int num_tokens, int vec_per_row, int shift, long long num_slots) {
+  pdl_trigger();
+  pdl_wait();
   for (int t = blockIdx.x; t < num_tokens; t += gridDim.x) {
     const long long s = __ldg(slots + t);
     if (s < 0) continue;
@@ -92,6 +96,8 @@ __global__ void kv_write_kernel(uint4* __restrict__ pool, const uint4* __restric
 __global__ void copy_blocks_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
                                    const int32_t* __restrict__ pairs, int num_pairs,
                                    int dst_num_blocks, int src_num_blocks, int vec_per_block) {
+  pdl_trigger();
+  pdl_wait();
   for (int i = blockIdx.x; i < num_pairs; i += gridDim.x) {
     const int s = __ldg(pairs + 2 * i), d = __ldg(pairs + 2 * i + 1);
     if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks) {
@@ -111,10 +117,9 @@ cudaError_t launch_copy_blocks(void* dst, int dst_num_blocks, const void* src, i
   const int vec_per_block = 2 * block_size * num_kv_heads * head_dim / 8;
   const long long cap = static_cast<long long>(num_sms) * 8;
   const int grid = static_cast<int>(num_pairs < cap ? num_pairs : cap);
-  copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(dst),
-                                               static_cast<const uint4*>(src), pairs, num_pairs,
-                                               dst_num_blocks, src_num_blocks, vec_per_block);
-  return cudaGetLastError();
+  return launch_pdl(copy_blocks_kernel, dim3(grid), dim3(256), 0, stream, static_cast<uint4*>(dst),
+                    static_cast<const uint4*>(src), pairs, num_pairs, dst_num_blocks,
+                    src_num_blocks, vec_per_block);
 }
 
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int max_blocks,
@@ -125,10 +130,10 @@ cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int 
   const int threads = 256;
   const int req_blocks = (num_reqs + threads / 32 - 1) / (threads / 32);
   const int pad_blocks = (num_tokens + threads - 1) / threads;
-  slot_mapping_kernel<<<req_blocks + pad_blocks, threads, 0, stream>>>(
-      slots, block_table, max_blocks, qsl, num_computed, num_reqs, num_tokens, num_blocks,
-      __builtin_ctz(static_cast<unsigned>(block_size)), req_blocks);
-  return cudaGetLastError();
+  return launch_pdl(slot_mapping_kernel, dim3(req_blocks + pad_blocks), dim3(threads), 0, stream,
+                    slots, block_table, max_blocks, qsl, num_computed, num_reqs, num_tokens,
+                    num_blocks, static_cast<int>(__builtin_ctz(static_cast<unsigned>(block_size))),
+                    req_blocks);
 }
 
 cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long long key_stride,
@@ -140,12 +145,11 @@ cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long
   const int threads = vec_per_row >= 128 ? 128 : (vec_per_row >= 64 ? 64 : 32);
   const long long cap = static_cast<long long>(num_sms) * 16;
   const int grid = static_cast<int>(num_tokens < cap ? num_tokens : cap);
-  kv_write_kernel<<<grid, threads, 0, stream>>>(
-      static_cast<uint4*>(pool), static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-      key_stride / 8, value_stride / 8, slots, num_tokens, vec_per_row,
-      __builtin_ctz(static_cast<unsigned>(block_size)),
-      static_cast<long long>(num_blocks) * block_size);
-  return cudaGetLastError();
+  return launch_pdl(kv_write_kernel, dim3(grid), dim3(threads), 0, stream, static_cast<uint4*>(pool),
+                    static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                    key_stride / 8, value_stride / 8, slots, num_tokens, vec_per_row,
+                    static_cast<int>(__builtin_ctz(static_cast<unsigned>(block_size))),
+                    static_cast<long long>(num_blocks) * block_size);
 }
 
 cudaError_t read_errors_kvwrite(uint32_t* out, bool clear) {

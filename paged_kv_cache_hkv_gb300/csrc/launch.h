@@ -61,6 +61,25 @@ inline cudaError_t smem_attr_once(Kernel kern, int bytes, std::atomic<unsigned l
   return e;
 }
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel in the stream is still running; it calls pdl_wait()
+// before reading that kernel's results.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Heads handled together by one decode warp, and head groups per kv head.
 inline int decode_heads_per_warp(int group) { return group < 4 ? group : 4; }
 

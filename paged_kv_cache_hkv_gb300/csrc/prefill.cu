@@ -407,6 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&kv_map);
     prefetch_tensormap(&q_map);
   }
+  if (warp == 8) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh.tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  pdl_trigger();
+  // barriers, tensor maps and TMEM above do not depend on the plan; its output does
+  pdl_wait();
   const int n_items = static_cast<int>(p.hdr[kHdrPrefillItems]);
   const int n_req = static_cast<int>(p.hdr[kHdrPrefillReqs]);
   int4* meta_s = reinterpret_cast<int4*>(gbase + Lay::kMeta);
@@ -424,13 +434,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the first work item is claimed while the CTA sets up
   int first_claim = 0;
   if (tid == 32 * 9) first_claim = static_cast<int>(atomicAdd(&p.hdr[kHdrPrefillNext], 1u));
-  if (warp == 8) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&sh.tmem)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -810,8 +813,8 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& k
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_attr_once(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(kv_map, q_map, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), static_cast<size_t>(smem), stream, kv_map,
+                    q_map, p);
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
