@@ -192,6 +192,22 @@ def test_prefill_mixed_shapes(Hq, Hkv, D):
     run_and_check(step)
 
 
+@pytest.mark.parametrize("n_prefill", [127, 128, 129, 300])
+def test_many_prefill_requests(n_prefill):
+    """More prefill requests than a CTA keeps in shared memory (128) take the
+    global-memory metadata path; thousands of small items cycle the CTAs'
+    item queues many times. Decodes are interleaved between them."""
+    rng = np.random.default_rng(n_prefill)
+    specs = []
+    for i in range(n_prefill):
+        specs.append(RequestSpec(int(rng.integers(0, 300)), int(rng.integers(2, 40))))
+        if i % 3 == 0:
+            specs.append(RequestSpec(int(rng.integers(0, 500)), 1))
+    step = make_step(specs, num_q_heads=16, num_kv_heads=4, head_dim=128, seed=n_prefill)
+    rows = rng.choice(step.num_tokens, size=min(step.num_tokens, 1500), replace=False)
+    run_and_check(step, rows=np.sort(rows))
+
+
 def test_prefill_chunks_match_one_shot_on_gpu():
     """A prompt split into chunks over three steps gives the rows of the
     one-shot prefill (each chunk attends the cached prefix plus itself)."""
