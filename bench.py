@@ -246,8 +246,8 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3}.get(
-        args.workload, 0)
+    seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3,
+                                                    "long_prefill": 6}.get(args.workload, 0)
     meta = synth.WORKLOADS[args.workload](seed=seed, materialize=False,
                                           block_size=args.block_size)
     shape = shape_of(meta)
@@ -295,6 +295,67 @@ def traffic_from_profile(kernel_src):
     return float(t.group(1))
 
 
+def run_e2e(ds, step, work, K, world, pg, sync_all):
+    """The step end to end through the public calls, as a serving loop runs
+    it: every step uploads all of its inputs (q, k, v, block table, lengths)
+    from pinned host memory and downloads its whole output. Two sets of
+    device buffers alternate between steps, and the uploads and downloads run
+    on their own streams, so step k+1's upload and step k-1's download
+    overlap step k's kernels. The cache pool is shared (the steps run in
+    order on one stream)."""
+    import torch
+
+    from paged_kv_cache_hkv_gb300.runner import DeviceStep
+
+    ds2 = DeviceStep(step, upload_pool=False)
+    ds2.kv_cache = ds.kv_cache
+    sets = [ds, ds2]
+    names = ("q", "k", "v", "block_table", "seq_lens", "query_start_loc", "num_computed")
+    host_in = [getattr(ds, n).cpu().pin_memory() for n in names]
+    host_out = [torch.empty(ds.out.shape, dtype=ds.out.dtype, pin_memory=True) for _ in sets]
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    compute = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    uploaded, computed, downloaded = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    sync_all()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(compute)
+    up.wait_event(e0)
+    down.wait_event(e0)
+    for k in range(K):
+        b = k % 2
+        cur = sets[b]
+        with torch.cuda.stream(up):  # inputs of step k, once step k-2 is done with the set
+            if k >= 2:
+                up.wait_event(computed[b])
+            for h, n in zip(host_in, names):
+                getattr(cur, n).copy_(h, non_blocking=True)
+            uploaded[b].record(up)
+        compute.wait_event(uploaded[b])
+        if k >= 2:  # the set's previous output has left the device
+            compute.wait_event(downloaded[b])
+        cur.run(stream=compute)
+        computed[b].record(compute)
+        with torch.cuda.stream(down):
+            down.wait_event(computed[b])
+            host_out[b].copy_(cur.out, non_blocking=True)
+            downloaded[b].record(down)
+    compute.wait_stream(up)
+    compute.wait_stream(down)
+    e1.record(compute)
+    sync_all()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, device="cuda")
+    # every step computes the same batch: the last download must equal the
+    # device-resident result
+    if not torch.equal(host_out[(K - 1) % 2], ds.out.cpu()):
+        raise SystemExit("end-to-end output differs from the device-resident step")
+    return {"value": whole_job_rate(work["tokens"], world, e2e_ms / K), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "overlap": "uploads and downloads on their own streams, two buffer sets"}
+
+
 def run_native(args):
     import torch
 
@@ -314,7 +375,8 @@ def run_native(args):
     base_seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3,
                                                          "tiny_decode": 1, "llama_decode": 2,
                                                          "prefix_sharing": 4,
-                                                         "long_context": 5}[args.workload]
+                                                         "long_context": 5,
+                                                         "long_prefill": 6}[args.workload]
     seed = replica_seed(base_seed, rank)
     step = synth.WORKLOADS[args.workload](seed=seed, block_size=args.block_size)
     ds = DeviceStep(step)
@@ -382,25 +444,7 @@ def run_native(args):
     # ---- end to end: host inputs in, host output out, every step
     e2e = None
     if not args.no_e2e:
-        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-        host_in = [(pin(t), t) for t in (ds.q, ds.k, ds.v, ds.block_table, ds.seq_lens,
-                                         ds.query_start_loc, ds.num_computed)]
-        host_out = torch.empty(ds.out.shape, dtype=ds.out.dtype, pin_memory=True)
-        h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
-        d2h = host_out.numel() * host_out.element_size()
-        sync_all()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(K):
-            for h, d in host_in:
-                d.copy_(h, non_blocking=True)
-            ds.run()
-            host_out.copy_(ds.out, non_blocking=True)
-        e1.record(stream)
-        sync_all()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, device="cuda")
-        e2e = {"value": whole_job_rate(work["tokens"], world, e2e_ms / K), "unit": UNIT,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        e2e = run_e2e(ds, step, work, K, world, pg, sync_all)
 
     # ---- roofline of the dominant kernel (decode)
     peaks = {}

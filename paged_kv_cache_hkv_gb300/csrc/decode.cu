@@ -675,17 +675,20 @@ constexpr int kDecodeWarps = PKV_DECODE_WARPS;    // warps per CTA
 // registers would fit a third: on the 1280-decode mixed
 // step (d = 128, 32 q / 8 kv heads) 2 CTAs of 4 warps per SM streamed at
 // 0.98 of the copy peak and 3 at 0.93 (shorter warp ranges, more partials).
-constexpr int kDecodeMaxCtasPerSm = 2;
+#ifndef PKV_DECODE_MAX_CTAS
+#define PKV_DECODE_MAX_CTAS 2
+#endif
+constexpr int kDecodeMaxCtasPerSm = PKV_DECODE_MAX_CTAS;
 
 template <int D, int GW>
 constexpr size_t decode_smem_bytes() {
-  // At least a third of an SM's shared memory (228 KB), so that no SM ever
-  // holds more than kDecodeMaxCtasPerSm CTAs -- also when the grid is
+  // More than 1 / (kDecodeMaxCtasPerSm + 1) of an SM's shared memory
+  // (228 KB), so that no SM ever holds more than kDecodeMaxCtasPerSm CTAs -- also when the grid is
   // launched early (programmatic dependent launch) and its first CTAs land
   // on the few SMs the previous kernel has already left.
   constexpr size_t used = sizeof(typename DecodeCfg<D, GW, kDecodeStages>::WarpSmem) * kDecodeWarps + 128;
-  constexpr size_t third = 228u * 1024u / 3u + 1024u;
-  return used > third ? used : third;
+  constexpr size_t share = 228u * 1024u / (kDecodeMaxCtasPerSm + 1) + 1024u;
+  return used > share ? used : share;
 }
 
 template <int D, int GW, int SH>

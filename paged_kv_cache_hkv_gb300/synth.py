@@ -363,6 +363,12 @@ def long_context(seed: int = 5, **kw) -> PagedStep:
     return make_step(_decodes(lengths), seed=seed, **LLAMA, **kw)
 
 
+def long_prefill(seed: int = 6, **kw) -> PagedStep:
+    """Prefill at scale: 4 prompt chunks of 2048 new tokens over 6144 cached
+    tokens each (keys up to 8192 per query), no decodes."""
+    return make_step([RequestSpec(6144, 2048) for _ in range(4)], seed=seed, **LLAMA, **kw)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama_decode": llama_decode,
@@ -370,4 +376,5 @@ WORKLOADS = {
     "prefill_rows": prefill_rows,
     "prefix_sharing": prefix_sharing,
     "long_context": long_context,
+    "long_prefill": long_prefill,
 }

@@ -68,6 +68,17 @@ def test_long_context_pool_written_exactly():
     assert np.array_equal(pool[blocks], expect)
 
 
+def test_long_prefill_sampled_rows():
+    """Chunks of 2048 new tokens over 6144 cached ones (keys up to 8192):
+    sampled rows from every chunk, both ends of each included."""
+    step = synth.long_prefill()
+    rng = np.random.default_rng(6)
+    rows = set(rng.choice(step.num_tokens, size=200, replace=False).tolist())
+    for r in range(step.num_reqs):
+        rows.update({int(step.query_start_loc[r]), int(step.query_start_loc[r + 1]) - 1})
+    run_and_check(step, rows=sorted(rows), check_pool=False)
+
+
 def test_mixed_step_parity():
     step = synth.mixed_step()
     run_and_check(step)
