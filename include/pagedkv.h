@@ -29,6 +29,13 @@
  *   last-block waste vs fewer block-table entries); other sizes return
  *   PKV_ERR_UNSUPPORTED. num_blocks * 2 * B must stay below 2^31.
  *   head_dim must be 64 or 128.
+ *
+ * Launches: every kernel is launched with programmatic stream serialization.
+ * A kernel may start (set up barriers, allocate tensor memory) while the
+ * previous kernel in the stream is still running, and it waits for that
+ * kernel to complete -- and its writes to be visible -- before reading
+ * anything. Work the caller queued earlier on the stream is therefore seen
+ * as with plain stream order. The calls can be recorded into a CUDA graph.
  */
 #ifndef PAGEDKV_H_
 #define PAGEDKV_H_
@@ -87,7 +94,8 @@ typedef struct pkv_attention_options {
    * [0] before the plan kernel, [1] before the prefill kernel, [2] before
    * the decode kernel, [3] before the combine kernel, [4] after it.
    * Consecutive pairs bracket one kernel each (an empty bracket when a
-   * kernel is not needed). */
+   * kernel is not needed). The events keep the kernels from overlapping
+   * (see "Launches" above), so a traced call can be a little slower. */
   void** trace_events;
 } pkv_attention_options;
 

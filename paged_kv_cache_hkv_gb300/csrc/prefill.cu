@@ -12,22 +12,21 @@
 // tile are the G = Hq/Hkv q heads of one kv head for 128/G consecutive
 // queries, so every K/V tile feeds all G heads (GQA). The item's key tiles
 // (128 keys = 8 chunks of 16 keys: 8 blocks of 16 tokens, 4 of 32 or 16 of
-// 8) are split between two softmax warpgroups:
-// warpgroup w takes tiles w, w+2, ... with its own accumulators
-// (TMEM columns [256w, 256w+128) for S, [256w+128, 256w+128+D) for O).
-// Two copy warps stream K and V tiles through a 2-stage ring by TMA (128-byte
-// swizzle, one 16-key chunk of one kv head per copy, two copies of 8 rows
-// for 8-token blocks) and one MMA thread issues
+// 8) are split between two softmax warpgroups: warpgroup w takes tiles w,
+// w+2, ... with its own accumulators (TMEM columns [256w, 256w+128) for S,
+// [256w+128, 256w+128+D) for O) and its own running max and sum.
 //   S_w = Q K^T      tcgen05.mma M=128 N=128, A = Q (smem), B = K (smem)
-//   O_w += P_w V     tcgen05.mma M=128 N=D, A = P_w (smem), B = V (smem)
-// while the warpgroups run the softmax: each thread owns one row, reads S
-// with tcgen05.ld, applies the causal mask, keeps a base-2 running max
-// (rescaling O in TMEM only when it grows by more than 2^8) and sum, and
-// writes P as bf16 into its warpgroup's smem buffer. One warpgroup's softmax
-// runs while the tensor core works on the other's tiles; each warpgroup's
-// next K/V tile streams in by TMA while the other one computes. At the end the two
-// partial (max, sum, O) are merged and each warpgroup writes half of the
-// output columns.
+//   O_w += P_w V     tcgen05.mma M=128 N=D, A = P_w (TMEM), B = V (smem)
+// Each softmax thread owns one row: it reads S with tcgen05.ld, applies the
+// causal mask, keeps a base-2 running max (rescaling O in TMEM only when it
+// grows by more than 2^8) and sum, and writes P as bf16 pairs over S_w's
+// columns with tcgen05.st. A K-copy warp (3-slot ring) and a V-copy warp
+// (2-slot ring) stream the tiles by TMA (128-byte swizzle, one 16-key chunk
+// of one kv head per copy, two copies of 8 rows for 8-token blocks); one
+// thread issues every MMA. At the end of an item the two partial (max, sum,
+// O) are merged and each warpgroup writes half of the output columns. The
+// CTAs are persistent and take items from a counter; the roles meet only at
+// mbarriers, so consecutive items overlap.
 //
 // Every wait is bounded; on a timeout the kernel records
 // PKV_DEVERR_TIMEOUT, drains its copies, frees TMEM and returns.
