@@ -247,6 +247,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3,
+                                                    "mixed_step_2048": 3,
                                                     "long_prefill": 6}.get(args.workload, 0)
     meta = synth.WORKLOADS[args.workload](seed=seed, materialize=False,
                                           block_size=args.block_size)
@@ -373,6 +374,7 @@ def run_native(args):
         pg = dist
 
     base_seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3,
+                                                         "mixed_step_2048": 3,
                                                          "tiny_decode": 1, "llama_decode": 2,
                                                          "prefix_sharing": 4,
                                                          "long_context": 5,
@@ -414,14 +416,21 @@ def run_native(args):
     KT = min(K, 100)
     trace = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.PKV_TRACE_EVENTS)]
              for _ in range(KT)]
+    write_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(KT)]
     for ev in trace:  # torch creates the CUDA event on its first record
         for e in ev:
             e.record(stream)
+    for a, b in write_ev:
+        a.record(stream)
+        b.record(stream)
     sync_all()
     s = ds.step
     for k in range(KT):
         ds.slot_map()
+        write_ev[k][0].record(stream)
         ds.write()
+        write_ev[k][1].record(stream)
         binding.pkv_paged_attention(
             ds.out, ds.q, ds.kv_cache, ds.block_table, ds.seq_lens, ds.query_start_loc,
             ds.num_computed, max_query_len=s.max_query_len, max_seq_len=s.max_seq_len,
@@ -434,6 +443,7 @@ def run_native(args):
         for i in range(binding.PKV_TRACE_EVENTS - 1):
             per_kernel[i] += ev[i].elapsed_time(ev[i + 1])
     per_kernel /= KT  # ms per launch: plan, prefill, decode, combine
+    write_ms = float(np.mean([a.elapsed_time(b) for a, b in write_ev]))
     total_ms = max_over_ranks(total_ms, pg, device="cuda")
     ms_per_step = total_ms / K
     value = whole_job_rate(work["tokens"], world, ms_per_step)
@@ -493,6 +503,12 @@ def run_native(args):
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "block_tradeoff": block_tradeoff(step),
         "decode_kv_read_gbs": dec_gbs,
+        # the same bytes over decode + combine time (both kernels of split-KV)
+        "decode_combine_kv_read_gbs": (work["decode_kv_bytes"] / ((per_kernel[2] + per_kernel[3]) * 1e-3)
+                                       / 1e9 if per_kernel[2] > 0 else None),
+        # cache write: each new token's K and V rows read and written
+        "kv_write": {"us": write_ms * 1e3,
+                     "gbs": work["write_bytes"] / (write_ms * 1e-3) / 1e9 if write_ms > 0 else None},
         "kernel_ms": {"plan": per_kernel[0], "prefill": per_kernel[1],
                       "decode": per_kernel[2], "combine": per_kernel[3]},
         "roofline": roofline,

@@ -334,6 +334,15 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   const int virt = layout.num_kv_heads * (group / gw);
   const WsLayout wl = ws_layout(num_reqs, virt, gw, layout.head_dim, warps);
   if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
+  // The decode stream holds at most num_reqs * ceil(max_seq_len / 16) * virt
+  // chunk-heads: with the default split, never use more warps than that (a
+  // small batch then launches a few CTAs instead of a full wave). The
+  // workspace sized for the full wave still fits.
+  if (!(options && options->decode_warps > 0)) {
+    const long long bound = static_cast<long long>(num_reqs) *
+                            ((static_cast<long long>(max_seq_len) + 15) / 16) * virt;
+    if (bound < warps) warps = bound > 0 ? bound : 1;
+  }
 
   char* wsb = static_cast<char*>(workspace);
   pkv::AttnWorkspace ws;

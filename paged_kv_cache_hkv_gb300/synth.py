@@ -341,6 +341,12 @@ def mixed_step(seed: int = 3, num_decodes: int = 1280, **kw) -> PagedStep:
     return make_step(mixed_step_specs(seed, num_decodes), seed=seed, **LLAMA, **kw)
 
 
+def mixed_step_2048(seed: int = 3, **kw) -> PagedStep:
+    """The mixed step under its 2048-token-budget reading: the same chunk and
+    prefills with 1024 decodes instead of 1280."""
+    return mixed_step(seed, num_decodes=1024, **kw)
+
+
 def prefill_rows(seed: int = 3, **kw) -> PagedStep:
     """The mixed step's prefill requests alone: the 512-token chunk over 1536
     cached tokens and the 8 fresh 64-token prefills."""
@@ -373,6 +379,7 @@ WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama_decode": llama_decode,
     "mixed_step": mixed_step,
+    "mixed_step_2048": mixed_step_2048,
     "prefill_rows": prefill_rows,
     "prefix_sharing": prefix_sharing,
     "long_context": long_context,
