@@ -85,8 +85,10 @@ typedef struct pkv_cache_layout {
  * defaults. */
 typedef struct pkv_attention_options {
   /* Decode warps that split the step's decode KV stream between them
-   * (split-KV). 0 = one full wave of the device. A single warp means no
-   * split at all; tests use other values to vary the partitioning. */
+   * (split-KV). 0 = one full wave of the device, or fewer when the hints
+   * bound the stream below that (num_reqs * ceil(max_seq_len / 16) * head
+   * groups). A single warp means no split at all; tests use other values to
+   * vary the partitioning. */
   int32_t decode_warps;
   int32_t reserved[7]; /* must be zero */
   /* Tracing: NULL, or PKV_TRACE_EVENTS cudaEvent_t handles (as void*) owned
