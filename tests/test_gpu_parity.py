@@ -403,3 +403,36 @@ def test_mixed_step_replays_in_a_cuda_graph():
         torch.cuda.synchronize()
         assert np.array_equal(ds.out_host(), eager)
     assert binding.pkv_get_device_errors(clear=True) == 0
+
+
+# ---------------------------------------------------------------- seeded fuzz
+FUZZ_SHAPES = [(4, 4, 64), (8, 4, 64), (16, 4, 64), (32, 4, 64), (8, 8, 128), (16, 8, 128),
+               (32, 8, 128), (64, 8, 128), (8, 2, 128), (4, 1, 128), (16, 2, 64), (12, 3, 128)]
+
+
+@pytest.mark.parametrize("trial", range(24))
+def test_seeded_fuzz(trial):
+    """Random shapes, block sizes, request mixes (decodes, fresh prefills,
+    chunks over a cached prefix, empty requests) and split-KV warp counts;
+    the slots, the whole pool and sampled rows are checked."""
+    rng = np.random.default_rng(9000 + trial)
+    Hq, Hkv, D = FUZZ_SHAPES[trial % len(FUZZ_SHAPES)]
+    B = int(rng.choice([8, 16, 32]))
+    specs = []
+    for _ in range(int(rng.integers(1, 40))):
+        kind = rng.choice(["decode", "decode", "prefill", "chunk", "empty"])
+        if kind == "decode":
+            specs.append(RequestSpec(int(rng.integers(0, 2000)), 1))
+        elif kind == "prefill":
+            specs.append(RequestSpec(0, int(rng.integers(2, 300))))
+        elif kind == "chunk":
+            specs.append(RequestSpec(int(rng.integers(1, 1500)), int(rng.integers(2, 400))))
+        else:
+            specs.append(RequestSpec(int(rng.integers(0, 500)), 0))
+    if all(s.query_len == 0 for s in specs):
+        specs.append(RequestSpec(10, 1))
+    step = make_step(specs, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=B,
+                     seed=trial)
+    warps = None if trial % 3 == 0 else int(rng.integers(1, 3000))
+    rows = rng.choice(step.num_tokens, size=min(step.num_tokens, 400), replace=False)
+    run_and_check(step, decode_warps=warps, rows=np.sort(rows))
