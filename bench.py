@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--seed", type=int, default=None)
     p.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32],
                    help="tokens per cache block")
+    p.add_argument("--graph", action="store_true",
+                   help="time the step as a CUDA graph captured once and replayed")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -84,6 +86,9 @@ def whole_job_rate(units_per_rank, world, max_ms_per_step):
 
 
 # ------------------------------------------------------------------ work
+L2_BYTES = 129 * 2 ** 20  # GB300 L2
+
+
 def step_work(step):
     """Algorithmic bytes and flops of one step.
 
@@ -100,6 +105,10 @@ def step_work(step):
         pairs += n * c + n * (n + 1) // 2
     return {
         "decode_kv_bytes": decode_kv,
+        # bytes a step touches at least once: the K/V of every allocated block
+        # slot (a shared prefix once), q and out rows
+        "touched_bytes": (block_tradeoff(step)["slots_allocated"] * Hkv * D * 2 * 2
+                          + 2 * step.num_tokens * Hq * D * 2),
         "decode_rows": int(dec.sum()),
         "prefill_pairs": pairs,
         "prefill_flops": 4 * D * Hq * pairs,
@@ -405,10 +414,22 @@ def run_native(args):
     sampler.start()
     time.sleep(0.15)
     # the step as a user runs it: nothing between the kernels, so each one may
-    # start its prologue while the one before finishes
+    # start its prologue while the one before finishes (or, with --graph, the
+    # three calls captured once into a CUDA graph and replayed)
+    run_step = ds.run
+    if args.graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            ds.run()
+        stream.wait_stream(side)
+        graph.replay()
+        run_step = graph.replay
+    sync_all()
     t_start.record(stream)
     for k in range(K):
-        ds.run()
+        run_step()
     t_stop.record(stream)
     sync_all()
     # per-kernel times from a separate run with events recorded between the
@@ -500,7 +521,10 @@ def run_native(args):
                    "block_size": step.block_size, "pool_blocks": step.num_blocks,
                    "decode_kv_bytes_per_step": work["decode_kv_bytes"],
                    "prefill_flops_per_step": work["prefill_flops"],
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+                   "l2": ("inputs larger than L2 (no flush)" if work["touched_bytes"] > L2_BYTES
+                          else "inputs fit in L2 (no flush: L2-warm timings)"),
+                   "parallelism": f"replicas x{world}",
+                   "launch": "cuda graph replay" if args.graph else "direct, programmatic dependent launch"},
         "block_tradeoff": block_tradeoff(step),
         "decode_kv_read_gbs": dec_gbs,
         # the same bytes over decode + combine time (both kernels of split-KV)
