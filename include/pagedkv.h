@@ -84,12 +84,12 @@ typedef struct pkv_cache_layout {
 /* Optional tuning and tracing of pkv_paged_attention; pass NULL for the
  * defaults. */
 typedef struct pkv_attention_options {
-  /* Decode warps that split the step's decode KV stream between them
-   * (split-KV). 0 = one full wave of the device, or fewer when the hints
-   * bound the stream below that (num_reqs * ceil(max_seq_len / 16) * head
-   * groups). A single warp means no split at all; tests use other values to
-   * vary the partitioning. */
-  int32_t decode_warps;
+  /* Ranges the step's decode KV stream of (request, 16-key chunk) positions
+   * is cut into, one CTA each (split-KV). 0 = one full wave of the device,
+   * or fewer when the hints bound the stream below that (num_reqs *
+   * ceil(max_seq_len / 16)). A single range means no split at all; tests use
+   * other values to vary the partitioning. */
+  int32_t decode_splits;
   int32_t reserved[7]; /* must be zero */
   /* Tracing: NULL, or PKV_TRACE_EVENTS cudaEvent_t handles (as void*) owned
    * by the caller. The call records them on `stream` around its kernels:

@@ -37,7 +37,7 @@ PKV_TRACE_EVENTS = 5
 
 
 class pkv_attention_options(ctypes.Structure):
-    _fields_ = [("decode_warps", c_i32), ("reserved", c_i32 * 7),
+    _fields_ = [("decode_splits", c_i32), ("reserved", c_i32 * 7),
                 ("trace_events", ctypes.POINTER(c_void_p))]
 
 
@@ -182,11 +182,11 @@ def pkv_copy_blocks(dst_pool, src_pool, block_pairs, stream=None):
         _ptr(block_pairs), block_pairs.shape[0], lay, _stream(stream)))
 
 
-def _options(decode_warps, trace_events=None):
-    if decode_warps is None and trace_events is None:
+def _options(decode_splits, trace_events=None):
+    if decode_splits is None and trace_events is None:
         return None
     o = pkv_attention_options()
-    o.decode_warps = int(decode_warps or 0)
+    o.decode_splits = int(decode_splits or 0)
     if trace_events is not None:
         if len(trace_events) != PKV_TRACE_EVENTS:
             raise ValueError(f"trace_events needs {PKV_TRACE_EVENTS} torch.cuda.Event")
@@ -200,11 +200,11 @@ def _options(decode_warps, trace_events=None):
 
 
 def pkv_attention_workspace_size(num_reqs: int, num_q_heads: int, kv_cache,
-                                 decode_warps=None) -> int:
+                                 decode_splits=None) -> int:
     """Workspace bytes for pkv_paged_attention; kv_cache is the pool tensor
     or a pkv_cache_layout."""
     lay = kv_cache if isinstance(kv_cache, pkv_cache_layout) else layout_of(kv_cache)
-    n = load().pkv_attention_workspace_size(num_reqs, num_q_heads, lay, _options(decode_warps))
+    n = load().pkv_attention_workspace_size(num_reqs, num_q_heads, lay, _options(decode_splits))
     if n < 0:
         raise PagedKVError("pkv_attention_workspace_size", int(n))
     return int(n)
@@ -212,7 +212,7 @@ def pkv_attention_workspace_size(num_reqs: int, num_q_heads: int, kv_cache,
 
 def pkv_paged_attention(out, q, kv_cache, block_table, seq_lens, query_start_loc,
                         num_computed_tokens, *, max_query_len: int, max_seq_len: int,
-                        scale: float, workspace, decode_warps=None, trace_events=None,
+                        scale: float, workspace, decode_splits=None, trace_events=None,
                         stream=None):
     """out [T, Hq, D] bf16 <- attention of one mixed step (see pagedkv.h).
 
@@ -234,7 +234,7 @@ def pkv_paged_attention(out, q, kv_cache, block_table, seq_lens, query_start_loc
         block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), _ptr(num_computed_tokens),
         seq_lens.shape[0], q.shape[0], int(max_query_len), int(max_seq_len), q.shape[1],
         float(scale), lay, _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _options(decode_warps, trace_events), _stream(stream)))
+        _options(decode_splits, trace_events), _stream(stream)))
     return out
 
 
@@ -249,7 +249,7 @@ def pkv_get_device_errors(clear: bool = True, stream=None) -> int:
 def pkv_paged_attention_static_workspace(out, q, kv_cache, block_table, seq_lens,
                                          query_start_loc, num_computed_tokens, *,
                                          max_query_len: int, max_seq_len: int, scale: float,
-                                         decode_warps=None, stream=None):
+                                         decode_splits=None, stream=None):
     """pkv_paged_attention without a caller workspace: for callers that cannot
     allocate device memory, the library uses its built-in scratch array (see
     pagedkv.h for the size limit and the one-stream rule)."""
@@ -267,5 +267,5 @@ def pkv_paged_attention_static_workspace(out, q, kv_cache, block_table, seq_lens
         _ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), _ptr(num_computed_tokens),
         seq_lens.shape[0], q.shape[0], int(max_query_len), int(max_seq_len), q.shape[1],
-        float(scale), layout_of(kv_cache), _options(decode_warps), _stream(stream)))
+        float(scale), layout_of(kv_cache), _options(decode_splits), _stream(stream)))
     return out

@@ -5,6 +5,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "../../include/pagedkv.h"
@@ -24,7 +25,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct DeviceInfo {
   int num_sms = 0;
   bool ok = false;
-  int full_wave_warps[2][3][3] = {};  // [D==128][log2 heads per warp][log2 B - 3]
+  std::map<long long, long long> full_wave_splits;  // by (D, group, B, kv heads)
 };
 
 constexpr int kMaxDevices = 64;
@@ -121,9 +122,9 @@ struct WsLayout {
   size_t hdr, dec_prefix, pf_req, pf_prefix, part_ml, part_o, bound, total;
 };
 
-WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long warps) {
+WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long splits) {
   WsLayout w;
-  const long long slots = pkv::decode_partial_slots(num_reqs, virt_heads, warps);
+  const long long slots = pkv::decode_partial_slots(num_reqs, virt_heads, splits);
   size_t off = 0;
   w.hdr = off;
   off += round256(pkv::kHdrWords * sizeof(uint32_t));
@@ -138,35 +139,37 @@ WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long
   w.part_o = off;
   off += round256(static_cast<size_t>(slots) * gw * head_dim * sizeof(float));
   w.bound = off;
-  off += round256(static_cast<size_t>(warps) * sizeof(int2));
+  off += round256(static_cast<size_t>(splits) * sizeof(int));
   w.total = off;
   return w;
 }
 
-int32_t decode_warps_for(DeviceInfo* d, int head_dim, int group, int block_size,
-                         const pkv_attention_options* opt, long long* warps) {
+// Ranges (CTAs) the decode stream is split into: the caller's choice, else
+// one full wave of the device for the shape (cached per device).
+int32_t decode_splits_for(DeviceInfo* d, int head_dim, int num_kv_heads, int group,
+                          int block_size, const pkv_attention_options* opt, long long* splits) {
   if (opt) {
     for (int i = 0; i < 7; ++i)
       if (opt->reserved[i] != 0) return PKV_ERR_BAD_SHAPE;
-    if (opt->decode_warps < 0) return PKV_ERR_BAD_SHAPE;
-    if (opt->decode_warps > 0) {
-      *warps = opt->decode_warps;
+    if (opt->decode_splits < 0) return PKV_ERR_BAD_SHAPE;
+    if (opt->decode_splits > 0) {
+      *splits = opt->decode_splits;
       return PKV_OK;
     }
   }
-  const int di = head_dim == 128 ? 1 : 0;
-  const int gw = pkv::decode_heads_per_warp(group);
-  const int gi = gw == 4 ? 2 : (gw == 2 ? 1 : 0);
-  std::lock_guard<std::mutex> lock(g_mu);
   const int sh = block_shift_of(block_size);
-  int& cached = d->full_wave_warps[di][gi][sh - 3];
-  if (cached == 0) {
-    int w = 0;
-    cudaError_t e = pkv::decode_full_wave_warps(head_dim, group, sh, d->num_sms, &w);
+  const long long key = ((static_cast<long long>(head_dim) * 16 + group) * 8 + sh) * 65536 +
+                        num_kv_heads;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = d->full_wave_splits.find(key);
+  if (it == d->full_wave_splits.end()) {
+    long long c = 0;
+    cudaError_t e =
+        pkv::decode_full_wave_splits(head_dim, num_kv_heads, group, sh, d->num_sms, &c);
     if (e != cudaSuccess) return cuda_fail(e, "decode occupancy");
-    cached = w;
+    it = d->full_wave_splits.emplace(key, c).first;
   }
-  *warps = cached;
+  *splits = it->second;
   return PKV_OK;
 }
 
@@ -285,12 +288,13 @@ int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
   st = device_info(&d);
   if (st != PKV_OK) return st;
   const int group = num_q_heads / layout.num_kv_heads;
-  long long warps = 0;
-  st = decode_warps_for(d, layout.head_dim, group, layout.block_size, options, &warps);
+  long long splits = 0;
+  st = decode_splits_for(d, layout.head_dim, layout.num_kv_heads, group, layout.block_size,
+                         options, &splits);
   if (st != PKV_OK) return st;
   const int gw = pkv::decode_heads_per_warp(group);
   const int virt = layout.num_kv_heads * (group / gw);
-  return static_cast<int64_t>(ws_layout(num_reqs, virt, gw, layout.head_dim, warps).total);
+  return static_cast<int64_t>(ws_layout(num_reqs, virt, gw, layout.head_dim, splits).total);
 }
 
 int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, const void* kv_cache,
@@ -327,21 +331,22 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   st = device_info(&d);
   if (st != PKV_OK) return st;
   const int group = num_q_heads / layout.num_kv_heads;
-  long long warps = 0;
-  st = decode_warps_for(d, layout.head_dim, group, layout.block_size, options, &warps);
+  long long splits = 0;
+  st = decode_splits_for(d, layout.head_dim, layout.num_kv_heads, group, layout.block_size,
+                         options, &splits);
   if (st != PKV_OK) return st;
   const int gw = pkv::decode_heads_per_warp(group);
   const int virt = layout.num_kv_heads * (group / gw);
-  const WsLayout wl = ws_layout(num_reqs, virt, gw, layout.head_dim, warps);
+  const WsLayout wl = ws_layout(num_reqs, virt, gw, layout.head_dim, splits);
   if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
-  // The decode stream holds at most num_reqs * ceil(max_seq_len / 16) * virt
-  // chunk-heads: with the default split, never use more warps than that (a
-  // small batch then launches a few CTAs instead of a full wave). The
-  // workspace sized for the full wave still fits.
-  if (!(options && options->decode_warps > 0)) {
-    const long long bound = static_cast<long long>(num_reqs) *
-                            ((static_cast<long long>(max_seq_len) + 15) / 16) * virt;
-    if (bound < warps) warps = bound > 0 ? bound : 1;
+  // The decode stream holds at most num_reqs * ceil(max_seq_len / 16)
+  // chunks: with the default split, never use more ranges than that (a small
+  // batch then launches a few CTAs instead of a full wave). The workspace
+  // sized for the full wave still fits.
+  if (!(options && options->decode_splits > 0)) {
+    const long long bound =
+        static_cast<long long>(num_reqs) * ((static_cast<long long>(max_seq_len) + 15) / 16);
+    if (bound < splits) splits = bound > 0 ? bound : 1;
   }
 
   char* wsb = static_cast<char*>(workspace);
@@ -352,7 +357,7 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   ws.pf_prefix = reinterpret_cast<int32_t*>(wsb + wl.pf_prefix);
   ws.part_ml = reinterpret_cast<float2*>(wsb + wl.part_ml);
   ws.part_o = reinterpret_cast<float*>(wsb + wl.part_o);
-  ws.bound = reinterpret_cast<int2*>(wsb + wl.bound);
+  ws.bound = reinterpret_cast<int*>(wsb + wl.bound);
 
   pkv::AttnArgs a;
   a.out = static_cast<uint16_t*>(out);
@@ -378,15 +383,17 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   const int D = layout.head_dim, Hkv = layout.num_kv_heads;
   const uint64_t row_bytes = static_cast<uint64_t>(Hkv) * D * 2;
   // pool as rows of one kv head: {d, kv head, (block*2 + k|v)*B + offset}.
-  // A decode copy is a block's 32 K and V rows (B = 16), 16 rows (half of the
-  // K or V rows of a 32-token block) or the 16 K and V rows of an 8-token
-  // block.
+  // A decode copy covers the kv heads of one CTA slab and a block's 32 K and
+  // V rows (B = 16), 16 rows (half of the K or V rows of a 32-token block)
+  // or the 16 K and V rows of an 8-token block.
   const int B = layout.block_size;
   const uint64_t pool_rows = static_cast<uint64_t>(layout.num_blocks) * 2 * B;
   const uint32_t dec_box = B == 16 ? 32u : 16u;
+  int slab_vh = 0, slab_kh = 0;
+  pkv::decode_slab(Hkv, group, &slab_vh, &slab_kh);
   CUtensorMap kv_map;
   st = make_map(&kv_map, kv_cache, D, Hkv, pool_rows, static_cast<uint64_t>(D) * 2, row_bytes, D,
-                1, dec_box, CU_TENSOR_MAP_SWIZZLE_NONE);
+                static_cast<uint32_t>(slab_kh), dec_box, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != PKV_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -414,7 +421,7 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   e = mark(2);
-  if (e == cudaSuccess) e = pkv::launch_decode(a, ws, kv_map, static_cast<int>(warps), s, ev);
+  if (e == cudaSuccess) e = pkv::launch_decode(a, ws, kv_map, splits, d->num_sms, s, ev);
   if (e == cudaSuccess) e = mark(4);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;

@@ -142,6 +142,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, AttnWorkspace ws
 }
 
 // ------------------------------------------------------------------ decode
+// Work split: the decode stream of the step is the sequence of (request,
+// 16-key chunk) positions; CTA c of C takes [c*N/C, (c+1)*N/C). A CTA holds
+// one consumer warp per virtual head (GW q heads of one kv head) of its head
+// slab -- up to 8 virtual heads, so 9 warps with the producer -- and each
+// chunk's K and V rows of every kv head of the slab arrive in one TMA copy
+// (one {D, KH, 32} box for 16-token blocks: 32 pool rows of KH*D*2
+// contiguous bytes), which streams DRAM far better than one 256-byte row
+// per kv head. A request cut by a range boundary leaves one partial per
+// CTA that touched it, in slot (request + c) * V + virtual head; the
+// combine kernel merges them.
 struct DecodeParams {
   const uint16_t* q;
   long long q_stride;
@@ -152,45 +162,60 @@ struct DecodeParams {
   const int32_t* qsl;
   int num_reqs, num_q_heads, num_blocks;
   int head_groups;  // q-head groups of GW per kv head
-  int virt_heads;   // num_kv_heads * head_groups
-  long long warps;  // W
+  int virt_heads;   // V = num_kv_heads * head_groups
+  int slab_vh;      // virtual heads per CTA slab (<= 8); slab s = virtual heads [s*slab_vh, ...)
+  int slab_kh;      // kv heads per slab = slab_vh / head_groups
+  long long splits; // C: CTAs along the stream (the grid is C x slabs)
+  int stages;       // depth of the shared-memory ring of K/V chunks (>= 2)
   float scale_log2;
   const int32_t* dec_prefix;
   const uint32_t* hdr;
   float2* part_ml;
   float* part_o;
-  int2* bound;  // [W]: (request, virtual head) holding the first position of each warp's range
+  int* bound;  // [C]: request holding the first position of CTA c's range (-1: none)
 };
 
-// Warp that owns position x of the decode stream: ranges start at
-// floor(w * N / W).
-__device__ __forceinline__ long long owner_warp(long long x, long long N, long long W) {
-  return ((x + 1) * W + N - 1) / N - 1;
+// CTA that owns position x of the decode stream: ranges start at floor(c * N / C).
+__device__ __forceinline__ long long owner_cta(long long x, long long N, long long C) {
+  return ((x + 1) * C + N - 1) / N - 1;
 }
 
-template <int D, int GW, int S>
+template <int D, int GW>
 struct DecodeCfg {
   static constexpr int LPK = D / 8;     // lanes per key row (8 bf16 per lane)
   static constexpr int KPI = 32 / LPK;  // keys per warp instruction ("sub-groups")
-  static constexpr int KPL = 16 / KPI;  // keys per lane per block
-  static constexpr int NV = GW * KPL;   // partial scores per lane per block
+  static constexpr int KPL = 16 / KPI;  // keys per lane per chunk
+  static constexpr int NV = GW * KPL;   // partial scores per lane per chunk
   static constexpr int NPL = NV >= LPK ? NV / LPK : 1;  // full scores per lane
   static constexpr int DUP = NV >= LPK ? 1 : LPK / NV;  // lanes holding the same score
   static constexpr int LPH = LPK / GW;                  // lanes per head in a sub-group
-  static constexpr uint32_t kKvBytes = 32u * D * 2u;  // K and V rows of one chunk
-  static constexpr uint32_t kQBytes = GW * D * 2u;
-  static_assert(KPL * KPI == 16, "block of 16 keys");
+  static_assert(KPL * KPI == 16, "chunk of 16 keys");
   static_assert(KPL % NPL == 0, "a lane's scores stay in one head");
 
-  struct alignas(128) WarpSmem {
-    uint16_t kv[S][32][D];  // K and V rows of one kv head and chunk (see k_row, v_row)
-    uint16_t q[S][GW * D];
-    int4 meta0[S];  // r, virtual head, block, flags
-    int4 meta1[S];  // valid keys, token row, output slot (-1 = final)
-    uint64_t full[S];
-    alignas(16) float p[KPI][NV];
+  struct alignas(16) WarpScratch {
+    float p[KPI][NV];
     float2 hs[GW];
   };
+};
+
+// Shared memory of a decode CTA (bytes from a 128-aligned base), the same on
+// host and device: S stages of [32 rows][KH kv heads][D] K/V then the slab's
+// q rows [VH * GW][D]; per-stage metadata; full / empty barriers; per-warp
+// scratch.
+template <int D, int GW>
+struct DecodeLayout {
+  uint32_t kv_bytes, row_bytes, stage_bytes, meta_off, bar_off, scratch_off, total;
+  __host__ __device__ DecodeLayout(int kh, int vh, int S) {
+    row_bytes = static_cast<uint32_t>(kh) * D * 2u;
+    kv_bytes = 32u * row_bytes;
+    const uint32_t q_bytes = static_cast<uint32_t>(vh) * GW * D * 2u;
+    stage_bytes = (kv_bytes + q_bytes + 127u) & ~127u;
+    meta_off = S * stage_bytes;
+    bar_off = meta_off + S * 16u;
+    scratch_off = (bar_off + 2u * S * 8u + 127u) & ~127u;
+    total = scratch_off + static_cast<uint32_t>(vh) *
+                              static_cast<uint32_t>(sizeof(typename DecodeCfg<D, GW>::WarpScratch));
+  }
 };
 
 enum : int { kFirst = 1, kLast = 2, kInvalid = 4, kEnd = 8 };
@@ -229,146 +254,161 @@ struct ReduceScatter {
   }
 };
 
-// The running max of a head is only moved (and o, l rescaled) when a block's
+// The running max of a head is only moved (and o, l rescaled) when a chunk's
 // max exceeds it by more than this many powers of two; in between, p may
 // reach 2^8, far inside fp32 range. The result is the same softmax.
 constexpr float kRescaleLog2 = 8.f;
 
-template <int D, int GW, int S, int WARPS, int SH>
-__global__ void __launch_bounds__(WARPS * 32)
+constexpr int kDecodeMaxSlab = 8;                        // virtual heads per CTA at most
+constexpr int kDecodeThreads = (kDecodeMaxSlab + 1) * 32;  // + the producer warp
+
+template <int D, int GW, int SH>
+__global__ void __launch_bounds__(kDecodeThreads)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
-  using C = DecodeCfg<D, GW, S>;
-  using Smem = typename C::WarpSmem;
+  using C = DecodeCfg<D, GW>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // dynamic shared memory is only guaranteed 16-byte aligned: round up
-  unsigned char* smem_base = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-  Smem& sm = reinterpret_cast<Smem*>(smem_base)[warp];
-  const int sub = lane / C::LPK, li = lane % C::LPK;
-  // no early trigger here: the combine kernel's CTAs, resident next to these
-  // for the whole decode while they wait for it, slow the decode warps down
+  unsigned char* base = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  const int VH = p.slab_vh, KH = p.slab_kh;
+  const uint32_t S = static_cast<uint32_t>(p.stages);
+  const DecodeLayout<D, GW> lay(KH, VH, p.stages);
+  int4* meta = reinterpret_cast<int4*>(base + lay.meta_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + lay.bar_off);
+  uint64_t* empty = full + S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // no early trigger here: a next kernel's CTAs, resident next to these for
+  // the whole decode while they wait for it, slow the decode warps down
   pdl_wait();
 
-  const long long W = p.warps;
-  const long long w = static_cast<long long>(blockIdx.x) * WARPS + warp;
-  if (w >= W) return;
-  const long long N = static_cast<long long>(p.virt_heads) * p.hdr[kHdrDecodeBlocks];
-  const long long x0 = w * N / W, x1 = (w + 1) * N / W;
+  const long long Cn = p.splits, c = blockIdx.x;
+  const int slab = blockIdx.y;
+  const long long N = p.hdr[kHdrDecodeBlocks];
+  const long long x0 = c * N / Cn, x1 = (c + 1) * N / Cn;
 
-  // ---------------- locate position x0: (request r, virtual head vg, block)
-  int r = -1, vg = 0, blk = 0, nblk = 0, L = 0, t = 0, out_slot = -1;
+  // ---------------- locate position x0: (request r, chunk blk)
+  int r = -1, blk = 0, nblk = 0;
   if (x0 < N) {
-    const long long u = x0 / p.virt_heads;
-    r = upper_index(p.dec_prefix, p.num_reqs, u);
+    r = upper_index(p.dec_prefix, p.num_reqs, x0);
     const int pr = __ldg(p.dec_prefix + r);
     nblk = __ldg(p.dec_prefix + r + 1) - pr;
-    const long long rem = x0 - static_cast<long long>(p.virt_heads) * pr;
-    vg = static_cast<int>(rem / nblk);
-    blk = static_cast<int>(rem - static_cast<long long>(vg) * nblk);
+    blk = static_cast<int>(x0 - pr);
   }
-  // the combine kernel finds split pairs from these records (warps with an
-  // empty range record the pair that holds their start too)
-  if (lane == 0) p.bound[w] = make_int2(r, vg);
+  // the combine kernel finds split requests from these records (CTAs with an
+  // empty range record the request that holds their start too)
+  if (threadIdx.x == 0 && slab == 0) p.bound[c] = r;
   if (x0 >= x1) return;
-
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < S; ++s) mbar_init(&sm.full[s], 1);
+  if (threadIdx.x == 0) {
+    for (uint32_t s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], VH);
+    }
     fence_barrier_init();
-    prefetch_tensormap(&kv_map);
   }
-  __syncwarp();
+  __syncthreads();
 
-  // ---------------- producer state (identical in every lane)
-  // blk counts 16-key chunks; the block table is read through a window of 32
-  // entries held one per lane
-  constexpr int sh = SH;
-  // K/V rows are read once per step: evict them from L2 first, so that the
-  // split-KV partials, q rows and tables stay (on the mixed step: decode
-  // 827 -> 819 us; combine of 8 long contexts 17 -> 13 us)
-  const uint64_t l2_policy = l2_evict_first_policy();
-  long long x = x0;
-  bool new_piece = true;
-  L = __ldg(p.seq_lens + r);
-  t = __ldg(p.qsl + r);
-  int nent = (L + (1 << sh) - 1) >> sh;  // table entries the request uses
-  int win_r = -1, win_base = 0, win_val = -1;
-
-  auto produce = [&](int s) {
-    if (x >= x1) {
-      if (lane == 0) {
-        sm.meta0[s] = make_int4(0, 0, 0, kEnd);
-        mbar_arrive(&sm.full[s]);
+  if (warp == VH) {
+    // ================= producer warp: metadata, block-table lookups and the
+    // copies of every chunk of the range, S stages ahead of the consumers
+    if (lane == 0) prefetch_tensormap(&kv_map);
+    constexpr int sh = SH;
+    // K/V rows are read once per step: evict them from L2 first, so that the
+    // split-KV partials, q rows and tables stay (mixed step: 827 -> 819 us)
+    const uint64_t l2_policy = l2_evict_first_policy();
+    int L = __ldg(p.seq_lens + r), t = __ldg(p.qsl + r);
+    int nent = (L + (1 << sh) - 1) >> sh;  // table entries the request uses
+    int win_r = -1, win_base = 0, win_val = -1;
+    int out_base = -1;
+    bool new_piece = true;
+    long long x = x0;
+    uint32_t issued = 0;  // stages handed out so far
+    uint32_t s = 0, eph = 0;  // ring slot of the next stage; parity of its empty barrier
+    bool ok = true;
+    for (;; ++issued) {
+      if (issued >= S && !mbar_wait(&empty[s], eph)) {
+        if (lane == 0) atomicOr(&g_errors_decode, kErrTimeout);
+        ok = false;
+        break;
       }
-      return;
-    }
-    if (new_piece) {
-      const long long a = static_cast<long long>(p.virt_heads) * __ldg(p.dec_prefix + r) +
-                          static_cast<long long>(vg) * nblk;
-      const long long wf = owner_warp(a, N, W), wl = owner_warp(a + nblk - 1, N, W);
-      out_slot = (wf == wl) ? -1 : static_cast<int>(static_cast<long long>(r) * p.virt_heads + vg + w);
-    }
-    // table entries of chunk blk: e0, and e0 + 1 for 8-token blocks
-    const int e0 = (sh == 4) ? blk : (sh == 5 ? blk >> 1 : 2 * blk);
-    const int e_hi = (sh == 3) ? e0 + 1 : e0;  // (constant-folded per block size)
-    if (r != win_r || e0 < win_base || e_hi >= win_base + 32) {
-      win_r = r;
-      win_base = e0;
-      const int j = e0 + lane;
-      win_val = (j < nent) ? __ldg(p.block_table + static_cast<long long>(r) * p.max_blocks + j) : -1;
-    }
-    const int phys = __shfl_sync(0xffffffffu, win_val, e0 - win_base);
-    const int nvalid = min(kChunkKeys, L - blk * kChunkKeys);
-    bool valid = phys >= 0 && phys < p.num_blocks;
-    bool second = false;  // 8-token blocks: the chunk's keys 8..15 exist
-    int phys1 = -1;
-    if constexpr (sh == 3) {
-      phys1 = __shfl_sync(0xffffffffu, win_val, e_hi - win_base);
-      second = nvalid > 8;
-      if (second) valid = valid && phys1 >= 0 && phys1 < p.num_blocks;
-    }
-    int flags = (new_piece ? kFirst : 0) | ((blk == nblk - 1 || x == x1 - 1) ? kLast : 0) |
-                (valid ? 0 : kInvalid);
-    if (lane == 0) {
-      sm.meta0[s] = make_int4(r, vg, blk, flags);
-      sm.meta1[s] = make_int4(nvalid, t, out_slot, 0);
-      const uint32_t kv_tx = (sh == 3 && !second) ? C::kKvBytes / 2 : C::kKvBytes;
-      const uint32_t tx = (valid ? kv_tx : 0u) + (new_piece ? C::kQBytes : 0u);
-      if (!valid) atomicOr(&g_errors_decode, kErrBlockRange);
-      if (tx) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&sm.full[s], tx);
-        if (valid) {
-          // pool rows of one kv head: (block * 2 + k|v) * B + offset
-          const int hk = vg / p.head_groups;
-          uint16_t* dst = &sm.kv[s][0][0];
-          if constexpr (sh == 4) {  // K and V of the block: 32 consecutive rows
-            tma_load_3d_hint(dst, &kv_map, 0, hk, phys * 32, &sm.full[s], l2_policy);
-          } else if constexpr (sh == 5) {  // half (blk & 1) of the block's K rows and V rows
-            const int row = phys * 64 + (blk & 1) * 16;
-            tma_load_3d_hint(dst, &kv_map, 0, hk, row, &sm.full[s], l2_policy);
-            tma_load_3d_hint(dst + 16 * D, &kv_map, 0, hk, row + 32, &sm.full[s], l2_policy);
-          } else {  // two blocks of 8, each its 16 consecutive K and V rows
-            tma_load_3d_hint(dst, &kv_map, 0, hk, phys * 16, &sm.full[s], l2_policy);
-            if (second) tma_load_3d_hint(dst + 16 * D, &kv_map, 0, hk, phys1 * 16, &sm.full[s], l2_policy);
-          }
+      if (x >= x1) {
+        if (lane == 0) {
+          meta[s] = make_int4(kEnd, 0, 0, 0);
+          mbar_arrive(&full[s]);
         }
-        if (new_piece)
-          bulk_load(&sm.q[s][0], p.q + static_cast<long long>(t) * p.q_stride + vg * GW * D,
-                    C::kQBytes, &sm.full[s]);
-      } else {
-        mbar_arrive(&sm.full[s]);
+        ++issued;
+        break;
       }
-    }
-    // advance the odometer (request, virtual head, block)
-    ++x;
-    ++blk;
-    new_piece = false;
-    if (blk == nblk) {
-      blk = 0;
-      new_piece = true;
-      if (++vg == p.virt_heads) {
-        vg = 0;
+      if (new_piece) {
+        const long long a = __ldg(p.dec_prefix + r);
+        const long long cf = owner_cta(a, N, Cn), cl = owner_cta(a + nblk - 1, N, Cn);
+        out_base = (cf == cl) ? -1 : static_cast<int>((r + c) * p.virt_heads);
+      }
+      // table entries of chunk blk: e0, and e0 + 1 for 8-token blocks
+      const int e0 = (sh == 4) ? blk : (sh == 5 ? blk >> 1 : 2 * blk);
+      const int e_hi = (sh == 3) ? e0 + 1 : e0;
+      if (r != win_r || e0 < win_base || e_hi >= win_base + 32) {
+        win_r = r;
+        win_base = e0;
+        const int j = e0 + lane;
+        win_val = (j < nent) ? __ldg(p.block_table + static_cast<long long>(r) * p.max_blocks + j) : -1;
+      }
+      const int phys = __shfl_sync(0xffffffffu, win_val, e0 - win_base);
+      const int nvalid = min(kChunkKeys, L - blk * kChunkKeys);
+      bool valid = phys >= 0 && phys < p.num_blocks;
+      bool second = false;  // 8-token blocks: the chunk's keys 8..15 exist
+      int phys1 = -1;
+      if constexpr (sh == 3) {
+        phys1 = __shfl_sync(0xffffffffu, win_val, e_hi - win_base);
+        second = nvalid > 8;
+        if (second) valid = valid && phys1 >= 0 && phys1 < p.num_blocks;
+      }
+      const int flags = (new_piece ? kFirst : 0) | ((blk == nblk - 1 || x == x1 - 1) ? kLast : 0) |
+                        (valid ? 0 : kInvalid);
+      if (lane == 0) {
+        meta[s] = make_int4(flags, nvalid, t, out_base);
+        unsigned char* stage = base + s * lay.stage_bytes;
+        const uint32_t kv_tx = (sh == 3 && !second) ? lay.kv_bytes / 2 : lay.kv_bytes;
+        const uint32_t q_tx = static_cast<uint32_t>(VH) * GW * D * 2u;
+        const uint32_t tx = (valid ? kv_tx : 0u) + (new_piece ? q_tx : 0u);
+        if (!valid) atomicOr(&g_errors_decode, kErrBlockRange);
+        if (tx) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(&full[s], tx);
+          if (valid) {
+            // pool rows of the slab's kv heads: (block * 2 + k|v) * B + offset
+            const int hk0 = slab * KH;
+            if constexpr (sh == 4) {  // K and V of the block: 32 consecutive rows
+              tma_load_3d_hint(stage, &kv_map, 0, hk0, phys * 32, &full[s], l2_policy);
+            } else if constexpr (sh == 5) {  // half (blk & 1) of the K rows and of the V rows
+              const int row = phys * 64 + (blk & 1) * 16;
+              tma_load_3d_hint(stage, &kv_map, 0, hk0, row, &full[s], l2_policy);
+              tma_load_3d_hint(stage + 16 * lay.row_bytes, &kv_map, 0, hk0, row + 32, &full[s],
+                               l2_policy);
+            } else {  // two blocks of 8, each its 16 consecutive K and V rows
+              tma_load_3d_hint(stage, &kv_map, 0, hk0, phys * 16, &full[s], l2_policy);
+              if (second)
+                tma_load_3d_hint(stage + 16 * lay.row_bytes, &kv_map, 0, hk0, phys1 * 16, &full[s],
+                                 l2_policy);
+            }
+          }
+          if (new_piece)  // the slab's q rows of the request (contiguous in the token row)
+            bulk_load(stage + lay.kv_bytes,
+                      p.q + static_cast<long long>(t) * p.q_stride + slab * VH * GW * D, q_tx,
+                      &full[s]);
+        } else {
+          mbar_arrive(&full[s]);
+        }
+      }
+      if (++s == S) {  // ring wraps; from the second wrap on, the empty parity flips
+        s = 0;
+        if (issued + 1 > S) eph ^= 1u;
+      }
+      // advance (request, chunk)
+      ++x;
+      ++blk;
+      new_piece = false;
+      if (blk == nblk) {
+        blk = 0;
+        new_piece = true;
         if (x < x1) {
           do {
             ++r;
@@ -380,10 +420,20 @@ __global__ void __launch_bounds__(WARPS * 32)
         }
       }
     }
-  };
+    if (!ok && lane == 0) {
+      // let every copy in flight land before the shared memory goes away
+      for (uint32_t k = (issued > S ? issued - S : 0); k < issued; ++k)
+        mbar_wait(&full[k % S], (k / S) & 1u, kDrainLimitNs);
+    }
+    return;
+  }
 
-  // ---------------- consumer state
-  // Position p of the per-block score registers holds logical index
+  // ================= consumer warp: virtual head vg = slab * VH + warp
+  const int vg = slab * VH + warp;
+  const int hk_local = warp / p.head_groups;  // kv head within the slab
+  auto& scr = reinterpret_cast<typename C::WarpScratch*>(base + lay.scratch_off)[warp];
+  const int sub = lane / C::LPK, li = lane % C::LPK;
+  // Position p of the per-chunk score registers holds logical index
   // p ^ perm: q head (p / KPL) ^ perm_h, key slot (p % KPL) ^ perm_k.
   const int perm = (li * C::NV) / C::LPK;
   const int perm_h = perm / C::KPL, perm_k = perm % C::KPL;
@@ -391,30 +441,21 @@ __global__ void __launch_bounds__(WARPS * 32)
   float2 q2[GW][4];  // q * scale * log2(e), position order (head hp ^ perm_h)
   float2 o2[GW][4];  // unnormalised output, logical heads, dims li*8 .. li*8+7
   float m_run = -INFINITY, l_run = 0.f;  // for head hm of this lane
+  const uint32_t RS = lay.row_bytes;    // bytes between stage rows
 
-#pragma unroll
-  for (int s = 0; s < S; ++s) produce(s);
-
-  uint32_t phases = 0;
-  int s = 0;
-  while (true) {
-    const uint32_t par = (phases >> s) & 1u;
-    phases ^= 1u << s;
-    if (!mbar_wait(&sm.full[s], par)) {
+  for (uint32_t s = 0, fph = 0;;) {  // ring slot, parity of its full barrier
+    if (!mbar_wait(&full[s], fph)) {
       atomicOr(&g_errors_decode, kErrTimeout);
-      // drain every stage that may still have a copy in flight, then stop
-      for (int k = 0; k < S; ++k)
-        if (k != s) mbar_wait(&sm.full[k], (phases >> k) & 1u, kDrainLimitNs);
       break;
     }
-    const int4 m0 = sm.meta0[s];
-    if (m0.w & kEnd) break;
-    const int4 m1 = sm.meta1[s];
-    const int flags = m0.w;
-    const uint32_t kv_base = smem_u32(&sm.kv[s][0][0]) + li * 16;
+    const int4 m = meta[s];
+    if (m.x & kEnd) break;
+    const int flags = m.x, nvalid = m.y, row = m.z, out_base = m.w;
+    const unsigned char* stage = base + s * lay.stage_bytes;
+    const uint32_t kv_base = smem_u32(stage) + hk_local * D * 2 + li * 16;
 
     if (flags & kFirst) {
-      const uint32_t qa = smem_u32(&sm.q[s][0]) + li * 16;
+      const uint32_t qa = smem_u32(stage + lay.kv_bytes) + warp * GW * D * 2 + li * 16;
 #pragma unroll
       for (int hp = 0; hp < GW; ++hp) {
         const uint4 qv = ld_shared_v4(qa + (hp ^ perm_h) * D * 2);
@@ -429,14 +470,13 @@ __global__ void __launch_bounds__(WARPS * 32)
       l_run = 0.f;
     }
     const bool bvalid = !(flags & kInvalid);
-    const int nvalid = m1.x;
 
     // ---- scores, partial over this lane's 8 dims
     float acc[C::NV];
 #pragma unroll
     for (int jp = 0; jp < C::KPL; ++jp) {
       const int key = (jp ^ perm_k) * C::KPI + sub;
-      const uint4 kv4 = ld_shared_v4(kv_base + k_row<SH>(key) * D * 2);
+      const uint4 kv4 = ld_shared_v4(kv_base + k_row<SH>(key) * RS);
       const uint32_t wd[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
       float2 k2[4];
 #pragma unroll
@@ -455,10 +495,10 @@ __global__ void __launch_bounds__(WARPS * 32)
     float sc[C::NPL];
     float lmax = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < C::NPL; ++i) {
-      const int key = ((perm + i) % C::KPL) * C::KPI + sub;
-      sc[i] = (bvalid && key < nvalid) ? acc[i] : -INFINITY;
-      lmax = fmaxf(lmax, sc[i]);
+    for (int q = 0; q < C::NPL; ++q) {
+      const int key = ((perm + q) % C::KPL) * C::KPI + sub;
+      sc[q] = (bvalid && key < nvalid) ? acc[q] : -INFINITY;
+      lmax = fmaxf(lmax, sc[q]);
     }
 #pragma unroll
     for (int off = 1; off < C::LPH; off <<= 1)
@@ -471,20 +511,20 @@ __global__ void __launch_bounds__(WARPS * 32)
       const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
       l_run *= alpha;
       m_run = m_new;
-      if (sub == 0 && (li % C::LPH) == 0) sm.hs[hm].x = alpha;
+      if (sub == 0 && (li % C::LPH) == 0) scr.hs[hm].x = alpha;
       __syncwarp();
 #pragma unroll
       for (int h = 0; h < GW; ++h) {
-        const float a = sm.hs[h].x;
+        const float a = scr.hs[h].x;
 #pragma unroll
         for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(o2[h][e].x * a, o2[h][e].y * a);
       }
     }
     float psum = 0.f;
 #pragma unroll
-    for (int i = 0; i < C::NPL; ++i) {
-      const float pv = (sc[i] == -INFINITY || m_run == -INFINITY) ? 0.f : exp2f(sc[i] - m_run);
-      sm.p[sub][perm + i] = pv;
+    for (int q = 0; q < C::NPL; ++q) {
+      const float pv = (sc[q] == -INFINITY || m_run == -INFINITY) ? 0.f : exp2f(sc[q] - m_run);
+      scr.p[sub][perm + q] = pv;
       psum += pv;
     }
     l_run += psum;
@@ -494,16 +534,16 @@ __global__ void __launch_bounds__(WARPS * 32)
     {
       float pj[C::NV];
 #pragma unroll
-      for (int i = 0; i < C::NV; i += 4) {
-        const float4 f = ld_shared_f4(smem_u32(&sm.p[sub][i]));
-        pj[i] = f.x;
-        pj[i + 1] = f.y;
-        pj[i + 2] = f.z;
-        pj[i + 3] = f.w;
+      for (int q = 0; q < C::NV; q += 4) {
+        const float4 f = ld_shared_f4(smem_u32(&scr.p[sub][q]));
+        pj[q] = f.x;
+        pj[q + 1] = f.y;
+        pj[q + 2] = f.z;
+        pj[q + 3] = f.w;
       }
       auto pv_key = [&](int j) {
         const int key = j * C::KPI + sub;
-        const uint4 vv = ld_shared_v4(kv_base + v_row<SH>(key) * D * 2);
+        const uint4 vv = ld_shared_v4(kv_base + v_row<SH>(key) * RS);
         const uint32_t wd[4] = {vv.x, vv.y, vv.z, vv.w};
         float2 v2[4];
 #pragma unroll
@@ -527,7 +567,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     __syncwarp();
 
-    // ---- end of this warp's piece of (request, head group)
+    // ---- end of this CTA's piece of the request
     if (flags & kLast) {
 #pragma unroll
       for (int off = C::LPK; off < 32; off <<= 1)
@@ -543,13 +583,13 @@ __global__ void __launch_bounds__(WARPS * 32)
       for (int off = 1; off < C::LPH; off <<= 1) lo += __shfl_xor_sync(0xffffffffu, lo, off);
 #pragma unroll
       for (int off = C::LPK; off < 32; off <<= 1) lo += __shfl_xor_sync(0xffffffffu, lo, off);
-      if (sub == 0 && (li % C::LPH) == 0) sm.hs[hm] = make_float2(m_run, lo);
+      if (sub == 0 && (li % C::LPH) == 0) scr.hs[hm] = make_float2(m_run, lo);
       __syncwarp();
-      const int vgh = m0.y, slot = m1.z, row = m1.y;
+      const long long slot = out_base < 0 ? -1 : static_cast<long long>(out_base) + vg;
       if (sub == 0) {
 #pragma unroll
         for (int h = 0; h < GW; ++h) {
-          const float2 ml = sm.hs[h];
+          const float2 ml = scr.hs[h];
           if (slot < 0) {
             const float inv = 1.f / ml.y;
             uint4 ov;
@@ -558,59 +598,59 @@ __global__ void __launch_bounds__(WARPS * 32)
             ov.z = pack_bf16x2(o2[h][2].x * inv, o2[h][2].y * inv);
             ov.w = pack_bf16x2(o2[h][3].x * inv, o2[h][3].y * inv);
             const long long off =
-                (static_cast<long long>(row) * p.num_q_heads + vgh * GW + h) * D + li * 8;
+                (static_cast<long long>(row) * p.num_q_heads + vg * GW + h) * D + li * 8;
             *reinterpret_cast<uint4*>(p.out + off) = ov;
           } else {
-            float4* dst = reinterpret_cast<float4*>(
-                p.part_o + (static_cast<long long>(slot) * GW + h) * D + li * 8);
+            float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * GW + h) * D + li * 8);
             dst[0] = make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
             dst[1] = make_float4(o2[h][2].x, o2[h][2].y, o2[h][3].x, o2[h][3].y);
-            if (li == 0) p.part_ml[static_cast<long long>(slot) * GW + h] = ml;
+            if (li == 0) p.part_ml[slot * GW + h] = ml;
           }
         }
       }
-      __syncwarp();
     }
-
-    produce(s);
-    s = (s + 1 == S) ? 0 : s + 1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
+    if (++s == S) {
+      s = 0;
+      fph ^= 1u;
+    }
   }
 }
 
 // ------------------------------------------------------------------ combine
-// One CTA per warp boundary w of the decode split, one warp per q head of
-// the pair. A (request, virtual head) pair is split when a boundary falls
-// strictly inside its blocks; the first such boundary is the one right after
-// the warp that owns the pair's first block, and that boundary's CTA merges
-// the pair's partials (one per non-empty warp range that touched it):
+// One CTA per (range boundary c of the split, virtual head vg), one warp per
+// q head. A request is split when a boundary falls strictly inside its
+// chunks; the first such boundary is the one right after the CTA that owns
+// the request's first chunk, and that boundary's CTAs merge the request's
+// partials (one per non-empty range that touched it):
 //   M = max_p m_p,  o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p.
 // Lanes first read the (m, l) of up to 32 pieces at once, then every lane
 // sums its dims over the pieces with independent loads.
 template <int D, int GW>
 __global__ void __launch_bounds__(GW * 32) combine_kernel(const DecodeParams p) {
-  const long long w = blockIdx.x;
+  const long long c = blockIdx.x;
+  const int vg = blockIdx.y;
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long W = p.warps;
+  const long long Cn = p.splits;
   pdl_trigger();
   pdl_wait();
-  if (w < 1 || w >= W) return;
-  const int2 rec = p.bound[w];
-  if (rec.x < 0) return;
-  const int r = rec.x, vg = rec.y;
+  if (c < 1 || c >= Cn) return;
+  const int r = p.bound[c];
+  if (r < 0) return;
   const int pr = __ldg(p.dec_prefix + r);
   const int nblk = __ldg(p.dec_prefix + r + 1) - pr;
-  const long long N = static_cast<long long>(p.virt_heads) * p.hdr[kHdrDecodeBlocks];
-  const long long a = static_cast<long long>(p.virt_heads) * pr + static_cast<long long>(vg) * nblk;
-  const long long wf = owner_warp(a, N, W);
-  if (wf != w - 1) return;
-  const int npieces = static_cast<int>(owner_warp(a + nblk - 1, N, W) - wf + 1);
-  const long long base = static_cast<long long>(r) * p.virt_heads + vg + wf;  // slot of piece 0
+  const long long N = p.hdr[kHdrDecodeBlocks];
+  const long long cf = owner_cta(pr, N, Cn);
+  if (cf != c - 1) return;
+  const int npieces = static_cast<int>(owner_cta(pr + nblk - 1, N, Cn) - cf + 1);
+  // slot of piece j (CTA cf + j): (r + cf + j) * V + vg
 
-  // (m, l) of piece j; empty warp ranges wrote nothing and weigh zero
+  // (m, l) of piece j; empty ranges wrote nothing and weigh zero
   auto piece_ml = [&](int j) -> float2 {
-    const long long ww = wf + j;
-    if (j >= npieces || ww * N / W == (ww + 1) * N / W) return make_float2(-INFINITY, 0.f);
-    return p.part_ml[(base + j) * GW + h];
+    const long long cc = cf + j;
+    if (j >= npieces || cc * N / Cn == (cc + 1) * N / Cn) return make_float2(-INFINITY, 0.f);
+    return p.part_ml[((r + cc) * p.virt_heads + vg) * GW + h];
   };
   float M = -INFINITY;
   for (int j0 = 0; j0 < npieces; j0 += 32) M = fmaxf(M, piece_ml(j0 + lane).x);
@@ -631,7 +671,8 @@ __global__ void __launch_bounds__(GW * 32) combine_kernel(const DecodeParams p) 
     for (int j = 0; j < cnt; ++j) {
       const float wj = __shfl_sync(0xffffffffu, wgt, j);
       if (wj == 0.f) continue;
-      const float* src = p.part_o + ((base + j0 + j) * GW + h) * D + lane * E;
+      const float* src =
+          p.part_o + (((r + cf + j0 + j) * p.virt_heads + vg) * GW + h) * D + lane * E;
       if constexpr (E == 4) {
         const float4 v = *reinterpret_cast<const float4*>(src);
         acc[0] += wj * v.x;
@@ -662,32 +703,39 @@ __global__ void __launch_bounds__(GW * 32) combine_kernel(const DecodeParams p) 
 }
 
 // ------------------------------------------------------------------ host
-#ifndef PKV_DECODE_STAGES
-#define PKV_DECODE_STAGES 2
+#ifndef PKV_DECODE_MAX_STAGES
+#define PKV_DECODE_MAX_STAGES 6
 #endif
-#ifndef PKV_DECODE_WARPS
-#define PKV_DECODE_WARPS 4
-#endif
-constexpr int kDecodeStages = PKV_DECODE_STAGES;  // smem stages per warp
-constexpr int kDecodeWarps = PKV_DECODE_WARPS;    // warps per CTA
+// Ring depth: as many stages as the CTA's share of the SM's shared memory
+// holds, within these bounds (one stage per 16-key chunk of the slab's kv
+// heads; more stages keep more bytes in flight per SM: 2 -> 3 stages of
+// 64 KB took the mixed-step decode from 830 to 788 us)
+constexpr int kDecodeMinStages = 2;
+constexpr int kDecodeMaxStages = PKV_DECODE_MAX_STAGES;
 
-// At most this many decode CTAs per SM in the default split, even where
-// registers would fit a third: on the 1280-decode mixed
-// step (d = 128, 32 q / 8 kv heads) 2 CTAs of 4 warps per SM streamed at
-// 0.98 of the copy peak and 3 at 0.93 (shorter warp ranges, more partials).
-#ifndef PKV_DECODE_MAX_CTAS
-#define PKV_DECODE_MAX_CTAS 2
-#endif
-constexpr int kDecodeMaxCtasPerSm = PKV_DECODE_MAX_CTAS;
+// Consumer warps per SM the default split aims at (CTAs per SM = this / slab
+// size, at least one): about the count that streamed fastest.
+constexpr int kDecodeWarpsPerSm = 8;
+
+// Decode slab of a shape: virtual heads per CTA and kv heads per CTA.
+void decode_slab(int num_kv_heads, int group, int* vh, int* kh) {
+  const int gw = decode_heads_per_warp(group);
+  const int hg = group / gw;
+  const int V = num_kv_heads * hg;
+  int s = V <= kDecodeMaxSlab ? V : kDecodeMaxSlab;
+  while (V % s || s % hg) --s;  // whole kv heads per slab, equal slabs
+  *vh = s;
+  *kh = s / hg;
+}
 
 template <int D, int GW>
-constexpr size_t decode_smem_bytes() {
-  // More than 1 / (kDecodeMaxCtasPerSm + 1) of an SM's shared memory
-  // (228 KB), so that no SM ever holds more than kDecodeMaxCtasPerSm CTAs -- also when the grid is
-  // launched early (programmatic dependent launch) and its first CTAs land
-  // on the few SMs the previous kernel has already left.
-  constexpr size_t used = sizeof(typename DecodeCfg<D, GW, kDecodeStages>::WarpSmem) * kDecodeWarps + 128;
-  constexpr size_t share = 228u * 1024u / (kDecodeMaxCtasPerSm + 1) + 1024u;
+static size_t decode_smem_bytes(int kh, int vh, int stages, int ctas_per_sm) {
+  // More than 1 / (ctas_per_sm + 1) of an SM's shared memory (228 KB), so
+  // that no SM ever holds more CTAs than the split assumes -- also when the
+  // grid is launched early (programmatic dependent launch) and its first
+  // CTAs land on the few SMs the previous kernel has already left.
+  const size_t used = DecodeLayout<D, GW>(kh, vh, stages).total + 128;
+  const size_t share = 228u * 1024u / (ctas_per_sm + 1) + 1024u;
   return used > share ? used : share;
 }
 
@@ -695,28 +743,42 @@ template <int D, int GW, int SH>
 static std::atomic<unsigned long long> g_decode_attr_done{0};
 
 template <int D, int GW, int SH>
-static cudaError_t decode_occupancy(int* ctas_per_sm) {
-  auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps, SH>;
-  const size_t smem = decode_smem_bytes<D, GW>();
-  cudaError_t e = smem_attr_once(kern, static_cast<int>(smem), g_decode_attr_done<D, GW, SH>);
+static cudaError_t decode_prepare(int kh, int vh, int num_sms, long long* splits, int* stages,
+                                  size_t* smem) {
+  auto kern = decode_kernel<D, GW, SH>;
+  cudaError_t e = smem_attr_once(kern, 227 * 1024, g_decode_attr_done<D, GW, SH>);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, kern, kDecodeWarps * 32, smem);
+  int want = kDecodeWarpsPerSm / vh;
+  if (want < 1) want = 1;
+  const size_t least = DecodeLayout<D, GW>(kh, vh, kDecodeMinStages).total + 128;
+  int fit = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, (vh + 1) * 32, least);
+  if (e != cudaSuccess) return e;
+  const int ctas = fit < want ? (fit < 1 ? 1 : fit) : want;
+  // deepest ring within the CTA's share (the SM's 228 KB less 1 KB reserved per CTA)
+  const size_t budget = 228u * 1024u / ctas - 1024u;
+  int S = kDecodeMinStages;
+  while (S < kDecodeMaxStages && DecodeLayout<D, GW>(kh, vh, S + 1).total + 128 <= budget) ++S;
+  *stages = S;
+  *smem = decode_smem_bytes<D, GW>(kh, vh, S, ctas);
+  if (splits) *splits = static_cast<long long>(num_sms) * ctas;
+  return cudaSuccess;
 }
 
 template <int D, int GW, int SH>
 static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_map,
-                                   cudaStream_t stream, void** trace) {
-  auto kern = decode_kernel<D, GW, kDecodeStages, kDecodeWarps, SH>;
-  const size_t smem = decode_smem_bytes<D, GW>();
-  cudaError_t e = smem_attr_once(kern, static_cast<int>(smem), g_decode_attr_done<D, GW, SH>);
+                                   int num_sms, cudaStream_t stream, void** trace) {
+  size_t smem = 0;
+  DecodeParams q = p;
+  cudaError_t e = decode_prepare<D, GW, SH>(p.slab_kh, p.slab_vh, num_sms, nullptr, &q.stages, &smem);
   if (e != cudaSuccess) return e;
-  const long long grid = (p.warps + kDecodeWarps - 1) / kDecodeWarps;
-  e = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kDecodeWarps * 32), smem, stream,
-                 kv_map, p);
+  const dim3 grid(static_cast<unsigned>(p.splits), static_cast<unsigned>(p.virt_heads / p.slab_vh));
+  e = launch_pdl(decode_kernel<D, GW, SH>, grid, dim3((p.slab_vh + 1) * 32), smem, stream, kv_map, q);
   if (e == cudaSuccess && trace) e = cudaEventRecord(static_cast<cudaEvent_t>(trace[3]), stream);
   if (e != cudaSuccess) return e;
-  return launch_pdl(combine_kernel<D, GW>, dim3(static_cast<unsigned>(p.warps)), dim3(GW * 32), 0,
-                    stream, p);
+  return launch_pdl(combine_kernel<D, GW>,
+                    dim3(static_cast<unsigned>(p.splits), static_cast<unsigned>(p.virt_heads)),
+                    dim3(GW * 32), 0, stream, p);
 }
 
 // Calls F<D, GW, SH>::run(args...) for the instantiated shapes: head_dim 64 or
@@ -735,28 +797,28 @@ static cudaError_t decode_dispatch(int head_dim, int gw, int sh, A&&... args) {
 }
 
 template <int D, int GW, int SH>
-struct OccupancyOp {
-  static cudaError_t run(int* ctas) { return decode_occupancy<D, GW, SH>(ctas); }
+struct PrepareOp {
+  static cudaError_t run(int kh, int vh, int sms, long long* splits) {
+    size_t smem = 0;
+    int stages = 0;
+    return decode_prepare<D, GW, SH>(kh, vh, sms, splits, &stages, &smem);
+  }
 };
 
 template <int D, int GW, int SH>
 struct LaunchOp {
-  static cudaError_t run(const DecodeParams& p, const CUtensorMap& m, cudaStream_t s, void** t) {
-    return launch_decode_t<D, GW, SH>(p, m, s, t);
+  static cudaError_t run(const DecodeParams& p, const CUtensorMap& m, int sms, cudaStream_t s,
+                         void** t) {
+    return launch_decode_t<D, GW, SH>(p, m, sms, s, t);
   }
 };
 
-
-cudaError_t decode_full_wave_warps(int head_dim, int group, int block_shift, int num_sms,
-                                   int* warps) {
-  int ctas = 0;
-  cudaError_t e = decode_dispatch<OccupancyOp>(head_dim, decode_heads_per_warp(group),
-                                               block_shift, &ctas);
-  if (e != cudaSuccess) return e;
-  if (ctas > kDecodeMaxCtasPerSm) ctas = kDecodeMaxCtasPerSm;
-  if (ctas < 1) ctas = 1;
-  *warps = num_sms * ctas * kDecodeWarps;
-  return cudaSuccess;
+cudaError_t decode_full_wave_splits(int head_dim, int num_kv_heads, int group, int block_shift,
+                                    int num_sms, long long* splits) {
+  int vh = 0, kh = 0;
+  decode_slab(num_kv_heads, group, &vh, &kh);
+  return decode_dispatch<PrepareOp>(head_dim, decode_heads_per_warp(group), block_shift, kh, vh,
+                                    num_sms, splits);
 }
 
 cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream) {
@@ -765,7 +827,7 @@ cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
-                          int decode_warps, cudaStream_t stream, void** trace) {
+                          long long splits, int num_sms, cudaStream_t stream, void** trace) {
   const int group = a.num_q_heads / a.num_kv_heads;
   const int gw = decode_heads_per_warp(group);
   DecodeParams p;
@@ -781,14 +843,16 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUte
   p.num_blocks = a.num_blocks;
   p.head_groups = group / gw;
   p.virt_heads = a.num_kv_heads * p.head_groups;
-  p.warps = decode_warps;
+  decode_slab(a.num_kv_heads, group, &p.slab_vh, &p.slab_kh);
+  p.splits = splits;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.dec_prefix = ws.dec_prefix;
   p.hdr = ws.hdr;
   p.part_ml = ws.part_ml;
   p.part_o = ws.part_o;
   p.bound = ws.bound;
-  return decode_dispatch<LaunchOp>(a.head_dim, gw, a.block_shift, p, kv_map, stream, trace);
+  return decode_dispatch<LaunchOp>(a.head_dim, gw, a.block_shift, p, kv_map, num_sms, stream,
+                                   trace);
 }
 
 cudaError_t read_errors_decode(uint32_t* out, bool clear) {

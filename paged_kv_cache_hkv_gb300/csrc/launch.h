@@ -27,7 +27,7 @@ struct AttnWorkspace {
   int32_t* pf_prefix;    // [R + 1]: prefill items before the k-th prefill request
   float2* part_ml;       // [slots][GW]: (running max in log2 units, sum)
   float* part_o;         // [slots][GW][D]: unnormalised partial outputs
-  int2* bound;           // [W]: pair holding the first position of each decode warp
+  int* bound;            // [C]: request holding the first position of each decode CTA range
 };
 
 struct AttnArgs {
@@ -83,10 +83,14 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // Heads handled together by one decode warp, and head groups per kv head.
 inline int decode_heads_per_warp(int group) { return group < 4 ? group : 4; }
 
-// slots of split-KV partials the decode kernel may write
-inline long long decode_partial_slots(int num_reqs, int virt_heads, long long warps) {
-  return static_cast<long long>(num_reqs) * virt_heads + warps;
+// slots of split-KV partials the decode kernel may write: (request + CTA) *
+// virtual heads + virtual head
+inline long long decode_partial_slots(int num_reqs, int virt_heads, long long splits) {
+  return (static_cast<long long>(num_reqs) + splits) * virt_heads;
 }
+
+// Virtual heads (consumer warps) and kv heads of one decode CTA for a shape.
+void decode_slab(int num_kv_heads, int group, int* slab_vh, int* slab_kh);
 
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int max_blocks,
                                 const int32_t* qsl, const int32_t* num_computed, int num_reqs,
@@ -104,14 +108,14 @@ cudaError_t launch_copy_blocks(void* dst, int dst_num_blocks, const void* src, i
 
 cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream);
 
-// Decode warps in one full wave on this device for the given shape.
-cudaError_t decode_full_wave_warps(int head_dim, int group, int block_shift, int num_sms,
-                                   int* warps);
+// Decode splits (CTAs along the decode stream) in one full wave of the device.
+cudaError_t decode_full_wave_splits(int head_dim, int num_kv_heads, int group, int block_shift,
+                                    int num_sms, long long* splits);
 
 // trace: NULL or the caller's event array; event [3] is recorded between the
 // decode and the combine kernel.
 cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
-                          int decode_warps, cudaStream_t stream, void** trace);
+                          long long splits, int num_sms, cudaStream_t stream, void** trace);
 
 cudaError_t launch_prefill(const AttnArgs& a, const AttnWorkspace& ws, const CUtensorMap& kv_map,
                            const CUtensorMap& q_map, int num_sms, cudaStream_t stream);

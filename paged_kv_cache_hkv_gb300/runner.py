@@ -29,7 +29,7 @@ def bf16_to_numpy(t: torch.Tensor) -> np.ndarray:
 class DeviceStep:
     """One step's inputs on the GPU plus its output buffers."""
 
-    def __init__(self, step, device="cuda", decode_warps=None, upload_pool=True):
+    def __init__(self, step, device="cuda", decode_splits=None, upload_pool=True):
         self.step = step
         self.device = torch.device(device)
         dev = self.device
@@ -45,11 +45,11 @@ class DeviceStep:
         self.slot_mapping = torch.empty(T, dtype=torch.int64, device=dev)
         self.out = torch.zeros((T, step.num_q_heads, step.head_dim), dtype=torch.bfloat16,
                                device=dev)
-        self.decode_warps = decode_warps
+        self.decode_splits = decode_splits
         self.layout = binding.pkv_cache_layout(step.num_blocks, step.block_size,
                                                step.num_kv_heads, step.head_dim)
         nbytes = binding.pkv_attention_workspace_size(step.num_reqs, step.num_q_heads,
-                                                      self.layout, decode_warps=decode_warps)
+                                                      self.layout, decode_splits=decode_splits)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
 
     # -- the three calls of the hot path
@@ -68,7 +68,7 @@ class DeviceStep:
             self.out, self.q, self.kv_cache, self.block_table, self.seq_lens,
             self.query_start_loc, self.num_computed, max_query_len=s.max_query_len,
             max_seq_len=s.max_seq_len, scale=s.scale, workspace=self.workspace,
-            decode_warps=self.decode_warps, stream=stream)
+            decode_splits=self.decode_splits, stream=stream)
 
     def run(self, stream=None):
         self.slot_map(stream)

@@ -1,11 +1,12 @@
 """CPU restatement of the decode kernel's integer work split and lane maps.
 
-The split-KV decode kernel cuts the step's stream of (request, kv head,
-block) positions into W equal ranges, one per warp; a (request, kv head)
-that straddles ranges is merged by the combine kernel from one partial slot
-per warp that touched it. These tests walk that rule in Python for many
-random shapes and check that every block is visited exactly once, that the
-partial slots never collide, and that the combine finds exactly the warps
+The split-KV decode kernel cuts the step's stream of (request, 16-key chunk)
+positions into C equal ranges, one per CTA (every head of a request's chunk
+is handled by the same CTA); a request that straddles ranges leaves one
+partial per CTA that touched it, in slot (request + CTA) * V + virtual head,
+and the combine kernel merges them. These tests walk that rule in Python for
+many random shapes and check that every chunk is visited exactly once, that
+the partial slots never collide, and that the combine finds exactly the CTAs
 that wrote. A second test replays the warp reduce-scatter of partial dot
 products lane by lane for every (head_dim, heads-per-warp) variant.
 """
@@ -14,81 +15,80 @@ import numpy as np
 import pytest
 
 
-def owner(x, N, W):
-    """Warp whose range [floor(w*N/W), floor((w+1)*N/W)) holds position x."""
-    return ((x + 1) * W + N - 1) // N - 1
+def owner(x, N, C):
+    """CTA whose range [floor(c*N/C), floor((c+1)*N/C)) holds position x."""
+    return ((x + 1) * C + N - 1) // N - 1
 
 
-def walk_split(nblk, Hv, W):
+def walk_split(nblk, V, C):
+    """Replay every CTA's range: (request, chunk) visits and partial slots."""
     R = len(nblk)
     prefix = np.concatenate([[0], np.cumsum(nblk)]).astype(np.int64)
-    N = Hv * int(prefix[-1])
+    N = int(prefix[-1])
     seen, slots = {}, {}
-    for w in range(W):
-        x0, x1 = w * N // W, (w + 1) * N // W
+    for c in range(C):
+        x0, x1 = c * N // C, (c + 1) * N // C
         if x0 >= x1:
             continue
-        u = x0 // Hv
-        r = max(i for i in range(R) if prefix[i] <= u)
+        r = max(i for i in range(R) if prefix[i] <= x0)
         nb = int(prefix[r + 1] - prefix[r])
         assert nb > 0
-        rem = x0 - Hv * int(prefix[r])
-        vg, blk = rem // nb, rem % nb
+        blk = x0 - int(prefix[r])
         x, new_piece = x0, True
         while x < x1:
             if new_piece:
-                a = Hv * int(prefix[r]) + vg * nb
-                wf, wl = owner(a, N, W), owner(a + nb - 1, N, W)
-                assert wf <= w <= wl
-                if wf != wl:
-                    slot = r * Hv + vg + w
-                    assert 0 <= slot < R * Hv + W
-                    assert slot not in slots
-                    slots[slot] = (r, vg)
-            key = (r, vg, blk)
+                a = int(prefix[r])
+                cf, cl = owner(a, N, C), owner(a + nb - 1, N, C)
+                assert cf <= c <= cl
+                if cf != cl:
+                    for vg in range(V):
+                        slot = (r + c) * V + vg
+                        assert 0 <= slot < (R + C) * V
+                        assert slot not in slots
+                        slots[slot] = (r, vg)
+            key = (r, blk)
             assert key not in seen
-            seen[key] = w
+            seen[key] = c
             x += 1
             blk += 1
             new_piece = False
             if blk == nb:
                 blk, new_piece = 0, True
-                vg += 1
-                if vg == Hv:
-                    vg = 0
-                    if x < x1:
+                if x < x1:
+                    r += 1
+                    nb = int(prefix[r + 1] - prefix[r])
+                    while nb == 0:
                         r += 1
                         nb = int(prefix[r + 1] - prefix[r])
-                        while nb == 0:
-                            r += 1
-                            nb = int(prefix[r + 1] - prefix[r])
     return prefix, N, seen, slots
 
 
 @pytest.mark.parametrize("trial", range(60))
-def test_stream_k_split_covers_every_block_once(trial):
+def test_stream_k_split_covers_every_chunk_once(trial):
     rng = np.random.default_rng(trial)
     R = int(rng.integers(1, 12))
     nblk = rng.integers(0, 30, size=R)
     if nblk.sum() == 0:
         nblk[0] = 3
-    Hv = int(rng.choice([1, 2, 4, 8]))
-    W = int(rng.integers(1, 300))
-    prefix, N, seen, slots = walk_split(nblk, Hv, W)
+    V = int(rng.choice([1, 2, 4, 8, 16]))
+    C = int(rng.integers(1, 300))
+    prefix, N, seen, slots = walk_split(nblk, V, C)
     assert len(seen) == N
     for r in range(R):
         nb = int(prefix[r + 1] - prefix[r])
-        for vg in range(Hv if nb else 0):
-            a = Hv * int(prefix[r]) + vg * nb
-            wf, wl = owner(a, N, W), owner(a + nb - 1, N, W)
-            writers = {seen[(r, vg, b)] for b in range(nb)}
-            if wf == wl:
-                assert writers == {wf}
-            else:
-                # the combine skips warps whose range is empty
-                used = {w for w in range(wf, wl + 1) if w * N // W != (w + 1) * N // W}
-                assert writers == used
-                assert all(slots[r * Hv + vg + w] == (r, vg) for w in used)
+        if nb == 0:
+            continue
+        a = int(prefix[r])
+        cf, cl = owner(a, N, C), owner(a + nb - 1, N, C)
+        writers = {seen[(r, b)] for b in range(nb)}
+        if cf == cl:
+            assert writers == {cf}
+        else:
+            # the combine skips CTAs whose range is empty
+            used = {c for c in range(cf, cl + 1) if c * N // C != (c + 1) * N // C}
+            assert writers == used
+            for vg in range(V):
+                assert all(slots[(r + c) * V + vg] == (r, vg) for c in used)
 
 
 @pytest.mark.parametrize("D,GW", [(64, 1), (64, 2), (64, 4), (128, 1), (128, 2), (128, 4)])
@@ -172,42 +172,36 @@ def test_select_free_reduce_scatter_with_permuted_lanes(D, GW):
             assert abs(v[lane, i] - logical[group, M + i].sum()) < 1e-9
 
 
-def pair_at(x, prefix, Hv):
-    """(request, virtual head) holding stream position x."""
-    u = x // Hv
-    r = max(i for i in range(len(prefix) - 1) if prefix[i] <= u)
-    nb = int(prefix[r + 1] - prefix[r])
-    return r, (x - Hv * int(prefix[r])) // nb
+def request_at(x, prefix):
+    """Request holding stream position x."""
+    return max(i for i in range(len(prefix) - 1) if prefix[i] <= x and prefix[i + 1] > x)
 
 
 @pytest.mark.parametrize("trial", range(60))
-def test_each_split_pair_is_combined_by_exactly_one_boundary(trial):
-    """Boundary warp w (1 <= w < W) reads the pair holding start(w) (empty
-    ranges included) and combines it iff the pair's first block belongs to
-    warp w - 1."""
+def test_each_split_request_is_combined_by_exactly_one_boundary(trial):
+    """Boundary CTA c (1 <= c < C) reads the request holding start(c) (empty
+    ranges included) and combines it iff the request's first chunk belongs
+    to CTA c - 1."""
     rng = np.random.default_rng(1000 + trial)
     R = int(rng.integers(1, 10))
     nblk = rng.integers(0, 25, size=R)
     if nblk.sum() == 0:
         nblk[-1] = 2
-    Hv = int(rng.choice([1, 2, 4, 8]))
-    W = int(rng.integers(1, 400))
+    C = int(rng.integers(1, 400))
     prefix = np.concatenate([[0], np.cumsum(nblk)]).astype(np.int64)
-    N = Hv * int(prefix[-1])
+    N = int(prefix[-1])
     claimed = {}
-    for w in range(1, W):
-        x = w * N // W
+    for c in range(1, C):
+        x = c * N // C
         if x >= N:
             continue
-        r, vg = pair_at(x, prefix, Hv)
-        nb = int(prefix[r + 1] - prefix[r])
-        a = Hv * int(prefix[r]) + vg * nb
-        if owner(a, N, W) == w - 1:
-            assert (r, vg) not in claimed
-            claimed[(r, vg)] = w
+        r = request_at(x, prefix)
+        if owner(int(prefix[r]), N, C) == c - 1:
+            assert r not in claimed
+            claimed[r] = c
     for r in range(R):
         nb = int(prefix[r + 1] - prefix[r])
-        for vg in range(Hv if nb else 0):
-            a = Hv * int(prefix[r]) + vg * nb
-            split = owner(a, N, W) != owner(a + nb - 1, N, W)
-            assert ((r, vg) in claimed) == split
+        if nb == 0:
+            continue
+        split = owner(int(prefix[r]), N, C) != owner(int(prefix[r]) + nb - 1, N, C)
+        assert (r in claimed) == split

@@ -28,8 +28,8 @@ def _clear_errors():
     yield
 
 
-def run_and_check(step, decode_warps=None, rows=None, check_pool=True):
-    ds = DeviceStep(step, decode_warps=decode_warps)
+def run_and_check(step, decode_splits=None, rows=None, check_pool=True):
+    ds = DeviceStep(step, decode_splits=decode_splits)
     ds.run()
     torch.cuda.synchronize()
     assert binding.pkv_get_device_errors(clear=True) == 0
@@ -85,12 +85,12 @@ def test_mixed_step_parity():
 
 
 # ---------------------------------------------------------------- split-KV
-@pytest.mark.parametrize("warps", [1, 3, 7, 64, 1000, 5000])
-def test_split_kv_partitionings(warps):
+@pytest.mark.parametrize("splits", [1, 3, 7, 64, 1000, 5000])
+def test_split_kv_partitionings(splits):
     step = make_step([RequestSpec(L - 1, 1) for L in (1, 2, 15, 16, 17, 33, 100, 257, 1000,
                                                        3001)],
-                     num_q_heads=8, num_kv_heads=2, head_dim=128, seed=40 + warps)
-    run_and_check(step, decode_warps=warps)
+                     num_q_heads=8, num_kv_heads=2, head_dim=128, seed=40 + splits)
+    run_and_check(step, decode_splits=splits)
 
 
 @pytest.mark.parametrize("Hq,Hkv,D", [(4, 4, 128), (8, 4, 128), (16, 4, 128), (32, 4, 128),
@@ -102,7 +102,7 @@ def test_decode_head_shapes(Hq, Hkv, D):
     step = make_step([RequestSpec(int(L) - 1, 1) for L in lens], num_q_heads=Hq,
                      num_kv_heads=Hkv, head_dim=D, seed=int(Hq + D))
     run_and_check(step)
-    run_and_check(step, decode_warps=37)
+    run_and_check(step, decode_splits=37)
 
 
 def test_decode_shuffled_order_same_rows():
@@ -110,7 +110,7 @@ def test_decode_shuffled_order_same_rows():
     lens = rng.integers(20, 900, size=17)
     specs = [RequestSpec(int(L) - 1, 1) for L in lens]
     a = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=9)
-    run_and_check(a, decode_warps=50)
+    run_and_check(a, decode_splits=50)
 
 
 def test_padding_rows_and_empty_requests():
@@ -257,7 +257,7 @@ def test_mixed_batch_order_independence():
     step = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=61)
     run_and_check(step)
     rev = make_step(specs[::-1], num_q_heads=32, num_kv_heads=8, head_dim=128, seed=61)
-    run_and_check(rev, decode_warps=9)
+    run_and_check(rev, decode_splits=9)
 
 
 # ---------------------------------------------------------------- block sizes
@@ -277,7 +277,7 @@ def test_block_sizes_mixed_step(B, Hq, Hkv, D):
     step = make_step(BLOCK_SPECS, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=B,
                      seed=B * 10 + Hq + D)
     run_and_check(step)
-    run_and_check(step, decode_warps=29)
+    run_and_check(step, decode_splits=29)
 
 
 @pytest.mark.parametrize("B", [8, 16, 32])
@@ -433,6 +433,6 @@ def test_seeded_fuzz(trial):
         specs.append(RequestSpec(10, 1))
     step = make_step(specs, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=B,
                      seed=trial)
-    warps = None if trial % 3 == 0 else int(rng.integers(1, 3000))
+    splits = None if trial % 3 == 0 else int(rng.integers(1, 3000))
     rows = rng.choice(step.num_tokens, size=min(step.num_tokens, 400), replace=False)
-    run_and_check(step, decode_warps=warps, rows=np.sort(rows))
+    run_and_check(step, decode_splits=splits, rows=np.sort(rows))
