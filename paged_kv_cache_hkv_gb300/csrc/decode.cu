@@ -667,12 +667,14 @@ __global__ void __launch_bounds__(GW * 32) combine_kernel(const DecodeParams p) 
     const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
     Ls += wgt * ml.y;
     const int cnt = min(32, npieces - j0);
-#pragma unroll 4
+    // 8 pieces' loads in flight per lane; a piece of weight 0 (an empty
+    // range, which wrote no partial) reads piece 0's slot and adds nothing
+#pragma unroll 8
     for (int j = 0; j < cnt; ++j) {
       const float wj = __shfl_sync(0xffffffffu, wgt, j);
-      if (wj == 0.f) continue;
+      const long long jj = wj == 0.f ? 0 : j0 + j;
       const float* src =
-          p.part_o + (((r + cf + j0 + j) * p.virt_heads + vg) * GW + h) * D + lane * E;
+          p.part_o + (((r + cf + jj) * p.virt_heads + vg) * GW + h) * D + lane * E;
       if constexpr (E == 4) {
         const float4 v = *reinterpret_cast<const float4*>(src);
         acc[0] += wj * v.x;
