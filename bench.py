@@ -92,19 +92,32 @@ L2_BYTES = 129 * 2 ** 20  # GB300 L2
 def step_work(step):
     """Algorithmic bytes and flops of one step.
 
-    decode_kv_bytes: K and V rows each decode row reads once (L * Hkv * D * 2
-    bytes each); prefill_flops: 4 * D * Hq per causal (query, key) pair
-    (QK^T and PV); write_bytes: each new token's K and V rows read and
-    written."""
+    decode_kv_bytes: the K and V rows the decode rows read, each physical
+    block once (a block shared by several requests counts the most tokens
+    any of them keeps in it; Hkv * D * 2 bytes per row); that is the least
+    the decode must bring from memory. decode_kv_logical_bytes: the same
+    per request (L * Hkv * D * 2 * 2 each), shared blocks once per reader.
+    prefill_flops: 4 * D * Hq per causal (query, key) pair (QK^T and PV);
+    write_bytes: each new token's K and V rows read and written."""
     D, Hq, Hkv = step.head_dim, step.num_q_heads, step.num_kv_heads
     dec = step.query_len == 1
-    decode_kv = int(step.seq_lens[dec].astype(np.int64).sum()) * Hkv * D * 2 * 2
+    row = Hkv * D * 2 * 2
+    decode_logical = int(step.seq_lens[dec].astype(np.int64).sum()) * row
+    B = step.block_size
+    fill = {}
+    for r in np.flatnonzero(dec):
+        L = int(step.seq_lens[r])
+        for j in range(-(-L // B)):
+            blk = int(step.block_table[r, j])
+            fill[blk] = max(fill.get(blk, 0), min(B, L - j * B))
+    decode_kv = sum(fill.values()) * row
     pairs = 0
     for c, n in zip(step.num_computed[~dec], step.query_len[~dec]):
         c, n = int(c), int(n)
         pairs += n * c + n * (n + 1) // 2
     return {
         "decode_kv_bytes": decode_kv,
+        "decode_kv_logical_bytes": decode_logical,
         # bytes a step touches at least once: the K/V of every allocated block
         # slot (a shared prefix once), q and out rows
         "touched_bytes": (block_tradeoff(step)["slots_allocated"] * Hkv * D * 2 * 2
@@ -520,6 +533,7 @@ def run_native(args):
                    "heads": f"{step.num_q_heads}q/{step.num_kv_heads}kv", "head_dim": step.head_dim,
                    "block_size": step.block_size, "pool_blocks": step.num_blocks,
                    "decode_kv_bytes_per_step": work["decode_kv_bytes"],
+                   "decode_kv_logical_bytes_per_step": work["decode_kv_logical_bytes"],
                    "prefill_flops_per_step": work["prefill_flops"],
                    "l2": ("inputs larger than L2 (no flush)" if work["touched_bytes"] > L2_BYTES
                           else "inputs fit in L2 (no flush: L2-warm timings)"),
@@ -530,6 +544,10 @@ def run_native(args):
         # the same bytes over decode + combine time (both kernels of split-KV)
         "decode_combine_kv_read_gbs": (work["decode_kv_bytes"] / ((per_kernel[2] + per_kernel[3]) * 1e-3)
                                        / 1e9 if per_kernel[2] > 0 else None),
+        # K/V rows as the requests see them (a shared block once per reader):
+        # differs from decode_kv_read_gbs only when decode rows share blocks
+        "decode_kv_logical_gbs": (work["decode_kv_logical_bytes"] / (dec_ms * 1e-3) / 1e9
+                                  if dec_ms > 0 else None),
         # cache write: each new token's K and V rows read and written
         "kv_write": {"us": write_ms * 1e3,
                      "gbs": work["write_bytes"] / (write_ms * 1e-3) / 1e9 if write_ms > 0 else None},

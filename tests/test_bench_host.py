@@ -50,3 +50,23 @@ def test_step_work_bytes_do_not_depend_on_block_size():
     assert works[0] == works[1] == works[2]
     assert works[0]["decode_kv_bytes"] == 100 * 2 * 128 * 2 * 2
     assert works[0]["prefill_flops"] == 4 * 128 * 8 * (30 * 20 + 30 * 31 // 2)
+
+
+def test_decode_bytes_count_a_shared_block_once():
+    # two decodes over one shared 32-token prefix (2 blocks of 16), each with
+    # 5 private tokens in a block of its own: 32 + 2 * 5 unique tokens
+    specs = [RequestSpec(36, 1, shares_prefix=True), RequestSpec(36, 1, shares_prefix=True)]
+    step = make_step(specs, num_q_heads=4, num_kv_heads=2, head_dim=64, prefix_tokens=32,
+                     seed=2, materialize=False)
+    w = bench.step_work(step)
+    row = 2 * 64 * 2 * 2
+    assert w["decode_kv_bytes"] == (32 + 2 * 5) * row
+    assert w["decode_kv_logical_bytes"] == 2 * 37 * row
+
+
+def test_decode_bytes_without_sharing_equal_the_logical_bytes():
+    specs = [RequestSpec(L - 1, 1) for L in (1, 15, 16, 17, 100)]
+    step = make_step(specs, num_q_heads=8, num_kv_heads=2, head_dim=128, seed=4,
+                     materialize=False)
+    w = bench.step_work(step)
+    assert w["decode_kv_bytes"] == w["decode_kv_logical_bytes"] == (1 + 15 + 16 + 17 + 100) * 2 * 128 * 4
