@@ -165,18 +165,6 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&v)[32]) {
 
 }  // namespace tc
 
-// OR of `v` over the 256 softmax threads (named barrier 1): every thread gets
-// the same answer.
-__device__ __forceinline__ bool softmax_any(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v))
-      : "memory");
-  return r != 0;
-}
 
 constexpr int kTileM = 128;    // query rows (query x head) per tile
 constexpr int kTileN = 128;    // keys per tile (8 chunks of 16)
@@ -231,8 +219,10 @@ struct PrefillShared {
   uint64_t v_free[kVStages];     // commit: the PV that read the V slot is done
   uint64_t s_full[2];            // commit: S of warpgroup w in TMEM
   uint64_t p_ready[2];           // 128 arrivals: P of warpgroup w in TMEM, O rescaled, V cleaned
-  uint64_t o_full;               // commit: every PV of the item done
-  uint64_t o_free;               // 256 arrivals: both warpgroups have read O and the (m, l) pairs
+  uint64_t o_full[2];            // commit: the item's last PV into O_w done
+  uint64_t o_free[2];            // 256 arrivals: O_w of its item read (a warpgroup that
+                                 // finishes an item alone arrives twice per thread)
+  uint64_t ml_full[2];           // 256 arrivals: both (m, l) of a merged item published
   uint64_t drain;
   uint64_t iq_full[kItemQ];      // item id j published in item_q[j % kItemQ]
   uint64_t iq_free[kItemQ];      // 10 arrivals: every role has read it
@@ -358,10 +348,14 @@ __device__ __forceinline__ bool chunk_ok(const PrefillParams& p, const PrefillIt
 //            O_w += P_w V with P_w read from TMEM, where softmax w wrote it
 //            over S_w (bf16 pairs, one pair per 32-bit column). MMAs run in
 //            issue order, so S(kt+2) overwrites P_w only after PV(kt) read it.
-//   warpgroups 0 and 1: softmax of tiles w, w+2, ... with their own running
-//            max and sum and their own O_w at TMEM columns [256w+128, 256w+128+D);
-//            at the end of the item the two partials are merged (log-sum-exp)
-//            and each warpgroup writes half of the output columns.
+//   warpgroups 0 and 1: tile number T of the CTA (counting every item's
+//            tiles) belongs to warpgroup T & 1. A warpgroup keeps its own
+//            running max and sum and its own O_w at TMEM columns
+//            [256w+128, 256w+128+D). An item of one tile is finished by its
+//            warpgroup alone, so consecutive one-tile items run on both
+//            warpgroups at once; an item of several tiles ends with the two
+//            partials merged (log-sum-exp), each warpgroup writing half of
+//            the output columns.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
@@ -392,8 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_ready[i], 128);
     }
-    mbar_init(&sh.o_full, 1);
-    mbar_init(&sh.o_free, 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.o_full[i], 1);
+      mbar_init(&sh.o_free[i], 256);
+      mbar_init(&sh.ml_full[i], 256);
+    }
     mbar_init(&sh.drain, 1);
     for (int i = 0; i < kItemQ; ++i) {
       mbar_init(&sh.iq_full[i], 1);
@@ -550,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((tid & 31) == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16(kTileM, kTileN, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(kTileM, D, 1);
-      uint32_t T = 0, np[2] = {0, 0};
+      // uses[w]: items so far whose PV wrote O_w
+      uint32_t T = 0, np[2] = {0, 0}, uses[2] = {0, 0};
       bool ok = true;
       for (int it = 0; ok; ++it) {
         const int item = take_item(sh, it, abort_flag, false);
@@ -558,8 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok || !valid(item)) break;
         const PrefillItem m = prefill_item(p, n_req, item, QT, meta, meta_prefix);
         const int nkv = m.nkv;
+        const int rot = static_cast<int>(T & 1u);  // tile kt goes to warpgroup (kt + rot) & 1
         auto issue_s = [&](int kt) -> bool {  // S_w = Q K^T for tile kt
-          const int w = kt & 1;
+          const int w = (kt + rot) & 1;
           const uint32_t Tk = T + kt;
           const int slot = static_cast<int>(Tk % kKStages);
           if (!wait_or_abort(&sh.k_full[slot], (Tk / kKStages) & 1u, abort_flag)) return false;
@@ -577,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         auto issue_pv = [&](int kt) -> bool {  // O_w += P_w V for tile kt, P_w from TMEM
-          const int w = kt & 1;
+          const int w = (kt + rot) & 1;
           const uint32_t Tv = T + kt;
           const int slot = static_cast<int>(Tv % kVStages);
           if (!wait_or_abort(&sh.v_full[slot], (Tv / kVStages) & 1u, abort_flag)) return false;
@@ -590,18 +589,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (kt >= 2 || kk > 0) ? 1u : 0u);
           }
           tc::commit(&sh.v_free[slot]);
-          if (kt == nkv - 1) tc::commit(&sh.o_full);
+          if (kt >= nkv - 2) tc::commit(&sh.o_full[w]);  // the item's last PV into O_w
           return true;
         };
         ok = wait_or_abort(&sh.q_full, it & 1u, abort_flag);
         if (ok) ok = issue_s(0);
         if (ok && nkv > 1) ok = issue_s(1);
         for (int kt = 0; ok && kt < nkv; ++kt) {
-          const int w = kt & 1;
+          const int w = (kt + rot) & 1;
           ok = wait_or_abort(&sh.p_ready[w], np[w] & 1u, abort_flag);
           ++np[w];
-          // the previous item's O must have been read before PV(0) overwrites it
-          if (ok && kt == 0 && it > 0) ok = wait_or_abort(&sh.o_free, (it - 1) & 1u, abort_flag);
+          // the first PV into O_w of the item overwrites it: the last item
+          // that used O_w must have been read
+          if (kt < 2) {
+            if (ok && uses[w] > 0) ok = wait_or_abort(&sh.o_free[w], (uses[w] - 1) & 1u, abort_flag);
+            ++uses[w];
+          }
           if (ok) ok = issue_pv(kt);
           if (ok && kt + 2 < nkv) ok = issue_s(kt + 2);
         }
@@ -620,27 +623,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_base + wg * 256u;  // S_wg, then P_wg
     const uint32_t t_o = t_s + 128u;                     // O_wg
-    uint32_t T = 0, ns = 0;
+    // Tile number T of the CTA (all items) belongs to warpgroup T & 1, so
+    // one-tile items alternate between the warpgroups and each finishes its
+    // own alone; an item of several tiles is split between them and merged.
+    // Both warpgroups walk every item, so they keep the same counts: T,
+    // uses[x] (items whose PV wrote O_x) and mi (merged items).
+    uint32_t T = 0, ns = 0, uses[2] = {0, 0}, mi = 0;
     bool ok = true;
-    // the two warpgroups take every decision to stop together (softmax_any)
-    int item = take_item(sh, 0, abort_flag, true);
-    bool stop = softmax_any(!valid(item));
     // chunk validity of tile kt of item m (lanes 0..7), read one tile ahead
     auto load_ids = [&](const PrefillItem& mm, int kt) -> int {
       return (lane < 8 && kt < mm.nkv && chunk_ok(p, mm, kt, lane)) ? 1 : -1;
     };
+    int item = take_item(sh, 0, abort_flag, true);
     PrefillItem m{};
     int next_id = -1;
-    if (!stop) {
+    if (valid(item)) {
       m = prefill_item(p, n_req, item, QT, meta, meta_prefix);
-      next_id = load_ids(m, wg);
+      next_id = load_ids(m, wg);  // T = 0: this warpgroup's first tile is tile wg
     }
-    for (int it = 0; !stop; ++it) {
+    for (int it = 0; ok && valid(item); ++it) {
       const int nkv = m.nkv;
+      const int rot = static_cast<int>(T & 1u);  // tile kt belongs to warpgroup (kt + rot) & 1
       const int qi = m.i0 + row / G;                    // query of this row
       const int lim = min(m.c + qi, m.kv_len - 1);      // last key this row may see
       float m_run = -INFINITY, l_run = 0.f;
-      for (int kt = wg, nmine = 0; kt < nkv; kt += 2, ++nmine) {
+      for (int kt = (wg - rot) & 1, nmine = 0; kt < nkv; kt += 2, ++nmine) {
         const uint32_t mask = __ballot_sync(0xffffffffu, next_id >= 0) & 0xFFu;
         ok = wait_or_abort(&sh.s_full[wg], ns & 1u, abort_flag);
         ++ns;
@@ -733,64 +740,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh.p_ready[wg]);
         next_id = load_ids(m, kt + 2);  // its latency hides under the next S wait
       }
+      if (!ok) break;
       // ---- the next item's id and metadata, while the last PVs run
-      const int item_n = ok ? take_item(sh, it + 1, abort_flag, true) : -1;
-      if (item_n < 0) ok = false;  // aborted: both warpgroups learn it below
+      const int item_n = take_item(sh, it + 1, abort_flag, true);
+      if (item_n < 0) {  // aborted
+        ok = false;
+        break;
+      }
       PrefillItem m_next{};
       if (valid(item_n)) {
         m_next = prefill_item(p, n_req, item_n, QT, meta, meta_prefix);
-        next_id = load_ids(m_next, wg);  // first tile of the next item
+        // this warpgroup's first tile of the next item
+        next_id = load_ids(m_next, (wg - static_cast<int>((T + nkv) & 1u)) & 1);
       }
-      // ---- merge the two partial results of the item
-      if (ok) ok = wait_or_abort(&sh.o_full, it & 1u, abort_flag);
-      tc::fence_after_sync();
-      float2* ml = reinterpret_cast<float2*>(gbase + Lay::kML) + (it & 1) * 2 * kTileM;
-      ml[wg * kTileM + row] = make_float2(m_run, l_run);
-      // (also the barrier that publishes ml) both warpgroups stop together:
-      // on a failure, or when the next item is the end marker (the same
-      // queue slot for both)
-      const bool failed = softmax_any(!ok || *abort_flag);
-      stop = failed || !valid(item_n);
-      const float2 ml0 = ml[row];
-      const float2 ml1 = ml[kTileM + row];
-      const float M = fmaxf(ml0.x, ml1.x);
-      const float a0 = (ml0.x == -INFINITY) ? 0.f : exp2f(ml0.x - M);
-      const float a1 = (ml1.x == -INFINITY) ? 0.f : exp2f(ml1.x - M);
-      const float inv = 1.f / (ml0.y * a0 + ml1.y * a1);
-      const bool has1 = nkv > 1;
-      const bool store = !failed && qi < m.n;
+      const bool store = qi < m.n;
       uint16_t* dst =
           p.out + (static_cast<long long>(m.q0 + qi) * p.num_q_heads + m.g * G + row % G) * D;
-      const uint32_t t_o0 = tmem + lane_base + 128u, t_o1 = tmem + lane_base + 256u + 128u;
-#pragma unroll 1
-      for (int q = 0; q < D / 32; ++q) {
-        const int col = wg * (D / 2) + q * 16;
-        uint32_t o0[16], o1[16];
-        tc::ld16(t_o0 + col, o0);
-        if (has1) tc::ld16(t_o1 + col, o1);
-        tc::wait16(o0);
-        if (has1) tc::wait16(o1);
-        if (store) {
-          uint32_t w[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float v[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int x = 2 * e + h;
-              v[h] = (__uint_as_float(o0[x]) * a0 + (has1 ? __uint_as_float(o1[x]) * a1 : 0.f)) * inv;
-            }
-            w[e] = pack_bf16x2(v[0], v[1]);
-          }
-          uint4* d4 = reinterpret_cast<uint4*>(dst + col);
-          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      if (nkv > 1) {
+        // ---- merge the two partial results of the item: each warpgroup
+        // writes half of the output columns from both O_0 and O_1
+        ok = wait_or_abort(&sh.o_full[0], uses[0] & 1u, abort_flag) &&
+             wait_or_abort(&sh.o_full[1], uses[1] & 1u, abort_flag);
+        if (!ok) break;
+        tc::fence_after_sync();
+        float2* ml = reinterpret_cast<float2*>(gbase + Lay::kML) + (mi & 1u) * 2 * kTileM;
+        ml[wg * kTileM + row] = make_float2(m_run, l_run);
+        mbar_arrive(&sh.ml_full[mi & 1u]);
+        if (!wait_or_abort(&sh.ml_full[mi & 1u], (mi >> 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
         }
+        const float2 ml0 = ml[row];
+        const float2 ml1 = ml[kTileM + row];
+        const float M = fmaxf(ml0.x, ml1.x);
+        const float a0 = (ml0.x == -INFINITY) ? 0.f : exp2f(ml0.x - M);
+        const float a1 = (ml1.x == -INFINITY) ? 0.f : exp2f(ml1.x - M);
+        const float inv = 1.f / (ml0.y * a0 + ml1.y * a1);
+        const uint32_t t_o0 = tmem + lane_base + 128u, t_o1 = tmem + lane_base + 256u + 128u;
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          const int col = wg * (D / 2) + q * 16;
+          uint32_t o0[16], o1[16];
+          tc::ld16(t_o0 + col, o0);
+          tc::ld16(t_o1 + col, o1);
+          tc::wait16(o0);
+          tc::wait16(o1);
+          if (store) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float v0 = (__uint_as_float(o0[2 * e]) * a0 + __uint_as_float(o1[2 * e]) * a1) * inv;
+              const float v1 =
+                  (__uint_as_float(o0[2 * e + 1]) * a0 + __uint_as_float(o1[2 * e + 1]) * a1) * inv;
+              w[e] = pack_bf16x2(v0, v1);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+        tc::fence_before_sync();
+        mbar_arrive(&sh.o_free[0]);
+        mbar_arrive(&sh.o_free[1]);
+        ++uses[0];
+        ++uses[1];
+        ++mi;
+      } else {
+        // ---- a one-tile item: its warpgroup (rot) writes every column alone
+        if (wg == rot) {
+          if (!wait_or_abort(&sh.o_full[wg], uses[wg] & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const float inv = 1.f / l_run;
+#pragma unroll 1
+          for (int q = 0; q < D / 16; ++q) {
+            uint32_t o[16];
+            tc::ld16(t_o + q * 16, o);
+            tc::wait16(o);
+            if (store) {
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+              uint4* d4 = reinterpret_cast<uint4*>(dst + q * 16);
+              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+          }
+          tc::fence_before_sync();
+          mbar_arrive_n(&sh.o_free[wg], 2);  // the only reader of O_wg: both shares
+        }
+        ++uses[rot];
       }
-      tc::fence_before_sync();
-      mbar_arrive(&sh.o_free);
       T += nkv;
       m = m_next;
+      item = item_n;
     }
   }
 
