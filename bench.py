@@ -300,20 +300,30 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ native arm
+def code_sha256(text):
+    """sha256 of a C/CUDA source's code with comments, indentation and empty
+    lines removed, so that editing a comment does not count as changing the
+    kernel. (The sources put no comment markers inside string literals.)"""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.strip() for ln in text.splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
 def traffic_from_profile(kernel_src):
     """DRAM traffic per launch of the decode kernel from the committed ncu
-    summary, if it was taken on the current source (else None)."""
+    summary, if it was taken on the current code (else None)."""
     path = os.path.join(ROOT, "profiles", "decode_kernel_mixed_step.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m = re.search(r"code_sha256:\s*([0-9a-f]{64})", text)
     t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     if not (m and t):
         return None
-    with open(kernel_src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != m.group(1):
+    with open(kernel_src, encoding="utf-8") as f:
+        if code_sha256(f.read()) != m.group(1):
             return None
     return float(t.group(1))
 

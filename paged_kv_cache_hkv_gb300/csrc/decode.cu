@@ -4,29 +4,30 @@
 // a request with one new token attends every one of its L cached keys, read
 // block by block through its block table without gathering them into a
 // contiguous buffer. GQA: the G = Hq/Hkv q heads of a kv head share every
-// K/V row, so one warp handles all of them (up to 4) and each row is read
-// from HBM once.
+// K/V row, so one warp handles up to 4 of them (a "virtual head") and each
+// row is read from HBM once.
 //
 // Work split (split-KV, "PagedAttention v2" in §4.2 of the first page; the
 // pages only name it): the decode KV stream of the whole step is the
-// sequence of (request, kv head, block) in that order; warp w of W takes the
-// contiguous range [w*N/W, (w+1)*N/W). Every warp streams the same number
-// of blocks whatever the length mix, and a (request, kv head) cut by a range
-// boundary leaves one partial (m, l, o) per warp that touched it; the
-// combine kernel merges those with the usual log-sum-exp rule. A
-// (request, kv head) that falls inside one warp's range is finished there
-// and written straight to the output.
+// sequence of (request, 16-key chunk) in that order; CTA c of C takes the
+// contiguous range [c*N/C, (c+1)*N/C) for a slab of up to 8 virtual heads
+// (whole kv heads; the grid is C x slabs). Every CTA streams the same number
+// of chunks whatever the length mix. A request cut by a range boundary
+// leaves one partial (m, l, o) per CTA that touched it, which the combine
+// kernel merges with the usual log-sum-exp rule; a request that falls
+// inside one CTA's range is finished there and written straight to the
+// output.
 //
 // The unit of the stream is a chunk of 16 keys, whatever the cache's block
 // size B: a 16-token block, half of a 32-token block or two 8-token blocks.
-// Inside a warp: a ring of S shared-memory stages, each holding one chunk's
-// 16 K rows and 16 V rows of one kv head (2*16*D*2 bytes; one 3-D TMA copy
-// for B = 16, where K and V of a block are 32 consecutive pool rows; two of
-// 16 rows for B = 32 (half the K rows, half the V rows) and for B = 8 (the
-// 8 K and 8 V rows of each block)) plus, on the first chunk of a piece, the G
-// query rows (one bulk copy). Lane 0 issues the copies S-1 chunks ahead of
-// the chunk being computed. Online softmax runs in base 2 with q pre-scaled
-// by scale*log2(e).
+// Inside a CTA one producer warp fills a ring of shared-memory stages, each
+// holding one chunk's 16 K rows and 16 V rows of every kv head of the slab:
+// one 3-D TMA copy for B = 16, where K and V of a block are 32 consecutive
+// pool rows; two of 16 rows for B = 32 (half the K rows, half the V rows)
+// and for B = 8 (the 8 K and 8 V rows of each block). On the first chunk of
+// a request it also bulk-copies the slab's query rows. One consumer warp per
+// virtual head reads its kv head's columns of each stage. Online softmax
+// runs in base 2 with q pre-scaled by scale*log2(e).
 #include "common.cuh"
 #include "launch.h"
 
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
   uint64_t* empty = full + S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // no early trigger here: a next kernel's CTAs, resident next to these for
-  // the whole decode while they wait for it, slow the decode warps down
+  // the whole decode while they wait for it, slow the decode down
   pdl_wait();
 
   const long long Cn = p.splits, c = blockIdx.x;

@@ -70,3 +70,19 @@ def test_decode_bytes_without_sharing_equal_the_logical_bytes():
                      materialize=False)
     w = bench.step_work(step)
     assert w["decode_kv_bytes"] == w["decode_kv_logical_bytes"] == (1 + 15 + 16 + 17 + 100) * 2 * 128 * 4
+
+
+def test_code_hash_ignores_comments_but_not_code():
+    src = "int f(int x) {  // add one\n  /* the\n  sum */ return x + 1;\n}\n"
+    same = "// a new note\nint f(int x) {\n\n   return x + 1;   \n}\n"
+    other = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench.code_sha256(src) == bench.code_sha256(same.replace("   return", "  return"))
+    assert bench.code_sha256(src) != bench.code_sha256(other)
+
+
+def test_committed_decode_traffic_matches_the_current_code():
+    """The committed DRAM-traffic summary was taken on the decode kernel's
+    current code (else the bench reports no traffic)."""
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "paged_kv_cache_hkv_gb300", "csrc", "decode.cu")
+    assert bench.traffic_from_profile(src) is not None
