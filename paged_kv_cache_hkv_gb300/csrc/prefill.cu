@@ -770,13 +770,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const float2 ml0 = ml[row];
-        const float2 ml1 = ml[kTileM + row];
+        // the partial of the item's even tiles (warpgroup rot) always comes
+        // first, so the rounding of the merge does not depend on which
+        // warpgroup the schedule gave those tiles: results are the same bits
+        // from run to run
+        const int e = rot;
+        const float2 ml0 = ml[e * kTileM + row];
+        const float2 ml1 = ml[(1 - e) * kTileM + row];
         const float M = fmaxf(ml0.x, ml1.x);
         const float a0 = (ml0.x == -INFINITY) ? 0.f : exp2f(ml0.x - M);
         const float a1 = (ml1.x == -INFINITY) ? 0.f : exp2f(ml1.x - M);
         const float inv = 1.f / (ml0.y * a0 + ml1.y * a1);
-        const uint32_t t_o0 = tmem + lane_base + 128u, t_o1 = tmem + lane_base + 256u + 128u;
+        const uint32_t t_o0 = tmem + lane_base + e * 256u + 128u;
+        const uint32_t t_o1 = tmem + lane_base + (1 - e) * 256u + 128u;
 #pragma unroll 1
         for (int q = 0; q < D / 32; ++q) {
           const int col = wg * (D / 2) + q * 16;
