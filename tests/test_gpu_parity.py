@@ -433,8 +433,9 @@ FUZZ_SHAPES = [(4, 4, 64), (8, 4, 64), (16, 4, 64), (32, 4, 64), (8, 8, 128), (1
 @pytest.mark.parametrize("trial", range(24))
 def test_seeded_fuzz(trial):
     """Random shapes, block sizes, request mixes (decodes, fresh prefills,
-    chunks over a cached prefix, empty requests) and split-KV warp counts;
-    the slots, the whole pool and sampled rows are checked."""
+    chunks over a cached prefix, empty requests) and split-KV CTA counts;
+    the slots, the whole pool and sampled rows are checked, and a second run
+    of the step must give the same bits."""
     rng = np.random.default_rng(9000 + trial)
     Hq, Hkv, D = FUZZ_SHAPES[trial % len(FUZZ_SHAPES)]
     B = int(rng.choice([8, 16, 32]))
@@ -456,3 +457,11 @@ def test_seeded_fuzz(trial):
     splits = None if trial % 3 == 0 else int(rng.integers(1, 3000))
     rows = rng.choice(step.num_tokens, size=min(step.num_tokens, 400), replace=False)
     run_and_check(step, decode_splits=splits, rows=np.sort(rows))
+    # the same step again gives the same bits, whatever the CTAs' schedule
+    ds = DeviceStep(step, decode_splits=splits)
+    outs = []
+    for _ in range(2):
+        ds.run()
+        torch.cuda.synchronize()
+        outs.append(ds.out.clone())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
