@@ -12,8 +12,9 @@
 // tile are the G = Hq/Hkv q heads of one kv head for 128/G consecutive
 // queries, so every K/V tile feeds all G heads (GQA). The item's key tiles
 // (128 keys = 8 chunks of 16 keys: 8 blocks of 16 tokens, 4 of 32 or 16 of
-// 8) are split between two softmax warpgroups: warpgroup w takes tiles w,
-// w+2, ... with its own accumulators (TMEM columns [256w, 256w+128) for S,
+// 8) are split between two softmax warpgroups: tile T of the CTA's tile
+// stream (every item's tiles in order) goes to warpgroup T & 1, which keeps
+// its own accumulators (TMEM columns [256w, 256w+128) for S,
 // [256w+128, 256w+128+D) for O) and its own running max and sum.
 //   S_w = Q K^T      tcgen05.mma M=128 N=128, A = Q (smem), B = K (smem)
 //   O_w += P_w V     tcgen05.mma M=128 N=D, A = P_w (TMEM), B = V (smem)
@@ -23,8 +24,10 @@
 // columns with tcgen05.st. A K-copy warp (3-slot ring) and a V-copy warp
 // (2-slot ring) stream the tiles by TMA (128-byte swizzle, one 16-key chunk
 // of one kv head per copy, two copies of 8 rows for 8-token blocks); one
-// thread issues every MMA. At the end of an item the two partial (max, sum,
-// O) are merged and each warpgroup writes half of the output columns. The
+// thread issues every MMA. An item of one tile is finished by its
+// warpgroup alone; at the end of a longer item the two partial (max, sum, O)
+// are merged (the even tiles' partial first, so the bits do not depend on
+// the schedule) and each warpgroup writes half of the output columns. The
 // CTAs are persistent and take items from a counter; the roles meet only at
 // mbarriers, so consecutive items overlap.
 //
