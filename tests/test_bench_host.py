@@ -86,3 +86,37 @@ def test_committed_decode_traffic_matches_the_current_code():
     src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                        "paged_kv_cache_hkv_gb300", "csrc", "decode.cu")
     assert bench.traffic_from_profile(src) is not None
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(*args):
+    import subprocess
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, timeout=600, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_json_line_with_the_contract_keys():
+    r = _bench("--impl", "reference", "--workload", "tiny_decode", "--steps", "2", "--warmup", "1")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    import json
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["higher_is_better"] is True and d["n_gpus"] == 1 and d["steps"] == 2
+    assert d["value"] > 0 and d["config"]["workload"] == "tiny_decode"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_native_arm_refuses_to_run_without_a_gpu():
+    pytest.importorskip("torch")
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    r = _bench("--workload", "tiny_decode", "--steps", "3", "--warmup", "3")
+    assert r.returncode != 0
+    assert "no CUDA device" in (r.stderr + r.stdout)
