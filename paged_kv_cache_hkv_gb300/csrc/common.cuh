@@ -208,4 +208,25 @@ __device__ __forceinline__ int upper_index(const int32_t* a, int n, long long x)
   return lo;
 }
 
+// The same answer as upper_index, found by a whole warp (every lane gets it):
+// each round the 32 lanes test 32 evenly spaced candidates, so the search
+// takes ceil(log32 n) dependent loads instead of log2 n. The candidates are
+// non-decreasing in the lane and a is non-decreasing, so the lanes whose
+// candidate is <= x form a prefix; the next interval lies between the last
+// of them and the first lane past it.
+__device__ __forceinline__ int warp_upper_index(const int32_t* a, int n, long long x) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = n;  // invariant: a[lo] <= x, answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int idx = lo + static_cast<int>((static_cast<long long>(lane) * (hi - lo)) >> 5);
+    const unsigned le = __ballot_sync(0xffffffffu, static_cast<long long>(__ldg(a + idx)) <= x);
+    const int k = 31 - __clz(le);  // lane 0 (candidate lo) is always in
+    const int idx_k = __shfl_sync(0xffffffffu, idx, k);
+    const int idx_next = __shfl_sync(0xffffffffu, idx, k < 31 ? k + 1 : 31);
+    hi = k < 31 ? idx_next : hi;
+    lo = idx_k;
+  }
+  return lo;
+}
+
 }  // namespace pkv

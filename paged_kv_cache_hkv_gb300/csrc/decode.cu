@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
   // ---------------- locate position x0: (request r, chunk blk)
   int r = -1, blk = 0, nblk = 0;
   if (x0 < N) {
-    r = upper_index(p.dec_prefix, p.num_reqs, x0);
+    r = warp_upper_index(p.dec_prefix, p.num_reqs, x0);
     const int pr = __ldg(p.dec_prefix + r);
     nblk = __ldg(p.dec_prefix + r + 1) - pr;
     blk = static_cast<int>(x0 - pr);
@@ -317,7 +317,24 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const uint64_t l2_policy = l2_evict_first_policy();
     int L = __ldg(p.seq_lens + r), t = __ldg(p.qsl + r);
     int nent = (L + (1 << sh) - 1) >> sh;  // table entries the request uses
+    int pr = __ldg(p.dec_prefix + r);       // stream position of the request's first chunk
     int win_r = -1, win_base = 0, win_val = -1;
+    // The next request's lengths and the first 32 entries of its block table
+    // row, loaded one request ahead: a request boundary then waits on no load.
+    int nx_pn = -1, nx_L = 0, nx_t = 0, nx_win = -1;
+    auto prefetch_next = [&]() {
+      if (r + 1 < p.num_reqs) {
+        nx_pn = __ldg(p.dec_prefix + r + 2);
+        nx_L = __ldg(p.seq_lens + r + 1);
+        nx_t = __ldg(p.qsl + r + 1);
+        nx_win = lane < p.max_blocks
+                     ? __ldg(p.block_table + static_cast<long long>(r + 1) * p.max_blocks + lane)
+                     : -1;
+      } else {
+        nx_pn = -1;
+      }
+    };
+    prefetch_next();
     int out_base = -1;
     bool new_piece = true;
     long long x = x0;
@@ -339,7 +356,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         break;
       }
       if (new_piece) {
-        const long long a = __ldg(p.dec_prefix + r);
+        const long long a = pr;
         const long long cf = owner_cta(a, N, Cn), cl = owner_cta(a + nblk - 1, N, Cn);
         out_base = (cf == cl) ? -1 : static_cast<int>((r + c) * p.virt_heads);
       }
@@ -411,13 +428,26 @@ __global__ void __launch_bounds__(kDecodeThreads)
         blk = 0;
         new_piece = true;
         if (x < x1) {
-          do {
+          pr += nblk;  // empty requests in between add no chunks
+          if (nx_pn - pr > 0) {  // the next request has chunks: its data is here
             ++r;
-            nblk = __ldg(p.dec_prefix + r + 1) - __ldg(p.dec_prefix + r);
-          } while (nblk == 0);
-          L = __ldg(p.seq_lens + r);
-          t = __ldg(p.qsl + r);
-          nent = (L + (1 << sh) - 1) >> sh;
+            nblk = nx_pn - pr;
+            L = nx_L;
+            t = nx_t;
+            nent = (L + (1 << sh) - 1) >> sh;
+            win_r = r;
+            win_base = 0;
+            win_val = lane < nent ? nx_win : -1;
+          } else {
+            do {
+              ++r;
+              nblk = __ldg(p.dec_prefix + r + 1) - __ldg(p.dec_prefix + r);
+            } while (nblk == 0);
+            L = __ldg(p.seq_lens + r);
+            t = __ldg(p.qsl + r);
+            nent = (L + (1 << sh) - 1) >> sh;
+          }
+          prefetch_next();
         }
       }
     }

@@ -205,3 +205,36 @@ def test_each_split_request_is_combined_by_exactly_one_boundary(trial):
             continue
         split = owner(int(prefix[r]), N, C) != owner(int(prefix[r]) + nb - 1, N, C)
         assert (r in claimed) == split
+
+
+def warp_upper_index(a, n, x):
+    """Host restatement of the decode kernel's warp search: 32 lanes test 32
+    evenly spaced candidates per round; a ballot picks the interval."""
+    lo, hi, rounds = 0, n, 0
+    while hi - lo > 1:
+        idx = [lo + (lane * (hi - lo) >> 5) for lane in range(32)]
+        le = [a[i] <= x for i in idx]
+        k = max(lane for lane in range(32) if le[lane])
+        assert all(le[:k + 1]) and not any(le[k + 1:])  # the true lanes form a prefix
+        hi = idx[k + 1] if k < 31 else hi
+        lo = idx[k]
+        rounds += 1
+    return lo, rounds
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_warp_search_equals_bisection(seed):
+    import bisect
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 5000))
+    # chunk counts per request, many zero (requests with no decode chunks)
+    counts = rng.integers(0, 5, size=n) * (rng.random(n) < 0.7)
+    counts[rng.integers(0, n)] += 1  # at least one chunk
+    a = np.concatenate([[0], np.cumsum(counts)]).tolist()
+    N = a[n]
+    for x in sorted(set([0, N - 1] + rng.integers(0, N, size=50).tolist())):
+        got, rounds = warp_upper_index(a, n, x)
+        want = bisect.bisect_right(a, x, 0, n) - 1  # largest r < n with a[r] <= x
+        assert got == want
+        assert a[got] <= x < a[got + 1]  # the request holding position x has chunks
+        assert rounds <= int(np.ceil(np.log(max(n, 2)) / np.log(32))) + 2
