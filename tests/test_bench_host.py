@@ -120,3 +120,17 @@ def test_native_arm_refuses_to_run_without_a_gpu():
     r = _bench("--workload", "tiny_decode", "--steps", "3", "--warmup", "3")
     assert r.returncode != 0
     assert "no CUDA device" in (r.stderr + r.stdout)
+
+
+@pytest.mark.parametrize("clocks,rejected", [
+    ({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}, False),
+    ({"sm_mhz": 1900.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}, False),
+    ({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["hw_slowdown"]}, True),
+    ({"sm_mhz": 1500.0, "sm_max_mhz": 2070.0, "reasons": ["hw_thermal_slowdown"]}, True),
+    ({"sm_mhz": 2000.0, "sm_max_mhz": 2070.0, "reasons": ["sw_thermal_slowdown"]}, True),
+    ({"sm_mhz": 1200.0, "sm_max_mhz": 2070.0, "reasons": []}, True),  # a leftover clock lock
+    ({"sm_mhz": 1950.0, "sm_max_mhz": 2070.0, "reasons": []}, False),
+    ({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}, False),
+])
+def test_clock_rejection_rule(clocks, rejected):
+    assert bench.clocks_rejected(clocks) == rejected
