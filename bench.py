@@ -407,8 +407,8 @@ def timed_region(ds, run_step, K, stream, device_index, sync_all):
     """K timed steps (CUDA events on the launching stream, clocks sampled
     meanwhile), then a separate run of min(K, 100) steps with events recorded
     between the kernels for per-kernel times. Returns the K steps' total ms,
-    ms per launch of (plan, prefill, decode, combine), the cache write's ms
-    per launch and the clock summary."""
+    the median ms per launch of (plan, prefill, decode, combine), the cache
+    write's median ms per launch and the clock summary."""
     import torch
 
     from paged_kv_cache_hkv_gb300 import binding
@@ -451,12 +451,11 @@ def timed_region(ds, run_step, K, stream, device_index, sync_all):
     sync_all()
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_stop)
-    per_kernel = np.zeros(binding.PKV_TRACE_EVENTS - 1)
-    for ev in trace:
-        for i in range(binding.PKV_TRACE_EVENTS - 1):
-            per_kernel[i] += ev[i].elapsed_time(ev[i + 1])
-    per_kernel /= KT  # ms per launch: plan, prefill, decode, combine
-    write_ms = float(np.mean([a.elapsed_time(b) for a, b in write_ev]))
+    # ms per launch, the median over the traced steps: plan, prefill, decode, combine
+    per_kernel = np.median(np.array([[ev[i].elapsed_time(ev[i + 1])
+                                      for i in range(binding.PKV_TRACE_EVENTS - 1)]
+                                     for ev in trace]), axis=0)
+    write_ms = float(np.median([a.elapsed_time(b) for a, b in write_ev]))
     return total_ms, per_kernel, write_ms, clocks
 
 
