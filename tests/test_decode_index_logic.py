@@ -238,3 +238,55 @@ def test_warp_search_equals_bisection(seed):
         assert got == want
         assert a[got] <= x < a[got + 1]  # the request holding position x has chunks
         assert rounds <= int(np.ceil(np.log(max(n, 2)) / np.log(32))) + 2
+
+
+def producer_walk(prefix, n_reqs, x0, x1):
+    """Host restatement of the decode producer's walk over its range
+    [x0, x1): the request at x0 from the warp search, then request by
+    request with the next request's prefix loaded one request ahead; a next
+    request with no chunks falls back to a scan."""
+    r, _ = warp_upper_index(prefix, n_reqs, x0)
+    pr = prefix[r]
+    nblk = prefix[r + 1] - pr
+    blk = x0 - pr
+    nx_pn = prefix[r + 2] if r + 1 < n_reqs else -1
+    out = []
+    x = x0
+    while x < x1:
+        out.append((r, blk))
+        x += 1
+        blk += 1
+        if blk == nblk:
+            blk = 0
+            if x < x1:
+                pr += nblk
+                if nx_pn - pr > 0:  # the lookahead's request has chunks
+                    r += 1
+                    nblk = nx_pn - pr
+                else:
+                    while True:
+                        r += 1
+                        nblk = prefix[r + 1] - prefix[r]
+                        if nblk:
+                            break
+                    assert prefix[r] == pr  # empty requests add no chunks
+                nx_pn = prefix[r + 2] if r + 1 < n_reqs else -1
+    return out
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_producer_walk_with_lookahead_visits_its_range_in_order(seed):
+    rng = np.random.default_rng(500 + seed)
+    n = int(rng.integers(1, 300))
+    counts = rng.integers(0, 6, size=n) * (rng.random(n) < 0.6)  # many empty requests
+    counts[rng.integers(0, n)] += 1
+    prefix = [0] + np.cumsum(counts).tolist()
+    N = prefix[n]
+    want = [(r, b) for r in range(n) for b in range(counts[r])]
+    for C in sorted({1, 2, 3, 7, 152, int(rng.integers(1, 2 * N + 2))}):
+        got = []
+        for c in range(C):
+            x0, x1 = c * N // C, (c + 1) * N // C
+            if x0 < x1:
+                got += producer_walk(prefix, n, x0, x1)
+        assert got == want
