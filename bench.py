@@ -17,7 +17,8 @@ a bounded per-step sample of the same workload instead.
 
 import os
 
-# The CPU oracle runs single-threaded so that its core count is exact.
+# Each oracle process runs numpy single-threaded (one process per host core),
+# so that the core count it reports is exact.
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -37,6 +38,8 @@ sys.path.insert(0, ROOT)
 from paged_kv_cache_hkv_gb300 import synth  # noqa: E402
 
 METRIC = "mixed-step attention tokens/s per layer"
+DEFAULT_SEEDS = {"mixed_step": 3, "prefill_rows": 3, "mixed_step_2048": 3, "tiny_decode": 1,
+                 "llama_decode": 2, "prefix_sharing": 4, "long_context": 5, "long_prefill": 6}
 UNIT = "tokens/s"
 
 
@@ -87,6 +90,7 @@ def whole_job_rate(units_per_rank, world, max_ms_per_step):
 
 # ------------------------------------------------------------------ work
 L2_BYTES = 129 * 2 ** 20  # GB300 L2
+HBM_NOMINAL_GBS = 7900.0  # GB300 HBM3e, nominal
 
 
 def step_work(step):
@@ -223,53 +227,151 @@ def clocks_rejected(clocks):
 
 
 # ------------------------------------------------------------------ oracle timing
-def stratified_sample(step_specs, seed, per_class):
-    """Specs of a bounded sample: rows drawn from each class of request
-    (the long chunk, the fresh prefills, the decodes) and the factor that
-    scales each class's time to the whole step."""
+# Rows of one step the CPU oracle computes per class of request, at most: the
+# mixed step (1280 decodes, one 512-row chunk, 8 x 64 prefill rows) fits in
+# full; larger workloads are sampled.
+ORACLE_ROW_CAP = {"decode": 1280, "chunk": 512, "prefill": 512}
+ORACLE_CLASSES = ("decode", "chunk", "prefill")
+
+
+def request_class(spec):
+    if spec.query_len == 1:
+        return "decode"
+    return "chunk" if spec.num_computed > 0 else "prefill"
+
+
+def oracle_plan(step_specs, seed, caps, workers):
+    """Rows the oracle computes, split over the host workers.
+
+    For each class of request (decodes, chunks over a cached prefix, fresh
+    prefills) every row is taken when the class has at most ``caps[class]``
+    rows, else a seeded sample of that many. Rows go round-robin to the
+    workers; a worker builds every request it holds rows of. Returns
+    {class: (per-worker [(request index, row in request)], total rows of
+    the class, rows taken)}."""
     rng = np.random.default_rng(seed + 1000)
-    classes = {}
-    for i, s in enumerate(step_specs):
-        key = "decode" if s.query_len == 1 else ("chunk" if s.num_computed > 0 else "prefill")
-        classes.setdefault(key, []).append(i)
-    plan = []
-    for key, idx in classes.items():
-        total_rows = sum(step_specs[i].query_len for i in idx)
-        if key == "decode":
-            take = list(rng.choice(idx, size=min(per_class["decode"], len(idx)), replace=False))
-            rows = [(i, 0) for i in take]
-        else:
-            i = int(rng.choice(idx))
-            n = step_specs[i].query_len
-            rr = sorted(rng.choice(n, size=min(per_class[key], n), replace=False))
-            rows = [(i, int(x)) for x in rr]
-        plan.append((key, rows, total_rows / len(rows)))
+    plan = {}
+    for key in ORACLE_CLASSES:
+        pairs = [(i, j) for i, sp in enumerate(step_specs) if request_class(sp) == key
+                 for j in range(sp.query_len)]
+        if not pairs:
+            continue
+        take = pairs
+        if len(pairs) > caps[key]:
+            idx = np.sort(rng.choice(len(pairs), size=caps[key], replace=False))
+            take = [pairs[k] for k in idx]
+        per = [take[w::workers] for w in range(workers)]
+        plan[key] = (per, len(pairs), len(take))
     return plan
 
 
-def time_oracle_sample(step_specs, shape, seed, per_class):
-    """Time the oracle (slot mapping, write, attention) on a stratified
-    sample; returns (estimated seconds for the whole step, description)."""
+def _oracle_worker(conn):
+    """One host process of the oracle timing. It builds its share of the
+    requests when told to ("build"), then runs the oracle on them each time
+    it is told to ("run"); the parent times each run over all workers."""
     import oracle
-    plan = stratified_sample(step_specs, seed, per_class)
-    total = 0.0
-    desc = []
-    for key, rows, scale in plan:
-        reqs = sorted({i for i, _ in rows})
-        sub_specs = [step_specs[i] for i in reqs]
-        sub = synth.make_step(sub_specs, seed=seed, **shape)
-        pos = {i: k for k, i in enumerate(reqs)}
-        sel = [int(sub.query_start_loc[pos[i]]) + j for i, j in rows]
+    built = {}
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            conn.close()
+            return
+        op, arg = msg
+        if op == "build":
+            built = {}
+            for key, specs, rows, shape, seed in arg:
+                reqs = sorted({i for i, _ in rows})
+                if not reqs:
+                    continue
+                pos = {i: k for k, i in enumerate(reqs)}
+                sub = synth.make_step([specs[i] for i in reqs], seed=seed, **shape)
+                sel = [int(sub.query_start_loc[pos[i]]) + j for i, j in rows]
+                built[key] = (sub, sel)
+            conn.send("ready")
+        elif op == "run":
+            item = built.get(arg)
+            if item is not None:
+                sub, sel = item
+                slots = oracle.slot_mapping(sub.block_table, sub.query_start_loc,
+                                            sub.num_computed, sub.block_size)
+                pool = oracle.kv_write(sub.kv_cache, sub.k, sub.v, slots)
+                oracle.paged_attention(sub.q, pool, sub.block_table, sub.seq_lens,
+                                       sub.query_start_loc, sub.num_computed, sub.scale,
+                                       rows=sel)
+            conn.send("done")
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - non-Linux hosts
+        return os.cpu_count() or 1
+
+
+class OracleTimer:
+    """The CPU oracle on every host core: one spawned process per core
+    (numpy single-threaded in each), fed one step's rows by oracle_plan.
+    ``time_step`` runs the step's classes one after another, each as one
+    wall-clock region over all workers, and scales each class to its full
+    row count."""
+
+    def __init__(self, step_specs, shape, seed, caps=ORACLE_ROW_CAP, workers=None):
+        import multiprocessing as mp
+        self.workers = workers or host_cores()
+        self.plan = oracle_plan(step_specs, seed, caps, self.workers)
+        ctx = mp.get_context("spawn")  # no fork after CUDA is up
+        self.conns, self.procs = [], []
+        for _ in range(self.workers):
+            a, b = ctx.Pipe()
+            proc = ctx.Process(target=_oracle_worker, args=(b,), daemon=True)
+            proc.start()
+            self.conns.append(a)
+            self.procs.append(proc)
+        for w, conn in enumerate(self.conns):
+            conn.send(("build", [(key, step_specs, per[w], shape, seed)
+                                 for key, (per, _, _) in self.plan.items()]))
+        for conn in self.conns:
+            if conn.recv() != "ready":
+                raise RuntimeError("oracle worker failed to build its inputs")
+
+    def _run(self, key):
         t0 = time.perf_counter()
-        slots = oracle.slot_mapping(sub.block_table, sub.query_start_loc, sub.num_computed,
-                                    sub.block_size)
-        pool = oracle.kv_write(sub.kv_cache, sub.k, sub.v, slots)
-        oracle.paged_attention(sub.q, pool, sub.block_table, sub.seq_lens, sub.query_start_loc,
-                               sub.num_computed, sub.scale, rows=sel)
-        dt = time.perf_counter() - t0
-        total += dt * scale
-        desc.append(f"{len(rows)} {key} rows x{scale:.0f}")
-    return total, "; ".join(desc)
+        for conn in self.conns:
+            conn.send(("run", key))
+        for conn in self.conns:
+            if conn.recv() != "done":
+                raise RuntimeError("oracle worker failed")
+        return time.perf_counter() - t0
+
+    def time_step(self):
+        """(estimated seconds for the whole step, seconds actually timed)."""
+        est = timed = 0.0
+        for key, (_, total, taken) in self.plan.items():
+            dt = self._run(key)
+            timed += dt
+            est += dt * total / taken
+        return est, timed
+
+    @property
+    def full_step(self):
+        return all(total == taken for _, total, taken in self.plan.values())
+
+    def describe(self):
+        parts = []
+        for key, (_, total, taken) in self.plan.items():
+            parts.append(f"{key}: {taken} of {total} rows" if taken < total
+                         else f"{key}: all {total} rows")
+        return (f"{'the whole step' if self.full_step else 'a seeded sample of the step'} "
+                f"({'; '.join(parts)}) on {self.workers} processes, one per host core")
+
+    def close(self):
+        for conn in self.conns:
+            try:
+                conn.send(None)
+            except (BrokenPipeError, OSError):
+                pass
+        for proc in self.procs:
+            proc.join(timeout=10)
 
 
 def shape_of(step):
@@ -279,34 +381,41 @@ def shape_of(step):
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
+    """The CPU oracle as the reference arm: every step is the workload's
+    step (the whole mixed step; larger workloads sampled per class, see
+    ORACLE_ROW_CAP) computed by the oracle on all host cores."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3,
-                                                    "mixed_step_2048": 3,
-                                                    "long_prefill": 6}.get(args.workload, 0)
+    seed = args.seed if args.seed is not None else DEFAULT_SEEDS[args.workload]
     meta = synth.WORKLOADS[args.workload](seed=seed, materialize=False,
                                           block_size=args.block_size)
-    shape = shape_of(meta)
-    per = {"decode": 4, "chunk": 8, "prefill": 4}
-    for w in range(args.warmup):
-        time_oracle_sample(meta.specs, shape, seed + w, per)
-    est = []
-    desc = ""
-    for k in range(args.steps):
-        t, desc = time_oracle_sample(meta.specs, shape, seed + 100 + k, per)
-        est.append(t)
+    timer = OracleTimer(meta.specs, shape_of(meta), seed)
+    try:
+        for _ in range(args.warmup):
+            timer.time_step()
+        est, timed = [], []
+        for _ in range(args.steps):
+            e, t = timer.time_step()
+            est.append(e)
+            timed.append(t)
+    finally:
+        timer.close()
     sec = float(np.mean(est))
     value = meta.num_tokens / sec
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        # the step time is measured when every row of the step runs; for a
+        # sampled workload it is the per-class extrapolation of the timed rows
+        "ms_per_step_is_estimate": not timer.full_step,
+        "sample_ms_per_step_timed": float(np.mean(timed)) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": args.workload, "tokens_per_step": meta.num_tokens,
                    "block_size": args.block_size},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "per step: " + desc + " (step time extrapolated by class)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": timer.workers, "kind": "oracle",
+                         "sample": "per step: " + timer.describe()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -326,20 +435,18 @@ def code_sha256(text):
 
 def traffic_from_profile(kernel_src):
     """DRAM traffic per launch of the decode kernel from the committed ncu
-    summary, if it was taken on the current code (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_kernel_mixed_step.md")
+    figures (profiles/decode_traffic.json), if they were taken on the
+    current code (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     try:
-        text = open(path).read()
-    except OSError:
-        return None
-    m = re.search(r"code_sha256:\s*([0-9a-f]{64})", text)
-    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m and t):
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
     with open(kernel_src, encoding="utf-8") as f:
-        if code_sha256(f.read()) != m.group(1):
+        if code_sha256(f.read()) != rec.get("code_sha256"):
             return None
-    return float(t.group(1))
+    return float(rec["traffic_bytes_per_launch"])
 
 
 def run_e2e(ds, step, work, K, world, pg, sync_all):
@@ -475,12 +582,7 @@ def run_native(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
         pg = dist
 
-    base_seed = args.seed if args.seed is not None else {"mixed_step": 3, "prefill_rows": 3,
-                                                         "mixed_step_2048": 3,
-                                                         "tiny_decode": 1, "llama_decode": 2,
-                                                         "prefix_sharing": 4,
-                                                         "long_context": 5,
-                                                         "long_prefill": 6}[args.workload]
+    base_seed = args.seed if args.seed is not None else DEFAULT_SEEDS[args.workload]
     seed = replica_seed(base_seed, rank)
     step = synth.WORKLOADS[args.workload](seed=seed, block_size=args.block_size)
     ds = DeviceStep(step)
@@ -549,10 +651,15 @@ def run_native(args):
     if args.workload == "mixed_step" and args.block_size == 16 and args.seed is None:
         traffic = traffic_from_profile(os.path.join(ROOT, "paged_kv_cache_hkv_gb300", "csrc",
                                                     "decode.cu"))
+    # The measured peak is a read+write copy; a read-only stream (the decode)
+    # runs a few percent above it, so frac can exceed 1. The chip's nominal
+    # HBM3e bandwidth is given beside it as an upper reference.
     roofline = {"kernel": "decode_kernel", "bound": "hbm", "achieved": dec_gbs,
                 "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
                 "frac": dec_gbs / hbm_peak if dec_gbs else None, "traffic": traffic,
-                "algorithmic_bytes_per_launch": work["decode_kv_bytes"]}
+                "algorithmic_bytes_per_launch": work["decode_kv_bytes"],
+                "peak_nominal": HBM_NOMINAL_GBS,
+                "frac_of_nominal": dec_gbs / HBM_NOMINAL_GBS if dec_gbs else None}
     pf_ms = per_kernel[1]
     tc_peak = float(peaks.get("bf16_tflops", 1900.0))
     prefill = None
@@ -564,10 +671,14 @@ def run_native(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sec, desc = time_oracle_sample(step.specs, shape_of(step), seed,
-                                       {"decode": 64, "chunk": 64, "prefill": 64})
-        cpu = {"value": work["tokens"] / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": desc + "; step time extrapolated by class"}
+        timer = OracleTimer(step.specs, shape_of(step), seed)
+        try:
+            sec, timed = timer.time_step()
+        finally:
+            timer.close()
+        cpu = {"value": work["tokens"] / sec, "unit": UNIT, "cores": timer.workers,
+               "kind": "oracle", "sample": timer.describe(),
+               "seconds_timed": timed, "extrapolated": not timer.full_step}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,

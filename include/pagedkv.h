@@ -126,7 +126,14 @@ const char* pkv_last_cuda_error(void);
  *                     query_start_loc[r+1]; tokens at or past
  *                     query_start_loc[num_reqs] get -1 (padding). A token
  *                     whose table entry is missing or outside the pool gets
- *                     -1 and sets PKV_DEVERR_BLOCK_RANGE / _LENGTHS.
+ *                     -1 and sets PKV_DEVERR_BLOCK_RANGE / _LENGTHS. Every
+ *                     row of a request with inconsistent lengths
+ *                     (query_start_loc[r] < 0, query_start_loc[r+1] <
+ *                     query_start_loc[r] or > num_tokens,
+ *                     num_computed_tokens[r] < 0, or query_start_loc[0] !=
+ *                     0) gets -1 and sets PKV_DEVERR_LENGTHS; so does every
+ *                     row before query_start_loc[0] when that is not 0. No
+ *                     row keeps what the buffer held before the call.
  * block_table         device int32 [num_reqs][max_blocks_per_req], -1 = unused.
  * query_start_loc     device int32 [num_reqs + 1], non-decreasing, [0] = 0.
  * num_computed_tokens device int32 [num_reqs].
@@ -270,7 +277,10 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride,
  *   requests per call on a 152-SM GB300.
  * - First call per device: it looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make this first call
- *   before any stream capture.
+ *   before any stream capture. The address is kept for the life of the
+ *   process: do not call this entry point again on a device after
+ *   cudaDeviceReset (or after its primary context was released and made
+ *   anew), since the library's device memory may then sit elsewhere.
  * - Shared state: every call on a device uses the same array and leaves its
  *   contents behind. Nothing needs to start at zero (each call re-plans the
  *   whole scratch area first). Calls whose kernels overlap on the GPU (on

@@ -39,6 +39,12 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
   const int c = __ldg(num_computed + r);
   if (q0 < 0 || q1 < q0 || q1 > num_tokens || c < 0 || (r == 0 && q0 != 0)) {
     if (lane == 0) atomicOr(&g_errors_kvwrite, kErrLengths);
+    // The request's rows (and, for request 0, every row before it) get -1:
+    // a slot left over in the caller's buffer would otherwise send this
+    // step's K/V into another sequence's block.
+    const int t0 = r == 0 ? 0 : max(q0, 0);
+    const int t1 = min(max(q1, q0), num_tokens);
+    for (int t = t0 + lane; t < t1; t += 32) slots[t] = -1;
     return;
   }
   const long long row = static_cast<long long>(r) * max_blocks;

@@ -166,7 +166,8 @@ def make_step(specs, *, num_q_heads: int, num_kv_heads: int, head_dim: int,
               pool_slack: float = 1.1, seed: int = 0, shuffle_pool: bool = True,
               prefix_tokens: int = 0, table_width: int | None = None,
               materialize: bool = True, scale: float | None = None,
-              chunk_tokens: int = 32768) -> PagedStep:
+              chunk_tokens: int = 32768, key_drift: float = 0.0,
+              spike: float = 0.0) -> PagedStep:
     """Build one step's inputs.
 
     specs: list of RequestSpec, in batch order.
@@ -177,6 +178,19 @@ def make_step(specs, *, num_q_heads: int, num_kv_heads: int, head_dim: int,
         with ``shares_prefix``.
     materialize: also draw the pool contents and Q/K/V (False gives only the
         metadata, for cheap host-side checks).
+    key_drift: value profile with scores that move along the sequence. Every
+        K row (cached and new) at absolute position p gets ``key_drift * p``
+        added to its first head_dim/2 components, and those components of q
+        head h are shifted by +1, 0 or -1 for h % 3 = 0, 1, 2. So the scores
+        of one head in three climb steadily with the key position (the
+        running max of an online softmax keeps moving), one in three stay
+        level and one in three fall.
+    spike: value profile with one key that outweighs all others. For each
+        decode request (one new token) with cached tokens of its own, one
+        cached key near the end of its context (within its last 48 cached
+        positions, outside any shared prefix) is replaced, in every kv head,
+        by ``spike`` times the sum of that kv head's q rows of the request, so
+        its score dwarfs every other score of the request. 0 = off.
     """
     B = block_size
     Hq, Hkv, D = num_q_heads, num_kv_heads, head_dim
@@ -204,7 +218,7 @@ def make_step(specs, *, num_q_heads: int, num_kv_heads: int, head_dim: int,
         raise ValueError(f"pool of {num_blocks} blocks cannot hold {needed}")
 
     ss = np.random.SeedSequence(seed)
-    s_pool, s_prefix, s_hist, s_new = ss.spawn(4)
+    s_pool, s_prefix, s_hist, s_new, s_spike = ss.spawn(5)
     rng_pool = np.random.Generator(np.random.PCG64(s_pool))
     order = rng_pool.permutation(num_blocks) if shuffle_pool else np.arange(num_blocks)
     free = _FreeQueue(order)
@@ -217,7 +231,7 @@ def make_step(specs, *, num_q_heads: int, num_kv_heads: int, head_dim: int,
         shared_blk, shared_off, _ = _walk(shared_list, free, prefix_tokens, B)
 
     tables = []
-    hist_blk, hist_off = [], []
+    hist_blk, hist_off, hist_pos = [], [], []
     new_blk, new_off = [], []
     for s in specs:
         blocks: list = []
@@ -231,6 +245,7 @@ def make_step(specs, *, num_q_heads: int, num_kv_heads: int, head_dim: int,
         nb, no, fill = _walk(blocks, free, s.query_len, B, fill)
         hist_blk.append(hb)
         hist_off.append(ho)
+        hist_pos.append(np.arange(start, s.num_computed, dtype=np.int64))
         new_blk.append(nb)
         new_off.append(no)
         tables.append(blocks)
@@ -297,7 +312,65 @@ def make_step(specs, *, num_q_heads: int, num_kv_heads: int, head_dim: int,
     step.k = f32_to_bf16_bits(rng_new.standard_normal((T, Hkv, D), dtype=np.float32))
     step.v = f32_to_bf16_bits(rng_new.standard_normal((T, Hkv, D), dtype=np.float32))
     step.kv_cache = pool
+    if key_drift:
+        _apply_key_drift(step, key_drift, shared_blk, shared_off, hist_blk, hist_off, hist_pos)
+    if spike:
+        _apply_spike(step, spike, hist_blk, hist_off, hist_pos,
+                     np.random.Generator(np.random.PCG64(s_spike)))
     return step
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact fp32 value of bf16 bit patterns (a bf16 is the top half of an
+    fp32)."""
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _apply_key_drift(step, drift, shared_blk, shared_off, hist_blk, hist_off, hist_pos):
+    """The ``key_drift`` value profile (see make_step)."""
+    D, Hq = step.head_dim, step.num_q_heads
+    half = D // 2
+    pool = step.kv_cache
+
+    def drift_rows(rows_bits, pos):
+        vals = bf16_bits_to_f32(rows_bits[..., :half]) + np.float32(drift) * pos.astype(
+            np.float32).reshape((-1,) + (1,) * (rows_bits.ndim - 1))
+        out = rows_bits.copy()
+        out[..., :half] = f32_to_bf16_bits(vals)
+        return out
+
+    if len(shared_blk):
+        pos = np.arange(len(shared_blk), dtype=np.int64)
+        pool[shared_blk, 0, shared_off] = drift_rows(pool[shared_blk, 0, shared_off], pos)
+    for blk, off, pos in zip(hist_blk, hist_off, hist_pos):
+        if len(blk):
+            pool[blk, 0, off] = drift_rows(pool[blk, 0, off], pos)
+    new_pos = np.concatenate([np.arange(c, c + n, dtype=np.int64) for c, n in
+                              zip(step.num_computed, step.query_len)] + [np.zeros(0, np.int64)])
+    if len(new_pos):
+        step.k = drift_rows(step.k, new_pos)
+    shift = np.array([1.0, 0.0, -1.0], np.float32)[np.arange(Hq) % 3]
+    qv = bf16_bits_to_f32(step.q[..., :half]) + shift[None, :, None]
+    step.q = step.q.copy()
+    step.q[..., :half] = f32_to_bf16_bits(qv)
+    step.meta["key_drift"] = float(drift)
+
+
+def _apply_spike(step, spike, hist_blk, hist_off, hist_pos, rng):
+    """The ``spike`` value profile (see make_step)."""
+    G = step.num_q_heads // step.num_kv_heads
+    placed = {}
+    for r in range(step.num_reqs):
+        if step.query_len[r] != 1 or len(hist_pos[r]) == 0:
+            continue
+        j = len(hist_pos[r]) - 1 - int(rng.integers(0, min(len(hist_pos[r]), 48)))
+        t = int(step.query_start_loc[r])
+        qf = bf16_bits_to_f32(step.q[t]).reshape(step.num_kv_heads, G, step.head_dim)
+        krow = f32_to_bf16_bits(np.float32(spike) * qf.sum(axis=1))
+        step.kv_cache[hist_blk[r][j], 0, hist_off[r][j]] = krow
+        placed[r] = int(hist_pos[r][j])
+    step.meta["spike"] = float(spike)
+    step.meta["spike_pos"] = placed
 
 
 # ---------------------------------------------------------------------------

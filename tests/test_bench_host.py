@@ -134,3 +134,27 @@ def test_native_arm_refuses_to_run_without_a_gpu():
 ])
 def test_clock_rejection_rule(clocks, rejected):
     assert bench.clocks_rejected(clocks) == rejected
+
+
+@pytest.mark.parametrize("workers", [1, 3, 16])
+def test_oracle_plan_takes_every_row_of_the_mixed_step_once(workers):
+    specs = __import__("paged_kv_cache_hkv_gb300.synth", fromlist=["x"]).mixed_step_specs(3)
+    plan = bench.oracle_plan(specs, 3, bench.ORACLE_ROW_CAP, workers)
+    seen = set()
+    for key, (per, total, taken) in plan.items():
+        assert total == taken  # the mixed step is timed whole
+        assert len(per) == workers
+        rows = [r for w in per for r in w]
+        assert len(rows) == len(set(rows)) == total
+        assert all(bench.request_class(specs[i]) == key for i, _ in rows)
+        seen.update(rows)
+    assert len(seen) == sum(s.query_len for s in specs)
+
+
+def test_oracle_plan_samples_a_class_beyond_its_cap():
+    specs = [RequestSpec(6144, 2048) for _ in range(4)]
+    plan = bench.oracle_plan(specs, 6, {"decode": 8, "chunk": 100, "prefill": 8}, 4)
+    per, total, taken = plan["chunk"]
+    assert (total, taken) == (8192, 100)
+    rows = [r for w in per for r in w]
+    assert len(set(rows)) == 100 and max(len(w) for w in per) - min(len(w) for w in per) <= 1

@@ -5,9 +5,12 @@ compared, so untouched slots must be unchanged too); attention must be within
 |gpu - oracle| <= max(2e-2, 1e-2 * |oracle|) per element.
 """
 
+import math
+
 import numpy as np
 import pytest
 
+import rescale_cases
 from parity import assert_close, oracle_step
 
 torch = pytest.importorskip("torch")
@@ -177,6 +180,46 @@ def test_bad_block_id_is_masked_and_flagged():
     # request 1 is untouched by the bad entry of request 0
     _, _, ref = oracle_step(step)
     assert_close(ds.out_host()[1:], ref[1:])
+
+
+def test_rows_of_a_request_with_bad_lengths_get_no_slot():
+    """A request whose lengths are inconsistent gets -1 in every row, so
+    nothing the slot buffer held before the call (here: valid slots of
+    other blocks) can steer this step's K/V into the pool."""
+    specs = [RequestSpec(40, 3), RequestSpec(70, 5), RequestSpec(9, 1)]
+    step = make_step(specs, num_q_heads=8, num_kv_heads=2, head_dim=64, seed=12)
+    ds = DeviceStep(step)
+    before = ds.pool_host()
+    nc = ds.num_computed.clone()
+    nc[1] = -1  # request 1: rows 3..7
+    ds.slot_mapping.copy_(torch.arange(step.num_tokens, dtype=torch.int64, device="cuda") + 16)
+    binding.pkv_slot_mapping(ds.slot_mapping, ds.block_table, ds.query_start_loc, nc,
+                             step.num_blocks, step.block_size)
+    binding.pkv_paged_kv_write(ds.kv_cache, ds.k, ds.v, ds.slot_mapping)
+    assert binding.pkv_get_device_errors(clear=True) & binding.DEVERR_LENGTHS
+    slots = ds.slots_host()
+    ref = oracle_step(step, rows=[])[0]
+    assert (slots[3:8] == -1).all()
+    assert np.array_equal(slots[:3], ref[:3]) and np.array_equal(slots[8:], ref[8:])
+    # the pool holds exactly the other requests' rows
+    kept = ref.copy()
+    kept[3:8] = -1
+    import oracle
+    assert np.array_equal(ds.pool_host(), oracle.kv_write(before, step.k, step.v, kept))
+
+
+def test_rows_before_a_bad_first_request_get_no_slot():
+    specs = [RequestSpec(5, 2), RequestSpec(30, 4)]
+    step = make_step(specs, num_q_heads=8, num_kv_heads=2, head_dim=64, seed=13)
+    ds = DeviceStep(step)
+    qsl = torch.tensor([1, 2, 6], dtype=torch.int32, device="cuda")  # [0] must be 0
+    ds.slot_mapping.fill_(5)
+    binding.pkv_slot_mapping(ds.slot_mapping, ds.block_table, qsl, ds.num_computed,
+                             step.num_blocks, step.block_size)
+    assert binding.pkv_get_device_errors(clear=True) & binding.DEVERR_LENGTHS
+    slots = ds.slots_host()
+    assert (slots[:2] == -1).all()  # request 0 and the row before it
+    assert np.array_equal(slots[2:], oracle_step(step, rows=[])[0][2:])
 
 
 def test_inconsistent_lengths_are_flagged():
@@ -400,6 +443,40 @@ def test_copy_blocks_out_of_range_pair_is_skipped_and_flagged():
     assert np.array_equal(_host_bits(pool), before)
 
 
+# ---------------------------------------------------------------- online-softmax edge paths
+# Inputs whose scores move far along the sequence (raised scale, keys that
+# drift with their position, one dominant key): the decode's per-chunk and
+# the prefill's per-tile lazy rescale of a non-empty partial, alphas and
+# merge weights that underflow to zero, and split-KV pieces of weight zero in
+# the combine (rescale_cases; the CPU restatement of the same update rules
+# runs on the same inputs in test_online_softmax_logic.py).
+@pytest.mark.parametrize("B", [8, 16, 32])
+@pytest.mark.parametrize("name", rescale_cases.DECODE_CASES + rescale_cases.PREFILL_CASES)
+def test_rescale_paths_llama_shape(name, B):
+    step = rescale_cases.case(name, B=B, seed=B)
+    run_and_check(step)
+    run_and_check(step, decode_splits=1)    # whole requests in one CTA
+    run_and_check(step, decode_splits=400)  # pieces of a few chunks each
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(16, 4, 64), (8, 8, 64), (16, 8, 128), (64, 8, 128)])
+@pytest.mark.parametrize("name", rescale_cases.DECODE_CASES + rescale_cases.PREFILL_CASES)
+def test_rescale_paths_head_shapes(name, Hq, Hkv, D):
+    step = rescale_cases.case(name, Hq=Hq, Hkv=Hkv, D=D, seed=Hq + D)
+    run_and_check(step, decode_splits=97)
+
+
+def test_mixed_step_with_raised_scale():
+    """The bench workload at 8/sqrt(d): the 512-token chunk's 15-16 key
+    tiles per item rescale along the way; sampled rows of every class."""
+    step = synth.mixed_step(scale=8 / math.sqrt(128))
+    rng = np.random.default_rng(8)
+    rows = np.sort(np.concatenate([np.arange(0, 1024, 3),
+                                   rng.choice(np.arange(1024, step.num_tokens), 400,
+                                              replace=False)]))
+    run_and_check(step, rows=rows)
+
+
 # ---------------------------------------------------------------- CUDA graphs
 def test_mixed_step_replays_in_a_cuda_graph():
     specs = [RequestSpec(300, 45), RequestSpec(0, 17), RequestSpec(1000, 1), RequestSpec(63, 1),
@@ -417,11 +494,17 @@ def test_mixed_step_replays_in_a_cuda_graph():
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         ds.run()
+    slots, pool, ref = oracle_step(step)
     for _ in range(2):
         ds.out.zero_()
+        ds.slot_mapping.fill_(-7)
         graph.replay()
         torch.cuda.synchronize()
         assert np.array_equal(ds.out_host(), eager)
+        # the replayed step itself against the oracle: slots, pool, output
+        assert np.array_equal(ds.slots_host(), slots)
+        assert np.array_equal(ds.pool_host(), pool)
+        assert_close(ds.out_host(), ref)
     assert binding.pkv_get_device_errors(clear=True) == 0
 
 

@@ -122,6 +122,35 @@ def build_case(rng, lens_q, lens_c, Hq, Hkv, D, NB=64, B=16, shuffle=True):
 
 
 # ---------------------------------------------------------------------------
+# the oracle's input decoder
+# ---------------------------------------------------------------------------
+
+# bfloat16 is the top half of an IEEE-754 binary32: sign, 8 exponent bits, 7
+# fraction bits. Each pattern below is decoded by hand from that definition.
+BF16_LITERALS = [
+    (0x3F80, 1.0),             # exponent 127, fraction 0
+    (0xC020, -2.5),            # sign, exponent 128, fraction 0b0100000 -> -(1 + 1/4) * 2
+    (0x4049, 3.140625),        # exponent 128, fraction 0b1001001 -> (1 + 73/128) * 2
+    (0x0000, 0.0),
+    (0x8000, -0.0),
+    (0x0080, 2.0 ** -126),     # smallest normal
+    (0x0001, 2.0 ** -133),     # smallest subnormal: 2^-126 * 2^-7
+    (0x7F7F, (2 - 2.0 ** -7) * 2.0 ** 127),  # largest finite
+    (0x7F80, math.inf),
+    (0xFF80, -math.inf),
+]
+
+
+def test_bf16_decoder_literal_values():
+    bits = np.array([b for b, _ in BF16_LITERALS], np.uint16)
+    got = oracle.bf16_bits_to_f64(bits)
+    for (b, want), g in zip(BF16_LITERALS, got):
+        assert g == want and math.copysign(1.0, g) == math.copysign(1.0, want), hex(b)
+    nan = oracle.bf16_bits_to_f64(np.array([0x7FC0, 0xFFC1], np.uint16))
+    assert np.isnan(nan).all()
+
+
+# ---------------------------------------------------------------------------
 # slot and block arithmetic
 # ---------------------------------------------------------------------------
 

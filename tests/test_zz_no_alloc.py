@@ -4,9 +4,10 @@ pkv_paged_attention_static_workspace serves callers that cannot allocate
 device memory -- a server whose memory all went to its own allocator and KV
 pool at start-up, a plugin whose host framework forbids raw cudaMalloc, a
 plain C caller with no allocator. It runs the same kernels on a scratch array
-built into the library. This file is collected last so that a failure here
-leaves every other test already run; it passes alone in a fresh process and
-after the rest of the suite.
+built into the library, so its output must be the same bits as the normal
+call's, and both must match the oracle. This file is collected last so that
+a failure here leaves every other test already run; it passes alone in a
+fresh process and after the rest of the suite.
 """
 
 import ctypes
@@ -14,7 +15,7 @@ import ctypes
 import numpy as np
 import pytest
 
-from parity import ABS_TOL, REL_TOL, bits_to_f64
+from parity import assert_close, oracle_step
 
 torch = pytest.importorskip("torch")
 
@@ -24,25 +25,22 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU containers
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 from paged_kv_cache_hkv_gb300 import binding  # noqa: E402
-from paged_kv_cache_hkv_gb300.runner import DeviceStep  # noqa: E402
+from paged_kv_cache_hkv_gb300.runner import DeviceStep, bf16_to_numpy  # noqa: E402
 from paged_kv_cache_hkv_gb300.synth import RequestSpec, make_step  # noqa: E402
 
 
-def _static_call(ds):
+def _static_call(ds, out):
     s = ds.step
-    out = torch.full_like(ds.out, float("nan"))
     binding.pkv_paged_attention_static_workspace(
         out, ds.q, ds.kv_cache, ds.block_table, ds.seq_lens, ds.query_start_loc,
         ds.num_computed, max_query_len=s.max_query_len, max_seq_len=s.max_seq_len,
         scale=s.scale)
     torch.cuda.synchronize()
-    return bits_to_f64(out.view(torch.int16).cpu().numpy().view(np.uint16))
 
 
-def _check_against(ref_bits, got):
-    ref = bits_to_f64(ref_bits)
-    err = np.abs(got - ref)
-    assert (err <= np.maximum(ABS_TOL, REL_TOL * np.abs(ref))).all(), float(np.nanmax(err))
+def _memory():
+    torch.cuda.synchronize()
+    return torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
 
 
 def test_static_workspace_matches_the_workspace_entry_point_twice():
@@ -56,13 +54,29 @@ def test_static_workspace_matches_the_workspace_entry_point_twice():
                   [RequestSpec(20, 30)],
                   num_q_heads=8, num_kv_heads=2, head_dim=64, seed=102),
     ]
+    outs = []
     for step in steps:
         ds = DeviceStep(step)
         ds.run()  # normal entry point with a torch-allocated workspace
         torch.cuda.synchronize()
         ref_bits = ds.out_host().copy()
-        got = _static_call(ds)
-        _check_against(ref_bits, got)
+        out = torch.full_like(ds.out, float("nan"))
+        outs.append((ds, out, ref_bits))
+    # first static call: the library looks up its scratch array's address
+    _static_call(outs[0][0], outs[0][1])
+    for rnd in range(2):  # two calls in a row per step, alternating shapes
+        for ds, out, ref_bits in outs:
+            out.fill_(float("nan"))
+            before = _memory()
+            _static_call(ds, out)
+            # nothing was allocated: neither torch's allocator nor the device
+            assert _memory() == before
+            got = bf16_to_numpy(out)
+            # the same kernels on the same inputs: the same bits
+            assert np.array_equal(got, ref_bits), f"round {rnd}: differs from the workspace call"
+            if rnd == 0:
+                _, _, ref = oracle_step(ds.step)
+                assert_close(got, ref)
     assert binding.pkv_get_device_errors(clear=True) == 0
 
 
