@@ -55,6 +55,9 @@ def parse_args():
                    help="tokens per cache block")
     p.add_argument("--graph", action="store_true",
                    help="time the step as a CUDA graph captured once and replayed")
+    p.add_argument("--shared-prefix", choices=["auto", "off"], default="auto",
+                   help="pass the shared-prefix hint when the workload's sharing requests "
+                        "form one run of decodes (auto), or never (off)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -461,7 +464,7 @@ def run_e2e(ds, step, work, K, world, pg, sync_all):
 
     from paged_kv_cache_hkv_gb300.runner import DeviceStep
 
-    ds2 = DeviceStep(step, upload_pool=False)
+    ds2 = DeviceStep(step, upload_pool=False, shared_prefix=ds.shared_prefix)
     ds2.kv_cache = ds.kv_cache
     sets = [ds, ds2]
     names = ("q", "k", "v", "block_table", "seq_lens", "query_start_loc", "num_computed")
@@ -554,15 +557,29 @@ def timed_region(ds, run_step, K, stream, device_index, sync_all):
         binding.pkv_paged_attention(
             ds.out, ds.q, ds.kv_cache, ds.block_table, ds.seq_lens, ds.query_start_loc,
             ds.num_computed, max_query_len=s.max_query_len, max_seq_len=s.max_seq_len,
-            scale=s.scale, workspace=ds.workspace, trace_events=trace[k])
+            scale=s.scale, workspace=ds.workspace, trace_events=trace[k],
+            shared_prefix=ds.shared_prefix)
     sync_all()
+    # the cache write alone, back to back (each launch rewrites the same rows,
+    # so every one moves the full bytes): its time per launch without the
+    # launch latency that a single bracketed launch carries
+    NW = 50
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    calls = ds.calls()
+    run_step()  # the GPU works on a step while the writes are queued behind it
+    w0.record(stream)
+    for _ in range(NW):
+        calls.write()
+    w1.record(stream)
+    sync_all()
+    write_b2b_ms = w0.elapsed_time(w1) / NW
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_stop)
     # ms per launch, the median over the traced steps: plan, prefill, decode, combine
     per_kernel = np.median(np.array([[ev[i].elapsed_time(ev[i + 1])
                                       for i in range(binding.PKV_TRACE_EVENTS - 1)]
                                      for ev in trace]), axis=0)
-    write_ms = float(np.median([a.elapsed_time(b) for a, b in write_ev]))
+    write_ms = (float(np.median([a.elapsed_time(b) for a, b in write_ev])), write_b2b_ms)
     return total_ms, per_kernel, write_ms, clocks
 
 
@@ -585,7 +602,7 @@ def run_native(args):
     base_seed = args.seed if args.seed is not None else DEFAULT_SEEDS[args.workload]
     seed = replica_seed(base_seed, rank)
     step = synth.WORKLOADS[args.workload](seed=seed, block_size=args.block_size)
-    ds = DeviceStep(step)
+    ds = DeviceStep(step, shared_prefix="auto" if args.shared_prefix == "auto" else None)
     binding.pkv_get_device_errors(clear=True)
     work = step_work(step)
     stream = torch.cuda.current_stream()
@@ -693,6 +710,9 @@ def run_native(args):
                    "prefill_flops_per_step": work["prefill_flops"],
                    "l2": ("inputs larger than L2 (no flush)" if work["touched_bytes"] > L2_BYTES
                           else "inputs fit in L2 (no flush: L2-warm timings)"),
+                   "shared_prefix_hint": (dict(zip(("len", "first_req", "num_reqs"),
+                                                   ds.shared_prefix))
+                                          if ds.shared_prefix else None),
                    "parallelism": f"replicas x{world}",
                    "launch": "cuda graph replay" if args.graph else "direct, programmatic dependent launch"},
         "block_tradeoff": block_tradeoff(step),
@@ -705,10 +725,18 @@ def run_native(args):
         "decode_kv_logical_gbs": (work["decode_kv_logical_bytes"] / (dec_ms * 1e-3) / 1e9
                                   if dec_ms > 0 else None),
         # cache write: each new token's K and V rows read and written
-        "kv_write": {"us": write_ms * 1e3,
-                     "gbs": work["write_bytes"] / (write_ms * 1e-3) / 1e9 if write_ms > 0 else None},
+        "kv_write": {"us": write_ms[0] * 1e3,
+                     "gbs": work["write_bytes"] / (write_ms[0] * 1e-3) / 1e9 if write_ms[0] > 0 else None,
+                     "us_back_to_back": write_ms[1] * 1e3,
+                     "gbs_back_to_back": (work["write_bytes"] / (write_ms[1] * 1e-3) / 1e9
+                                          if write_ms[1] > 0 else None)},
         "kernel_ms": {"plan": per_kernel[0], "prefill": per_kernel[1],
                       "decode": per_kernel[2], "combine": per_kernel[3]},
+        # a step of decodes only: the K/V bytes over every attention kernel
+        # (with a shared-prefix hint the tensor-core kernel attends the shared
+        # keys, the decode kernel the rest)
+        "attention_kv_read_gbs": (work["decode_kv_bytes"] / (sum(per_kernel[1:4]) * 1e-3) / 1e9
+                                  if step.max_query_len == 1 else None),
         "roofline": roofline,
         "prefill_roofline": prefill,
         "cpu_baseline": cpu,

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 /* status codes */
 #define PKV_OK 0
@@ -72,6 +72,10 @@ extern "C" {
                                        max_blocks_per_req blocks                 */
 #define PKV_DEVERR_TIMEOUT 0x8u     /* an on-chip wait (TMA / tensor core) gave
                                        up after its time limit                    */
+#define PKV_DEVERR_SHARED 0x10u     /* the shared-prefix hint of
+                                       pkv_attention_options did not hold for
+                                       some request; it was attended without
+                                       the hint (results unaffected)            */
 
 /* Shape of the physical pool. */
 typedef struct pkv_cache_layout {
@@ -90,7 +94,32 @@ typedef struct pkv_attention_options {
    * ceil(max_seq_len / 16)). A single range means no split at all; tests use
    * other values to vary the partitioning. */
   int32_t decode_splits;
-  int32_t reserved[7]; /* must be zero */
+  /* Shared prefix of a run of decode requests (prefix caching: "vLLM
+   * 架构源码解析（一）" §4.3.1, blocks with ref_cnt > 1 at the head of
+   * several block tables). shared_num_reqs > 0 declares that the requests
+   * shared_first_req .. shared_first_req + shared_num_reqs - 1 are decodes
+   * (one new token each) whose first shared_prefix_len tokens live in the
+   * same physical blocks: block_table[r][j] == block_table[shared_first_req][j]
+   * for j < shared_prefix_len / B. The call then attends those requests'
+   * query rows over the shared prefix once, as one dense tensor-core
+   * contraction (rows = requests x q heads, the prefix's keys read once
+   * per kv head), and each request's decode covers only its own keys past
+   * the prefix, starting from that partial result. The output is the same
+   * attention (shared blocks behave as private copies); only the traffic
+   * changes.
+   *   - shared_prefix_len: tokens, a multiple of 16 and of B, >= 16; 0 =
+   *     off (then the other two fields must be 0).
+   *   - The hint is checked on the device: a request of the run whose
+   *     table does not start with the shared entries, or whose seq_len is
+   *     not above shared_prefix_len, is attended without it; if a request of
+   *     the run has a query_len other than 1 the whole run is. Either sets
+   *     PKV_DEVERR_SHARED. The results stay correct in every case.
+   *   - The workspace grows with shared_num_reqs
+   *     (pkv_attention_workspace_size takes the same options). */
+  int32_t shared_prefix_len;
+  int32_t shared_first_req;
+  int32_t shared_num_reqs;
+  int32_t reserved[4]; /* must be zero */
   /* Tracing: NULL, or PKV_TRACE_EVENTS cudaEvent_t handles (as void*) owned
    * by the caller. The call records them on `stream` around its kernels:
    * [0] before the plan kernel, [1] before the prefill kernel, [2] before

@@ -26,6 +26,7 @@ DEVERR_SLOT_RANGE = 0x1
 DEVERR_BLOCK_RANGE = 0x2
 DEVERR_LENGTHS = 0x4
 DEVERR_TIMEOUT = 0x8
+DEVERR_SHARED = 0x10
 
 
 class pkv_cache_layout(ctypes.Structure):
@@ -37,8 +38,9 @@ PKV_TRACE_EVENTS = 5
 
 
 class pkv_attention_options(ctypes.Structure):
-    _fields_ = [("decode_splits", c_i32), ("reserved", c_i32 * 7),
-                ("trace_events", ctypes.POINTER(c_void_p))]
+    _fields_ = [("decode_splits", c_i32), ("shared_prefix_len", c_i32),
+                ("shared_first_req", c_i32), ("shared_num_reqs", c_i32),
+                ("reserved", c_i32 * 4), ("trace_events", ctypes.POINTER(c_void_p))]
 
 
 _SIGNATURES = {
@@ -182,11 +184,15 @@ def pkv_copy_blocks(dst_pool, src_pool, block_pairs, stream=None):
         _ptr(block_pairs), block_pairs.shape[0], lay, _stream(stream)))
 
 
-def _options(decode_splits, trace_events=None):
-    if decode_splits is None and trace_events is None:
+def _options(decode_splits, trace_events=None, shared_prefix=None):
+    """Options struct (or None for the defaults). shared_prefix: None, or
+    (shared_prefix_len, shared_first_req, shared_num_reqs) -- see pagedkv.h."""
+    if decode_splits is None and trace_events is None and shared_prefix is None:
         return None
     o = pkv_attention_options()
     o.decode_splits = int(decode_splits or 0)
+    if shared_prefix is not None:
+        o.shared_prefix_len, o.shared_first_req, o.shared_num_reqs = (int(x) for x in shared_prefix)
     if trace_events is not None:
         if len(trace_events) != PKV_TRACE_EVENTS:
             raise ValueError(f"trace_events needs {PKV_TRACE_EVENTS} torch.cuda.Event")
@@ -200,11 +206,12 @@ def _options(decode_splits, trace_events=None):
 
 
 def pkv_attention_workspace_size(num_reqs: int, num_q_heads: int, kv_cache,
-                                 decode_splits=None) -> int:
+                                 decode_splits=None, shared_prefix=None) -> int:
     """Workspace bytes for pkv_paged_attention; kv_cache is the pool tensor
     or a pkv_cache_layout."""
     lay = kv_cache if isinstance(kv_cache, pkv_cache_layout) else layout_of(kv_cache)
-    n = load().pkv_attention_workspace_size(num_reqs, num_q_heads, lay, _options(decode_splits))
+    n = load().pkv_attention_workspace_size(num_reqs, num_q_heads, lay,
+                                            _options(decode_splits, None, shared_prefix))
     if n < 0:
         raise PagedKVError("pkv_attention_workspace_size", int(n))
     return int(n)
@@ -213,7 +220,7 @@ def pkv_attention_workspace_size(num_reqs: int, num_q_heads: int, kv_cache,
 def pkv_paged_attention(out, q, kv_cache, block_table, seq_lens, query_start_loc,
                         num_computed_tokens, *, max_query_len: int, max_seq_len: int,
                         scale: float, workspace, decode_splits=None, trace_events=None,
-                        stream=None):
+                        shared_prefix=None, stream=None):
     """out [T, Hq, D] bf16 <- attention of one mixed step (see pagedkv.h).
 
     trace_events: optional list of PKV_TRACE_EVENTS torch.cuda.Event (created
@@ -234,7 +241,7 @@ def pkv_paged_attention(out, q, kv_cache, block_table, seq_lens, query_start_loc
         block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), _ptr(num_computed_tokens),
         seq_lens.shape[0], q.shape[0], int(max_query_len), int(max_seq_len), q.shape[1],
         float(scale), lay, _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _options(decode_splits, trace_events), _stream(stream)))
+        _options(decode_splits, trace_events, shared_prefix), _stream(stream)))
     return out
 
 
@@ -249,7 +256,7 @@ def pkv_get_device_errors(clear: bool = True, stream=None) -> int:
 def pkv_paged_attention_static_workspace(out, q, kv_cache, block_table, seq_lens,
                                          query_start_loc, num_computed_tokens, *,
                                          max_query_len: int, max_seq_len: int, scale: float,
-                                         decode_splits=None, stream=None):
+                                         decode_splits=None, shared_prefix=None, stream=None):
     """pkv_paged_attention without a caller workspace: for callers that cannot
     allocate device memory, the library uses its built-in scratch array (see
     pagedkv.h for the size limit and the one-stream rule)."""
@@ -267,5 +274,81 @@ def pkv_paged_attention_static_workspace(out, q, kv_cache, block_table, seq_lens
         _ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), _ptr(num_computed_tokens),
         seq_lens.shape[0], q.shape[0], int(max_query_len), int(max_seq_len), q.shape[1],
-        float(scale), layout_of(kv_cache), _options(decode_splits), _stream(stream)))
+        float(scale), layout_of(kv_cache), _options(decode_splits, None, shared_prefix),
+        _stream(stream)))
     return out
+
+
+class StepCalls:
+    """The three calls of one step -- pkv_slot_mapping, pkv_paged_kv_write,
+    pkv_paged_attention -- with their arguments checked and marshalled once.
+
+    A serving loop that keeps its step buffers (as DeviceStep does) pays the
+    argument checks and the tensor-to-pointer conversion once, not on every
+    step; ``run`` then makes the three C calls in a row on the given stream.
+    The buffers must stay allocated and keep their shapes while the object is
+    used."""
+
+    def __init__(self, *, slot_mapping, block_table, query_start_loc, num_computed_tokens,
+                 kv_cache, key, value, out, q, seq_lens, max_query_len: int,
+                 max_seq_len: int, scale: float, workspace, decode_splits=None,
+                 shared_prefix=None):
+        _require(slot_mapping, torch.int64, "slot_mapping")
+        for t, n in ((block_table, "block_table"), (query_start_loc, "query_start_loc"),
+                     (num_computed_tokens, "num_computed_tokens"), (seq_lens, "seq_lens")):
+            _require(t, torch.int32, n)
+        for t, n in ((kv_cache, "kv_cache"), (key, "key"), (value, "value"), (out, "out"),
+                     (q, "q")):
+            _require(t, torch.bfloat16, n)
+        for t, n in ((key, "key"), (value, "value"), (q, "q")):
+            if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+                raise ValueError(f"{n} must be [T, H, D] with contiguous rows")
+        if not out.is_contiguous() or not block_table.is_contiguous():
+            raise ValueError("out and block_table must be contiguous")
+        lay = layout_of(kv_cache)
+        self.lib = load()
+        self._opts = _options(decode_splits, None, shared_prefix)
+        self.slot_args = (
+            _ptr(slot_mapping), _ptr(block_table), block_table.shape[1], _ptr(query_start_loc),
+            _ptr(num_computed_tokens), num_computed_tokens.shape[0], slot_mapping.shape[0],
+            lay.num_blocks, lay.block_size)
+        self.write_args = (
+            _ptr(kv_cache), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
+            _ptr(slot_mapping), key.shape[0], lay)
+        self.attn_args = (
+            _ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), _ptr(block_table),
+            block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc),
+            _ptr(num_computed_tokens), seq_lens.shape[0], q.shape[0], int(max_query_len),
+            int(max_seq_len), q.shape[1], float(scale), lay, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), self._opts)
+        # the tensors stay referenced, so their memory stays valid
+        self._keep = (slot_mapping, block_table, query_start_loc, num_computed_tokens,
+                      kv_cache, key, value, out, q, seq_lens, workspace)
+
+    def slot_map(self, stream=None):
+        status = self.lib.pkv_slot_mapping(*self.slot_args, _stream(stream))
+        if status:
+            raise PagedKVError("pkv_slot_mapping", status)
+
+    def write(self, stream=None):
+        status = self.lib.pkv_paged_kv_write(*self.write_args, _stream(stream))
+        if status:
+            raise PagedKVError("pkv_paged_kv_write", status)
+
+    def attend(self, stream=None):
+        status = self.lib.pkv_paged_attention(*self.attn_args, _stream(stream))
+        if status:
+            raise PagedKVError("pkv_paged_attention", status)
+
+    def run(self, stream=None):
+        st = _stream(stream)
+        lib = self.lib
+        status = lib.pkv_slot_mapping(*self.slot_args, st)
+        if status:
+            raise PagedKVError("pkv_slot_mapping", status)
+        status = lib.pkv_paged_kv_write(*self.write_args, st)
+        if status:
+            raise PagedKVError("pkv_paged_kv_write", status)
+        status = lib.pkv_paged_attention(*self.attn_args, st)
+        if status:
+            raise PagedKVError("pkv_paged_attention", status)

@@ -118,11 +118,35 @@ int32_t check_layout(const pkv_cache_layout& l) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-struct WsLayout {
-  size_t hdr, dec_prefix, pf_req, pf_prefix, part_ml, part_o, bound, total;
+// The shared-prefix hint of the options, checked (all zero = off).
+struct SharedHint {
+  int len = 0, first = 0, num = 0, pieces = 0, tpp = 0;
 };
 
-WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long splits) {
+int32_t shared_hint(const pkv_attention_options* opt, const pkv_cache_layout& l, int group,
+                    int num_reqs, int num_sms, SharedHint* h) {
+  *h = SharedHint();
+  if (!opt) return PKV_OK;
+  const int len = opt->shared_prefix_len, first = opt->shared_first_req,
+            num = opt->shared_num_reqs;
+  if (len == 0 && first == 0 && num == 0) return PKV_OK;
+  if (len <= 0 || first < 0 || num < 1) return PKV_ERR_BAD_SHAPE;
+  if (len % 16 || len % l.block_size) return PKV_ERR_BAD_SHAPE;
+  if (static_cast<long long>(first) + num > num_reqs) return PKV_ERR_BAD_SHAPE;
+  h->len = len;
+  h->first = first;
+  h->num = num;
+  pkv::shared_split(num, group, l.num_kv_heads, len, num_sms, &h->pieces, &h->tpp);
+  return PKV_OK;
+}
+
+struct WsLayout {
+  size_t hdr, dec_prefix, pf_req, pf_prefix, part_ml, part_o, bound, casc_use, casc_ml, casc_o,
+      total;
+};
+
+WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long splits,
+                   const SharedHint& sh, int num_q_heads) {
   WsLayout w;
   const long long slots = pkv::decode_partial_slots(num_reqs, virt_heads, splits);
   size_t off = 0;
@@ -133,13 +157,20 @@ WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long
   w.pf_req = off;
   off += round256((num_reqs + 1) * sizeof(int32_t));
   w.pf_prefix = off;
-  off += round256((num_reqs + 1) * sizeof(int32_t));
+  off += round256((num_reqs + 2) * sizeof(int32_t));
   w.part_ml = off;
   off += round256(static_cast<size_t>(slots) * gw * sizeof(float2));
   w.part_o = off;
   off += round256(static_cast<size_t>(slots) * gw * head_dim * sizeof(float));
   w.bound = off;
   off += round256(static_cast<size_t>(splits) * sizeof(int));
+  const size_t shared_rows = static_cast<size_t>(sh.pieces) * sh.num * num_q_heads;
+  w.casc_use = off;
+  off += round256(static_cast<size_t>(sh.num) * sizeof(int32_t));
+  w.casc_ml = off;
+  off += round256(shared_rows * sizeof(float2));
+  w.casc_o = off;
+  off += round256(shared_rows * head_dim * sizeof(float));
   w.total = off;
   return w;
 }
@@ -149,7 +180,7 @@ WsLayout ws_layout(int num_reqs, int virt_heads, int gw, int head_dim, long long
 int32_t decode_splits_for(DeviceInfo* d, int head_dim, int num_kv_heads, int group,
                           int block_size, const pkv_attention_options* opt, long long* splits) {
   if (opt) {
-    for (int i = 0; i < 7; ++i)
+    for (int i = 0; i < 4; ++i)
       if (opt->reserved[i] != 0) return PKV_ERR_BAD_SHAPE;
     if (opt->decode_splits < 0) return PKV_ERR_BAD_SHAPE;
     if (opt->decode_splits > 0) {
@@ -292,9 +323,13 @@ int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
   st = decode_splits_for(d, layout.head_dim, layout.num_kv_heads, group, layout.block_size,
                          options, &splits);
   if (st != PKV_OK) return st;
+  SharedHint sh;
+  st = shared_hint(options, layout, group, num_reqs, d->num_sms, &sh);
+  if (st != PKV_OK) return st;
   const int gw = pkv::decode_heads_per_warp(group);
   const int virt = layout.num_kv_heads * (group / gw);
-  return static_cast<int64_t>(ws_layout(num_reqs, virt, gw, layout.head_dim, splits).total);
+  return static_cast<int64_t>(
+      ws_layout(num_reqs, virt, gw, layout.head_dim, splits, sh, num_q_heads).total);
 }
 
 int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, const void* kv_cache,
@@ -335,9 +370,15 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   st = decode_splits_for(d, layout.head_dim, layout.num_kv_heads, group, layout.block_size,
                          options, &splits);
   if (st != PKV_OK) return st;
+  SharedHint sh;
+  st = shared_hint(options, layout, group, num_reqs, d->num_sms, &sh);
+  if (st != PKV_OK) return st;
+  if (static_cast<long long>(sh.len) >
+      static_cast<long long>(max_blocks_per_req) * layout.block_size)
+    return PKV_ERR_BAD_SHAPE;
   const int gw = pkv::decode_heads_per_warp(group);
   const int virt = layout.num_kv_heads * (group / gw);
-  const WsLayout wl = ws_layout(num_reqs, virt, gw, layout.head_dim, splits);
+  const WsLayout wl = ws_layout(num_reqs, virt, gw, layout.head_dim, splits, sh, num_q_heads);
   if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
   // The decode stream holds at most num_reqs * ceil(max_seq_len / 16)
   // chunks: with the default split, never use more ranges than that (a small
@@ -358,6 +399,9 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   ws.part_ml = reinterpret_cast<float2*>(wsb + wl.part_ml);
   ws.part_o = reinterpret_cast<float*>(wsb + wl.part_o);
   ws.bound = reinterpret_cast<int*>(wsb + wl.bound);
+  ws.casc_use = reinterpret_cast<int32_t*>(wsb + wl.casc_use);
+  ws.casc_ml = reinterpret_cast<float2*>(wsb + wl.casc_ml);
+  ws.casc_o = reinterpret_cast<float*>(wsb + wl.casc_o);
 
   pkv::AttnArgs a;
   a.out = static_cast<uint16_t*>(out);
@@ -379,6 +423,11 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   a.num_blocks = layout.num_blocks;
   a.block_shift = block_shift_of(layout.block_size);
   a.scale = scale;
+  a.shared_len = sh.len;
+  a.shared_first = sh.first;
+  a.shared_num = sh.num;
+  a.shared_pieces = sh.pieces;
+  a.shared_tpp = sh.tpp;
 
   const int D = layout.head_dim, Hkv = layout.num_kv_heads;
   const uint64_t row_bytes = static_cast<uint64_t>(Hkv) * D * 2;
@@ -405,7 +454,7 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   if (e == cudaSuccess) e = pkv::launch_plan(a, ws, s);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
-  if (max_query_len > 1) {
+  if (max_query_len > 1 || sh.num > 0) {
     // pool for the tensor-core path: 64-element (128-byte) swizzled rows,
     // 16 rows per copy (8 for 8-token blocks)
     CUtensorMap kv_map_sw, q_map;

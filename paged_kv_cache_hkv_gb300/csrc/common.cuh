@@ -12,6 +12,7 @@ constexpr uint32_t kErrSlotRange = 0x1u;
 constexpr uint32_t kErrBlockRange = 0x2u;
 constexpr uint32_t kErrLengths = 0x4u;
 constexpr uint32_t kErrTimeout = 0x8u;
+constexpr uint32_t kErrShared = 0x10u;
 
 // The attention kernels move keys in chunks of 16 (one decode stage, one
 // MMA K step). A cache block holds 8, 16 or 32 tokens, so a chunk is two

@@ -28,6 +28,9 @@
 // a request it also bulk-copies the slab's query rows. One consumer warp per
 // virtual head reads its kv head's columns of each stage. Online softmax
 // runs in base 2 with q pre-scaled by scale*log2(e).
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -82,7 +85,10 @@ __device__ __forceinline__ Int3 block_exclusive_scan(Int3 v, Int3* total) {
 }
 
 // Counts of one request: decode 16-key chunks, is-prefill, prefill work items.
-__device__ __forceinline__ Int3 plan_counts(const AttnArgs& a, int r, int tile_q, bool flag) {
+// A decode request that takes its shared prefix from the shared items
+// streams only the chunks past the prefix.
+__device__ __forceinline__ Int3 plan_counts(const AttnArgs& a, const AttnWorkspace& ws, int r,
+                                            int tile_q, bool flag) {
   Int3 v{0, 0, 0};
   const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
   const int n = q1 - q0, L = __ldg(a.seq_lens + r), c = __ldg(a.num_computed + r);
@@ -94,6 +100,9 @@ __device__ __forceinline__ Int3 plan_counts(const AttnArgs& a, int r, int tile_q
     if (flag) atomicOr(&g_errors_decode, kErrLengths);
   } else if (n == 1) {
     v.a = static_cast<int>(nblk);
+    const int i = r - a.shared_first;
+    if (a.shared_num > 0 && i >= 0 && i < a.shared_num && ws.casc_use[i])
+      v.a -= a.shared_len / kChunkKeys;
   } else if (n > 1) {
     v.b = 1;
     v.c = ((n + tile_q - 1) / tile_q) * a.num_kv_heads;
@@ -106,23 +115,91 @@ __device__ __forceinline__ Int3 plan_counts(const AttnArgs& a, int r, int tile_q
 // and after one block scan writes the prefix sums and the compact list of
 // prefill requests. Requests with inconsistent lengths are skipped and
 // flagged.
+// The shared-prefix hint, checked: every request of the run starts as a
+// member; one whose table does not begin with the run's first request's
+// entries, or whose context does not reach past the prefix, drops out (it is
+// attended without the hint); one with other than a single new token turns
+// the whole run off. Returns the number of shared-prefix work items.
+__device__ int plan_shared(const AttnArgs& a, const AttnWorkspace& ws, int tile_q) {
+  __shared__ int run_off, dropped;
+  const int num = a.shared_num;
+  if (threadIdx.x == 0) {
+    run_off = 0;
+    dropped = 0;
+  }
+  for (int i = threadIdx.x; i < num; i += blockDim.x) ws.casc_use[i] = 1;
+  __syncthreads();
+  for (int i = threadIdx.x; i < num; i += blockDim.x) {
+    const int r = a.shared_first + i;
+    if (__ldg(a.qsl + r + 1) - __ldg(a.qsl + r) != 1) run_off = 1;
+    if (__ldg(a.seq_lens + r) <= a.shared_len) {
+      ws.casc_use[i] = 0;
+      dropped = 1;
+    }
+  }
+  // table entries: request i's j-th against the first request's, four
+  // (request, entry group) pairs per thread in flight; groups of 4 entries
+  // (16-byte loads) when the rows allow it
+  const int pb = a.shared_len >> a.block_shift;  // shared table entries
+  const int32_t* row0 = a.block_table + static_cast<long long>(a.shared_first) * a.max_blocks;
+  const bool vec = ((reinterpret_cast<uintptr_t>(row0) & 15u) == 0) && (a.max_blocks % 4 == 0) &&
+                   (pb % 4 == 0);
+  if (vec) {
+    const int pb4 = pb / 4;
+    const long long pairs = static_cast<long long>(num - 1) * pb4;
+    const int4* r0 = reinterpret_cast<const int4*>(row0);
+#pragma unroll 4
+    for (long long x = threadIdx.x; x < pairs; x += blockDim.x) {
+      const int i = 1 + static_cast<int>(x / pb4);
+      const int j = static_cast<int>(x - static_cast<long long>(i - 1) * pb4);
+      const int4 u = __ldg(r0 + static_cast<long long>(i) * (a.max_blocks / 4) + j);
+      const int4 v = __ldg(r0 + j);
+      if (u.x != v.x || u.y != v.y || u.z != v.z || u.w != v.w) {
+        ws.casc_use[i] = 0;
+        dropped = 1;
+      }
+    }
+  } else {
+    const long long pairs = static_cast<long long>(num - 1) * pb;
+#pragma unroll 4
+    for (long long x = threadIdx.x; x < pairs; x += blockDim.x) {
+      const int i = 1 + static_cast<int>(x / pb);
+      const int j = static_cast<int>(x - static_cast<long long>(i - 1) * pb);
+      if (__ldg(row0 + static_cast<long long>(i) * a.max_blocks + j) != __ldg(row0 + j)) {
+        ws.casc_use[i] = 0;
+        dropped = 1;
+      }
+    }
+  }
+  __syncthreads();
+  const bool off = run_off != 0;
+  if (off)
+    for (int i = threadIdx.x; i < num; i += blockDim.x) ws.casc_use[i] = 0;
+  if (threadIdx.x == 0 && (off || dropped)) atomicOr(&g_errors_decode, kErrShared);
+  __syncthreads();
+  if (off) return 0;
+  const int qtiles = (num + tile_q - 1) / tile_q;
+  return qtiles * a.shared_pieces * a.num_kv_heads;
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, AttnWorkspace ws, int tile_q) {
   __shared__ Int3 total;
   pdl_trigger();
   pdl_wait();
+  const int shared_items = a.shared_num > 0 ? plan_shared(a, ws, tile_q) : 0;
   const int R = a.num_reqs;
   const int per = (R + 1023) / 1024;
   const int r0 = min(R, static_cast<int>(threadIdx.x) * per), r1 = min(R, r0 + per);
   Int3 sum{0, 0, 0};
   for (int r = r0; r < r1; ++r) {
-    const Int3 v = plan_counts(a, r, tile_q, true);
+    const Int3 v = plan_counts(a, ws, r, tile_q, true);
     sum.a += v.a;
     sum.b += v.b;
     sum.c += v.c;
   }
   Int3 run = block_exclusive_scan(sum, &total);
   for (int r = r0; r < r1; ++r) {
-    const Int3 v = plan_counts(a, r, tile_q, false);
+    const Int3 v = plan_counts(a, ws, r, tile_q, false);
     ws.dec_prefix[r] = run.a;
     if (v.b) {
       ws.pf_req[run.b] = r;
@@ -134,10 +211,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, AttnWorkspace ws
   }
   if (threadIdx.x == 0) {
     ws.dec_prefix[R] = total.a;
-    ws.pf_prefix[total.b] = total.c;
+    int nreq = total.b, nitems = total.c;
+    if (shared_items > 0) {  // the shared-prefix items come after every prefill request
+      ws.pf_req[nreq] = -1;
+      ws.pf_prefix[nreq] = nitems;
+      nitems += shared_items;
+      ++nreq;
+    }
+    ws.pf_prefix[nreq] = nitems;
     ws.hdr[kHdrDecodeBlocks] = static_cast<uint32_t>(total.a);
-    ws.hdr[kHdrPrefillReqs] = static_cast<uint32_t>(total.b);
-    ws.hdr[kHdrPrefillItems] = static_cast<uint32_t>(total.c);
+    ws.hdr[kHdrPrefillReqs] = static_cast<uint32_t>(nreq);
+    ws.hdr[kHdrPrefillItems] = static_cast<uint32_t>(nitems);
     ws.hdr[kHdrPrefillNext] = 0u;
   }
 }
@@ -174,6 +258,14 @@ struct DecodeParams {
   float2* part_ml;
   float* part_o;
   int* bound;  // [C]: request holding the first position of CTA c's range (-1: none)
+  // Shared prefix: request shared_first + i with shared_use[i] streams only
+  // its chunks from shared_chunks on and always leaves partials; the combine
+  // kernel merges them with the shared items' partials of its row
+  // (shared_pieces of them).
+  int shared_first, shared_num, shared_chunks, shared_pieces;
+  const int32_t* shared_use;
+  const float2* shared_ml;
+  const float* shared_o;
 };
 
 // CTA that owns position x of the decode stream: ranges start at floor(c * N / C).
@@ -315,20 +407,33 @@ __global__ void __launch_bounds__(kDecodeThreads)
     // K/V rows are read once per step: evict them from L2 first, so that the
     // split-KV partials, q rows and tables stay (mixed step: 827 -> 819 us)
     const uint64_t l2_policy = l2_evict_first_policy();
+    // chunks of request rr before its first streamed one (its shared prefix)
+    auto chunk_off = [&](int rr) -> int {
+      const int i = rr - p.shared_first;
+      return (p.shared_num > 0 && i >= 0 && i < p.shared_num && __ldg(p.shared_use + i))
+                 ? p.shared_chunks
+                 : 0;
+    };
+    // table entry of absolute chunk a
+    auto entry_of = [&](int a) -> int { return (sh == 4) ? a : (sh == 5 ? a >> 1 : 2 * a); };
     int L = __ldg(p.seq_lens + r), t = __ldg(p.qsl + r);
     int nent = (L + (1 << sh) - 1) >> sh;  // table entries the request uses
     int pr = __ldg(p.dec_prefix + r);       // stream position of the request's first chunk
+    int off = chunk_off(r);                 // chunk = blk + off
     int win_r = -1, win_base = 0, win_val = -1;
-    // The next request's lengths and the first 32 entries of its block table
-    // row, loaded one request ahead: a request boundary then waits on no load.
-    int nx_pn = -1, nx_L = 0, nx_t = 0, nx_win = -1;
+    // The next request's lengths and the 32 entries of its block table row
+    // from its first streamed chunk on, loaded one request ahead: a request
+    // boundary then waits on no load.
+    int nx_pn = -1, nx_L = 0, nx_t = 0, nx_win = -1, nx_off = 0;
     auto prefetch_next = [&]() {
       if (r + 1 < p.num_reqs) {
         nx_pn = __ldg(p.dec_prefix + r + 2);
         nx_L = __ldg(p.seq_lens + r + 1);
         nx_t = __ldg(p.qsl + r + 1);
-        nx_win = lane < p.max_blocks
-                     ? __ldg(p.block_table + static_cast<long long>(r + 1) * p.max_blocks + lane)
+        nx_off = chunk_off(r + 1);
+        const int e = entry_of(nx_off) + lane;
+        nx_win = e < p.max_blocks
+                     ? __ldg(p.block_table + static_cast<long long>(r + 1) * p.max_blocks + e)
                      : -1;
       } else {
         nx_pn = -1;
@@ -356,12 +461,15 @@ __global__ void __launch_bounds__(kDecodeThreads)
         break;
       }
       if (new_piece) {
+        // a request split over several CTAs, or one whose shared prefix is
+        // attended elsewhere, leaves a partial for the combine kernel
         const long long a = pr;
         const long long cf = owner_cta(a, N, Cn), cl = owner_cta(a + nblk - 1, N, Cn);
-        out_base = (cf == cl) ? -1 : static_cast<int>((r + c) * p.virt_heads);
+        out_base = (cf == cl && off == 0) ? -1 : static_cast<int>((r + c) * p.virt_heads);
       }
       // table entries of chunk blk: e0, and e0 + 1 for 8-token blocks
-      const int e0 = (sh == 4) ? blk : (sh == 5 ? blk >> 1 : 2 * blk);
+      const int ab = blk + off;  // the chunk's place in the request
+      const int e0 = entry_of(ab);
       const int e_hi = (sh == 3) ? e0 + 1 : e0;
       if (r != win_r || e0 < win_base || e_hi >= win_base + 32) {
         win_r = r;
@@ -370,7 +478,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         win_val = (j < nent) ? __ldg(p.block_table + static_cast<long long>(r) * p.max_blocks + j) : -1;
       }
       const int phys = __shfl_sync(0xffffffffu, win_val, e0 - win_base);
-      const int nvalid = min(kChunkKeys, L - blk * kChunkKeys);
+      const int nvalid = min(kChunkKeys, L - ab * kChunkKeys);
       bool valid = phys >= 0 && phys < p.num_blocks;
       bool second = false;  // 8-token blocks: the chunk's keys 8..15 exist
       int phys1 = -1;
@@ -434,10 +542,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
             nblk = nx_pn - pr;
             L = nx_L;
             t = nx_t;
+            off = nx_off;
             nent = (L + (1 << sh) - 1) >> sh;
             win_r = r;
-            win_base = 0;
-            win_val = lane < nent ? nx_win : -1;
+            win_base = entry_of(off);
+            win_val = win_base + lane < nent ? nx_win : -1;
           } else {
             do {
               ++r;
@@ -445,6 +554,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
             } while (nblk == 0);
             L = __ldg(p.seq_lens + r);
             t = __ldg(p.qsl + r);
+            off = chunk_off(r);
             nent = (L + (1 << sh) - 1) >> sh;
           }
           prefetch_next();
@@ -656,6 +766,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
 // the request's first chunk, and that boundary's CTAs merge the request's
 // partials (one per non-empty range that touched it):
 //   M = max_p m_p,  o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p.
+// CTAs c >= C (one per request of a shared-prefix run) merge such a
+// request's decode partials with the shared-prefix items' partials of its
+// row; the boundary CTAs leave those requests to them.
 // Lanes first read the (m, l) of up to 32 pieces at once, then every lane
 // sums its dims over the pieces with independent loads.
 template <int D, int GW>
@@ -666,22 +779,44 @@ __global__ void __launch_bounds__(GW * 32) combine_kernel(const DecodeParams p) 
   const long long Cn = p.splits;
   pdl_trigger();
   pdl_wait();
-  if (c < 1 || c >= Cn) return;
-  const int r = p.bound[c];
-  if (r < 0) return;
+  auto in_shared_run = [&](int rr) -> bool {
+    const int i = rr - p.shared_first;
+    return p.shared_num > 0 && i >= 0 && i < p.shared_num && __ldg(p.shared_use + i);
+  };
+  int r, si = -1;  // si: the request's place in the shared-prefix run, if it has one
+  if (c >= Cn) {
+    si = static_cast<int>(c - Cn);
+    if (si >= p.shared_num || !__ldg(p.shared_use + si)) return;
+    r = p.shared_first + si;
+  } else {
+    if (c < 1) return;
+    r = p.bound[c];
+    if (r < 0) return;
+  }
   const int pr = __ldg(p.dec_prefix + r);
   const int nblk = __ldg(p.dec_prefix + r + 1) - pr;
   const long long N = p.hdr[kHdrDecodeBlocks];
   const long long cf = owner_cta(pr, N, Cn);
-  if (cf != c - 1) return;
-  const int npieces = static_cast<int>(owner_cta(pr + nblk - 1, N, Cn) - cf + 1);
-  // slot of piece j (CTA cf + j): (r + cf + j) * V + vg
+  if (si < 0 && (cf != c - 1 || in_shared_run(r))) return;
+  // pieces j < nd: the decode partial of CTA cf + j, in slot (r + cf + j) * V
+  // + vg; pieces nd .. nd + ns - 1: the shared-prefix items' partials
+  const int nd = static_cast<int>(owner_cta(pr + nblk - 1, N, Cn) - cf + 1);
+  const int ns = si >= 0 ? p.shared_pieces : 0;
+  const int npieces = nd + ns;
+  const long long srow = static_cast<long long>(si) * p.num_q_heads + vg * GW + h;
+  const long long sstride = static_cast<long long>(p.shared_num) * p.num_q_heads;
 
   // (m, l) of piece j; empty ranges wrote nothing and weigh zero
   auto piece_ml = [&](int j) -> float2 {
+    if (j >= npieces) return make_float2(-INFINITY, 0.f);
+    if (j >= nd) return p.shared_ml[srow + (j - nd) * sstride];
     const long long cc = cf + j;
-    if (j >= npieces || cc * N / Cn == (cc + 1) * N / Cn) return make_float2(-INFINITY, 0.f);
+    if (cc * N / Cn == (cc + 1) * N / Cn) return make_float2(-INFINITY, 0.f);
     return p.part_ml[((r + cc) * p.virt_heads + vg) * GW + h];
+  };
+  auto piece_o = [&](int j) -> const float* {
+    if (j >= nd) return p.shared_o + (srow + (j - nd) * sstride) * D;
+    return p.part_o + (((r + cf + j) * p.virt_heads + vg) * GW + h) * D;
   };
   float M = -INFINITY;
   for (int j0 = 0; j0 < npieces; j0 += 32) M = fmaxf(M, piece_ml(j0 + lane).x);
@@ -703,9 +838,7 @@ __global__ void __launch_bounds__(GW * 32) combine_kernel(const DecodeParams p) 
 #pragma unroll 8
     for (int j = 0; j < cnt; ++j) {
       const float wj = __shfl_sync(0xffffffffu, wgt, j);
-      const long long jj = wj == 0.f ? 0 : j0 + j;
-      const float* src =
-          p.part_o + (((r + cf + jj) * p.virt_heads + vg) * GW + h) * D + lane * E;
+      const float* src = piece_o(wj == 0.f ? 0 : j0 + j) + lane * E;
       if constexpr (E == 4) {
         const float4 v = *reinterpret_cast<const float4*>(src);
         acc[0] += wj * v.x;
@@ -775,12 +908,38 @@ static size_t decode_smem_bytes(int kh, int vh, int stages, int ctas_per_sm) {
 template <int D, int GW, int SH>
 static std::atomic<unsigned long long> g_decode_attr_done{0};
 
+// Launch shape of one decode instantiation on one device for a slab shape,
+// worked out once (the occupancy query costs microseconds of host time per
+// call, which short steps would pay on every launch).
+struct DecodePrep {
+  int dev, kh, vh, num_sms, stages;
+  long long splits;
+  size_t smem;
+};
+
+template <int D, int GW, int SH>
+static std::vector<DecodePrep> g_decode_prep;
+static std::mutex g_decode_prep_mu;
+
 template <int D, int GW, int SH>
 static cudaError_t decode_prepare(int kh, int vh, int num_sms, long long* splits, int* stages,
                                   size_t* smem) {
   auto kern = decode_kernel<D, GW, SH>;
   cudaError_t e = smem_attr_once(kern, 227 * 1024, g_decode_attr_done<D, GW, SH>);
   if (e != cudaSuccess) return e;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(g_decode_prep_mu);
+    for (const DecodePrep& d : g_decode_prep<D, GW, SH>)
+      if (d.dev == dev && d.kh == kh && d.vh == vh && d.num_sms == num_sms) {
+        *stages = d.stages;
+        *smem = d.smem;
+        if (splits) *splits = d.splits;
+        return cudaSuccess;
+      }
+  }
   int want = kDecodeWarpsPerSm / vh;
   if (want < 1) want = 1;
   const size_t least = DecodeLayout<D, GW>(kh, vh, kDecodeMinStages).total + 128;
@@ -794,7 +953,10 @@ static cudaError_t decode_prepare(int kh, int vh, int num_sms, long long* splits
   while (S < kDecodeMaxStages && DecodeLayout<D, GW>(kh, vh, S + 1).total + 128 <= budget) ++S;
   *stages = S;
   *smem = decode_smem_bytes<D, GW>(kh, vh, S, ctas);
-  if (splits) *splits = static_cast<long long>(num_sms) * ctas;
+  const long long full = static_cast<long long>(num_sms) * ctas;
+  if (splits) *splits = full;
+  std::lock_guard<std::mutex> lock(g_decode_prep_mu);
+  g_decode_prep<D, GW, SH>.push_back(DecodePrep{dev, kh, vh, num_sms, S, full, *smem});
   return cudaSuccess;
 }
 
@@ -810,7 +972,8 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kv_
   if (e == cudaSuccess && trace) e = cudaEventRecord(static_cast<cudaEvent_t>(trace[3]), stream);
   if (e != cudaSuccess) return e;
   return launch_pdl(combine_kernel<D, GW>,
-                    dim3(static_cast<unsigned>(p.splits), static_cast<unsigned>(p.virt_heads)),
+                    dim3(static_cast<unsigned>(p.splits + p.shared_num),
+                         static_cast<unsigned>(p.virt_heads)),
                     dim3(GW * 32), 0, stream, p);
 }
 
@@ -884,6 +1047,13 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnWorkspace& ws, const CUte
   p.part_ml = ws.part_ml;
   p.part_o = ws.part_o;
   p.bound = ws.bound;
+  p.shared_first = a.shared_first;
+  p.shared_num = a.shared_num;
+  p.shared_chunks = a.shared_len / kChunkKeys;
+  p.shared_pieces = a.shared_pieces;
+  p.shared_use = ws.casc_use;
+  p.shared_ml = ws.casc_ml;
+  p.shared_o = ws.casc_o;
   return decode_dispatch<LaunchOp>(a.head_dim, gw, a.block_shift, p, kv_map, num_sms, stream,
                                    trace);
 }

@@ -65,32 +65,58 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
   }
 }
 
-// One CTA per token (grid-stride over tokens): its threads copy the token's K
-// row and V row, 16 bytes each, into the pool at the token's slot.
-// vec_per_row = Hkv * D / 8; shift = log2(B).
-__global__ void kv_write_kernel(uint4* __restrict__ pool, const uint4* __restrict__ key,
-                                const uint4* __restrict__ value, long long key_stride_v,
-                                long long value_stride_v, const int64_t* __restrict__ slots,
-                                int num_tokens, int vec_per_row, int shift, long long num_slots) {
+// The write as one flat stream of 16-byte words: word w of the step is
+// (token t, K|V, word e of the row) with w = (2 t + kv) * vec_per_row + e,
+// so consecutive threads read consecutive words of a token's K row, then of
+// its V row, and write them to consecutive words of the pool row. Every
+// thread takes kWriteVecs words, a grid stride apart, and issues all their
+// loads -- the slot and the data, which do not depend on each other --
+// before any store, so each SM keeps tens of KB of reads in flight instead
+// of one dependent slot-then-data chain per token. Index is int for steps
+// of fewer than 2^31 words, else long long.
+constexpr int kWriteVecs = 4;
+constexpr int kWriteThreads = 512;
+
+template <typename Index>
+__global__ void __launch_bounds__(kWriteThreads)
+    kv_write_kernel(uint4* __restrict__ pool, const uint4* __restrict__ key,
+                    const uint4* __restrict__ value, long long key_stride_v,
+                    long long value_stride_v, const int64_t* __restrict__ slots, Index total,
+                    Index row_pair, int vec_per_row, int shift, long long num_slots) {
   pdl_trigger();
   pdl_wait();
-  for (int t = blockIdx.x; t < num_tokens; t += gridDim.x) {
-    const long long s = __ldg(slots + t);
-    if (s < 0) continue;
-    if (s >= num_slots) {
-      if (threadIdx.x == 0) atomicOr(&g_errors_kvwrite, kErrSlotRange);
-      continue;
+  const Index stride = static_cast<Index>(gridDim.x) * blockDim.x;
+  for (Index w0 = static_cast<Index>(blockIdx.x) * blockDim.x + threadIdx.x; w0 < total;
+       w0 += stride * kWriteVecs) {
+    uint4 val[kWriteVecs];
+    long long slot[kWriteVecs];
+    Index tok[kWriteVecs];
+    int kv[kWriteVecs], e[kWriteVecs];
+#pragma unroll
+    for (int u = 0; u < kWriteVecs; ++u) {
+      const Index w = w0 + u * stride;
+      slot[u] = -1;
+      if (w < total) {
+        tok[u] = w / row_pair;
+        const int rem = static_cast<int>(w - tok[u] * row_pair);
+        kv[u] = rem >= vec_per_row;
+        e[u] = rem - kv[u] * vec_per_row;
+        slot[u] = __ldg(slots + tok[u]);
+        const uint4* src = kv[u] ? value + static_cast<long long>(tok[u]) * value_stride_v
+                                 : key + static_cast<long long>(tok[u]) * key_stride_v;
+        val[u] = __ldg(src + e[u]);
+      }
     }
-    const long long blk = s >> shift, off = s & ((1 << shift) - 1);
-    uint4* kdst = pool + (((blk * 2) << shift) + off) * vec_per_row;
-    uint4* vdst = kdst + (static_cast<long long>(vec_per_row) << shift);
-    const uint4* ksrc = key + t * key_stride_v;
-    const uint4* vsrc = value + t * value_stride_v;
-    for (int e = threadIdx.x; e < vec_per_row; e += blockDim.x) {
-      const uint4 kv = __ldg(ksrc + e);
-      const uint4 vv = __ldg(vsrc + e);
-      kdst[e] = kv;
-      vdst[e] = vv;
+#pragma unroll
+    for (int u = 0; u < kWriteVecs; ++u) {
+      const long long s = slot[u];
+      if (s < 0) continue;  // padding row, or past the end
+      if (s >= num_slots) {
+        if (kv[u] == 0 && e[u] == 0) atomicOr(&g_errors_kvwrite, kErrSlotRange);
+        continue;
+      }
+      const long long blk = s >> shift, off = s & ((1 << shift) - 1);
+      pool[((((blk * 2 + kv[u]) << shift) + off) * vec_per_row) + e[u]] = val[u];
     }
   }
 }
@@ -148,14 +174,24 @@ cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long
                             int num_sms, cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
   const int vec_per_row = num_kv_heads * head_dim / 8;
-  const int threads = vec_per_row >= 128 ? 128 : (vec_per_row >= 64 ? 64 : 32);
-  const long long cap = static_cast<long long>(num_sms) * 16;
-  const int grid = static_cast<int>(num_tokens < cap ? num_tokens : cap);
-  return launch_pdl(kv_write_kernel, dim3(grid), dim3(threads), 0, stream, static_cast<uint4*>(pool),
-                    static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-                    key_stride / 8, value_stride / 8, slots, num_tokens, vec_per_row,
-                    static_cast<int>(__builtin_ctz(static_cast<unsigned>(block_size))),
-                    static_cast<long long>(num_blocks) * block_size);
+  const long long total = static_cast<long long>(num_tokens) * 2 * vec_per_row;
+  const long long per_cta = static_cast<long long>(kWriteThreads) * kWriteVecs;
+  const long long cap = static_cast<long long>(num_sms) * 2;  // 2 x 512 threads per SM
+  const long long need = (total + per_cta - 1) / per_cta;
+  const int grid = static_cast<int>(need < cap ? need : cap);
+  const int shift = static_cast<int>(__builtin_ctz(static_cast<unsigned>(block_size)));
+  const long long num_slots = static_cast<long long>(num_blocks) * block_size;
+  // int indexes while w0 + kWriteVecs * stride stays below 2^31
+  if (total + static_cast<long long>(grid) * kWriteThreads * kWriteVecs < (1ll << 31))
+    return launch_pdl(kv_write_kernel<int>, dim3(grid), dim3(kWriteThreads), 0, stream,
+                      static_cast<uint4*>(pool), static_cast<const uint4*>(key),
+                      static_cast<const uint4*>(value), key_stride / 8, value_stride / 8, slots,
+                      static_cast<int>(total), 2 * vec_per_row, vec_per_row, shift, num_slots);
+  return launch_pdl(kv_write_kernel<long long>, dim3(grid), dim3(kWriteThreads), 0, stream,
+                    static_cast<uint4*>(pool), static_cast<const uint4*>(key),
+                    static_cast<const uint4*>(value), key_stride / 8, value_stride / 8, slots,
+                    total, static_cast<long long>(2 * vec_per_row), vec_per_row, shift,
+                    num_slots);
 }
 
 cudaError_t read_errors_kvwrite(uint32_t* out, bool clear) {

@@ -23,11 +23,16 @@ enum : int {
 struct AttnWorkspace {
   uint32_t* hdr;         // [kHdrWords]
   int32_t* dec_prefix;   // [R + 1]: decode 16-key chunks before request r
-  int32_t* pf_req;       // [R]: request id of the k-th prefill request
-  int32_t* pf_prefix;    // [R + 1]: prefill items before the k-th prefill request
+  int32_t* pf_req;       // [R + 1]: request id of the k-th prefill request (-1: the
+                         // shared-prefix items, listed after every prefill request)
+  int32_t* pf_prefix;    // [R + 2]: prefill items before the k-th prefill request
   float2* part_ml;       // [slots][GW]: (running max in log2 units, sum)
   float* part_o;         // [slots][GW][D]: unnormalised partial outputs
   int* bound;            // [C]: request holding the first position of each decode CTA range
+  // shared-prefix items (only when the call has a shared-prefix hint)
+  int32_t* casc_use;     // [shared_num]: 1 if the request takes its prefix from the shared items
+  float2* casc_ml;       // [pieces][shared_num][Hq]: (max in log2 units, sum) of each piece
+  float* casc_o;         // [pieces][shared_num][Hq][D]: unnormalised output of each piece
 };
 
 struct AttnArgs {
@@ -44,7 +49,36 @@ struct AttnArgs {
   int num_q_heads, num_kv_heads, head_dim, num_blocks;
   int block_shift;  // log2 of the tokens per cache block (3, 4 or 5)
   float scale;
+  // Shared-prefix hint: requests shared_first .. + shared_num - 1 share their
+  // first shared_len tokens (0 = off). Their prefix is attended by shared
+  // items of the prefill kernel: q tiles of their rows x kv heads x key
+  // pieces of shared_tpp 128-key tiles (shared_pieces of them).
+  int shared_len, shared_first, shared_num;
+  int shared_pieces, shared_tpp;
 };
+
+// Key pieces of the shared-prefix items: enough items to fill the device
+// (q tiles x kv heads x pieces ~ num_sms), each piece at least two 128-key
+// tiles so that both softmax warpgroups of a CTA take part.
+// At most this many pieces, so that a decode warp merges a row's partials
+// with loads it issues all at once (GW heads x pieces <= 32 lanes).
+constexpr int kMaxSharedPieces = 8;
+
+inline void shared_split(int shared_num, int group, int num_kv_heads, int shared_len,
+                         int num_sms, int* pieces, int* tpp) {
+  const int qt = (shared_num + (128 / group) - 1) / (128 / group);
+  const int tiles = (shared_len + 127) / 128;
+  const int base = qt * num_kv_heads;
+  int want = base > 0 ? num_sms / base : 1;
+  if (want < 1) want = 1;
+  int t = (tiles + want - 1) / want;
+  if (t < 2) t = 2;
+  if (t < (tiles + kMaxSharedPieces - 1) / kMaxSharedPieces)
+    t = (tiles + kMaxSharedPieces - 1) / kMaxSharedPieces;
+  if (t > tiles) t = tiles;
+  *tpp = t;
+  *pieces = (tiles + t - 1) / t;
+}
 
 // Raise a kernel's dynamic shared memory limit once per device: `done` is a
 // per-kernel bit mask of devices already set up, so later launches (also

@@ -210,6 +210,11 @@ struct PrefillParams {
   uint32_t* hdr;
   const int32_t* pf_req;
   const int32_t* pf_prefix;
+  // shared-prefix items (see AttnArgs): their partial results go to
+  // shared_ml / shared_o instead of the output
+  int shared_len, shared_first, shared_num, shared_pieces, shared_tpp;
+  float2* shared_ml;
+  float* shared_o;
 };
 
 // mbarriers. "commit" ones are arrived on by tcgen05.commit of the MMA thread.
@@ -275,8 +280,10 @@ struct PrefillItem {
   int q0;      // batch row of the request's first query
   int n;       // new tokens of the request
   int i0;      // first query of the tile (within the request)
-  int kv_len;  // keys the tile's last query sees
+  int kv_len;  // keys the tile's last query sees (shared items: end of the piece)
   int nkv;     // key tiles
+  int kt0;     // first key tile (0, or a shared item's piece start)
+  int piece;   // shared items: key piece, else -1
   long long bt_row;  // offset of the request's block table row
 };
 
@@ -305,11 +312,33 @@ __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams& p, int 
     const int k = upper_index(p.pf_prefix, n_req, item);
     r = __ldg(p.pf_req + k);
     local = item - __ldg(p.pf_prefix + k);
-    m.c = __ldg(p.num_computed + r);
-    m.q0 = __ldg(p.qsl + r);
-    m.n = __ldg(p.qsl + r + 1) - m.q0;
+    if (r >= 0) {
+      m.c = __ldg(p.num_computed + r);
+      m.q0 = __ldg(p.qsl + r);
+      m.n = __ldg(p.qsl + r + 1) - m.q0;
+    } else {
+      m.c = p.shared_len;
+      m.q0 = __ldg(p.qsl + p.shared_first);
+      m.n = p.shared_num;
+    }
   }
   m.g = local % p.num_kv_heads;
+  if (r < 0) {
+    // shared-prefix item: rows = the run's decode rows (one per request) x
+    // the kv head's q heads, keys = one piece of the shared prefix, all of
+    // them visible to every row
+    const int rest = local / p.num_kv_heads;
+    m.piece = rest % p.shared_pieces;
+    m.i0 = (rest / p.shared_pieces) * QT;
+    const int tiles = (p.shared_len + kTileN - 1) / kTileN;
+    m.kt0 = m.piece * p.shared_tpp;
+    m.nkv = min(p.shared_tpp, tiles - m.kt0);
+    m.kv_len = min((m.kt0 + m.nkv) * kTileN, p.shared_len);
+    m.bt_row = static_cast<long long>(p.shared_first) * p.max_blocks;
+    return m;
+  }
+  m.piece = -1;
+  m.kt0 = 0;
   const int ntile = (m.n + QT - 1) / QT;
   const int mt = ntile - 1 - local / p.num_kv_heads;
   m.i0 = mt * QT;
@@ -425,8 +454,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       meta_prefix_s[i] = __ldg(p.pf_prefix + i);
       if (i < n_req) {
         const int r = __ldg(p.pf_req + i);
-        const int q0 = __ldg(p.qsl + r);
-        meta_s[i] = make_int4(r, __ldg(p.num_computed + r), q0, __ldg(p.qsl + r + 1) - q0);
+        if (r >= 0) {
+          const int q0 = __ldg(p.qsl + r);
+          meta_s[i] = make_int4(r, __ldg(p.num_computed + r), q0, __ldg(p.qsl + r + 1) - q0);
+        } else {  // the shared-prefix items
+          meta_s[i] = make_int4(-1, p.shared_len, __ldg(p.qsl + p.shared_first), p.shared_num);
+        }
       }
     }
   }
@@ -499,8 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_or_abort(&empty[slot], ((T - S) / S) & 1u, abort_flag);
           if (!ok) break;
         }
-        if (kt * E + E > win_base + 32) {
-          win_base = kt * E;
+        const int ka = m.kt0 + kt;  // key tile (keys ka*128 ..)
+        if (ka * E + E > win_base + 32) {
+          win_base = ka * E;
           const int e = win_base + ln;
           win_val = entry_id(p, m, e);
           if (!is_v && (e << bsh) < m.kv_len && win_val < 0)
@@ -510,14 +544,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pool rows of one kv head: (block * 2 + k|v) * B + offset
         int id0, id1 = -1, row0, row1 = 0;
         if (bsh == 4) {
-          id0 = __shfl_sync(0xffffffffu, win_val, kt * 8 + b - win_base);
+          id0 = __shfl_sync(0xffffffffu, win_val, ka * 8 + b - win_base);
           row0 = id0 * 32 + (is_v ? 16 : 0);
         } else if (bsh == 5) {
-          id0 = __shfl_sync(0xffffffffu, win_val, kt * 4 + (b >> 1) - win_base);
+          id0 = __shfl_sync(0xffffffffu, win_val, ka * 4 + (b >> 1) - win_base);
           row0 = id0 * 64 + (b & 1) * 16 + (is_v ? 32 : 0);
         } else {
-          id0 = __shfl_sync(0xffffffffu, win_val, kt * 16 + 2 * b - win_base);
-          id1 = __shfl_sync(0xffffffffu, win_val, kt * 16 + 2 * b + 1 - win_base);
+          id0 = __shfl_sync(0xffffffffu, win_val, ka * 16 + 2 * b - win_base);
+          id1 = __shfl_sync(0xffffffffu, win_val, ka * 16 + 2 * b + 1 - win_base);
           row0 = id0 * 16 + (is_v ? 8 : 0);
           row1 = id1 * 16 + (is_v ? 8 : 0);
         }
@@ -635,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     // chunk validity of tile kt of item m (lanes 0..7), read one tile ahead
     auto load_ids = [&](const PrefillItem& mm, int kt) -> int {
-      return (lane < 8 && kt < mm.nkv && chunk_ok(p, mm, kt, lane)) ? 1 : -1;
+      return (lane < 8 && kt < mm.nkv && chunk_ok(p, mm, mm.kt0 + kt, lane)) ? 1 : -1;
     };
     int item = take_item(sh, 0, abort_flag, true);
     PrefillItem m{};
@@ -659,8 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a tile every row sees in full needs no mask; otherwise column j is
         // visible iff j <= jlim and its 16-key chunk was loaded (chunk c =
         // columns 16c .. 16c+15)
-        const bool full = kt * kTileN + kTileN - 1 <= m.c + m.i0 && mask == 0xFFu;
-        const int jlim = lim - kt * kTileN;
+        const int ka = m.kt0 + kt;  // key tile (keys ka*128 ..)
+        const bool full = ka * kTileN + kTileN - 1 <= m.c + m.i0 && mask == 0xFFu;
+        const int jlim = lim - ka * kTileN;
         // the whole S row in one TMEM round trip: 4 x 32 columns, one wait
         uint32_t sr[4][32];
 #pragma unroll
@@ -721,12 +756,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
         // V rows of keys past kv_len or of chunks not loaded must be zero
         // (0 * NaN): for such a tile wait for its V copy first
-        if (kt * kTileN + kTileN > m.kv_len || mask != 0xFFu) {
+        if (ka * kTileN + kTileN > m.kv_len || mask != 0xFFu) {
           const uint32_t Tv = T + kt;
           const int slot = static_cast<int>(Tv % kVStages);
           ok = wait_or_abort(&sh.v_full[slot], (Tv / kVStages) & 1u, abort_flag);
           if (!ok) break;
-          const int key = kt * kTileN + row;
+          const int key = ka * kTileN + row;
           if (key >= m.kv_len || !(mask >> (row >> 4) & 1u)) {
             unsigned char* vrow = gbase + Lay::kV + slot * Lay::kTileKV;
 #pragma unroll
@@ -759,6 +794,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool store = qi < m.n;
       uint16_t* dst =
           p.out + (static_cast<long long>(m.q0 + qi) * p.num_q_heads + m.g * G + row % G) * D;
+      // shared-prefix items keep the row's partial (max, sum, unnormalised O)
+      // for the decode of request shared_first + qi: slot of (piece, qi, head)
+      const bool partial = m.piece >= 0;
+      const long long pslot =
+          (static_cast<long long>(m.piece) * p.shared_num + qi) * p.num_q_heads + m.g * G + row % G;
       if (nkv > 1) {
         // ---- merge the two partial results of the item: each warpgroup
         // writes half of the output columns from both O_0 and O_1
@@ -783,7 +823,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float M = fmaxf(ml0.x, ml1.x);
         const float a0 = (ml0.x == -INFINITY) ? 0.f : exp2f(ml0.x - M);
         const float a1 = (ml1.x == -INFINITY) ? 0.f : exp2f(ml1.x - M);
-        const float inv = 1.f / (ml0.y * a0 + ml1.y * a1);
+        const float lsum = ml0.y * a0 + ml1.y * a1;
+        const float inv = 1.f / lsum;
+        if (partial && store && wg == 0) p.shared_ml[pslot] = make_float2(M, lsum);
         const uint32_t t_o0 = tmem + lane_base + e * 256u + 128u;
         const uint32_t t_o1 = tmem + lane_base + (1 - e) * 256u + 128u;
 #pragma unroll 1
@@ -794,7 +836,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::ld16(t_o1 + col, o1);
           tc::wait16(o0);
           tc::wait16(o1);
-          if (store) {
+          if (partial) {
+            if (store) {
+              float4* d4 = reinterpret_cast<float4*>(p.shared_o + pslot * D + col);
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                float v[4];
+#pragma unroll
+                for (int y = 0; y < 4; ++y)
+                  v[y] = __uint_as_float(o0[4 * x + y]) * a0 + __uint_as_float(o1[4 * x + y]) * a1;
+                d4[x] = make_float4(v[0], v[1], v[2], v[3]);
+              }
+            }
+          } else if (store) {
             uint32_t w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -823,12 +877,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::fence_after_sync();
           const float inv = 1.f / l_run;
+          if (partial && store) p.shared_ml[pslot] = make_float2(m_run, l_run);
 #pragma unroll 1
           for (int q = 0; q < D / 16; ++q) {
             uint32_t o[16];
             tc::ld16(t_o + q * 16, o);
             tc::wait16(o);
-            if (store) {
+            if (partial) {
+              if (store) {
+                float4* d4 = reinterpret_cast<float4*>(p.shared_o + pslot * D + q * 16);
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                  d4[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
+                                      __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
+              }
+            } else if (store) {
               uint32_t w[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e)
@@ -889,10 +952,23 @@ cudaError_t launch_prefill(const AttnArgs& a, const AttnWorkspace& ws, const CUt
   p.hdr = ws.hdr;
   p.pf_req = ws.pf_req;
   p.pf_prefix = ws.pf_prefix;
-  // upper bound of work items from the host hints: every row can be in a tile
+  p.shared_len = a.shared_len;
+  p.shared_first = a.shared_first;
+  p.shared_num = a.shared_num;
+  p.shared_pieces = a.shared_pieces;
+  p.shared_tpp = a.shared_tpp;
+  p.shared_ml = ws.casc_ml;
+  p.shared_o = ws.casc_o;
+  // upper bound of work items from the host hints: every row can be in a
+  // tile (only rows of requests with more than one new token are, when the
+  // call has no shared prefix), plus the shared-prefix items
   const long long tile_q = kTileM / p.group;
-  const long long max_items =
-      ((static_cast<long long>(a.num_tokens) + tile_q - 1) / tile_q + a.num_reqs) * a.num_kv_heads;
+  long long max_items = a.max_query_len > 1
+      ? ((static_cast<long long>(a.num_tokens) + tile_q - 1) / tile_q + a.num_reqs) *
+            a.num_kv_heads
+      : 0;
+  if (a.shared_num > 0)
+    max_items += (a.shared_num + tile_q - 1) / tile_q * a.shared_pieces * a.num_kv_heads;
   const int grid = static_cast<int>(max_items < num_sms ? max_items : num_sms);
   if (grid <= 0) return cudaSuccess;
   if (a.head_dim == 128) return launch_prefill_t<128>(p, kv_map, q_map, grid, stream);

@@ -31,11 +31,12 @@ def _clear_errors():
     yield
 
 
-def run_and_check(step, decode_splits=None, rows=None, check_pool=True):
-    ds = DeviceStep(step, decode_splits=decode_splits)
+def run_and_check(step, decode_splits=None, rows=None, check_pool=True, shared_prefix=None,
+                  expect_flags=0):
+    ds = DeviceStep(step, decode_splits=decode_splits, shared_prefix=shared_prefix)
     ds.run()
     torch.cuda.synchronize()
-    assert binding.pkv_get_device_errors(clear=True) == 0
+    assert binding.pkv_get_device_errors(clear=True) == expect_flags
     slots, pool, ref = oracle_step(step, rows=rows)
     assert np.array_equal(ds.slots_host(), slots)
     if check_pool:
@@ -475,6 +476,85 @@ def test_mixed_step_with_raised_scale():
                                    rng.choice(np.arange(1024, step.num_tokens), 400,
                                               replace=False)]))
     run_and_check(step, rows=rows)
+
+
+# ---------------------------------------------------------------- shared prefix
+# A run of decode requests whose tables start with the same blocks (prefix
+# caching, ref_cnt > 1): with the shared-prefix hint the call attends the
+# shared keys once per group on the tensor cores and each decode only its own
+# keys past them. The result must be the oracle's (shared blocks behave as
+# private copies).
+def test_prefix_sharing_workload_with_the_shared_prefix_hint():
+    step = synth.prefix_sharing()
+    from paged_kv_cache_hkv_gb300.runner import shared_prefix_of
+    assert shared_prefix_of(step) == (1024, 0, 128)
+    run_and_check(step, shared_prefix="auto")
+    run_and_check(step, shared_prefix="auto", decode_splits=1)
+    run_and_check(step, shared_prefix="auto", decode_splits=600)
+
+
+def _partly_shared_specs(rng, prefix, n_shared=37):
+    specs = [RequestSpec(int(rng.integers(100, 700)), int(rng.integers(40, 200)))]  # a chunk
+    specs += [RequestSpec(0, int(rng.integers(2, 80))) for _ in range(3)]             # prompts
+    specs += [RequestSpec(int(L) - 1, 1) for L in rng.integers(1, 900, size=9)]        # decodes
+    specs += [RequestSpec(prefix + int(x), 1, shares_prefix=True)                     # the run
+              for x in rng.integers(0, 300, size=n_shared)]
+    specs += [RequestSpec(int(L) - 1, 1) for L in rng.integers(1, 900, size=5)]
+    return specs
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (16, 4, 64), (8, 8, 128), (64, 8, 128),
+                                      (8, 2, 64)])
+def test_shared_prefix_in_a_mixed_batch(B, Hq, Hkv, D):
+    rng = np.random.default_rng(B * 100 + Hq + D)
+    prefix = {8: 96, 16: 800, 32: 512}[B]  # under one key tile, 6.25 tiles, 4 tiles
+    step = make_step(_partly_shared_specs(rng, prefix), num_q_heads=Hq, num_kv_heads=Hkv,
+                     head_dim=D, block_size=B, prefix_tokens=prefix, seed=B + Hq + D)
+    hint = (prefix, 13, 37)
+    from paged_kv_cache_hkv_gb300.runner import shared_prefix_of
+    assert shared_prefix_of(step) == hint
+    run_and_check(step, shared_prefix=hint)
+    run_and_check(step, shared_prefix=hint, decode_splits=23)
+
+
+def test_shared_prefix_hint_is_checked_per_request():
+    """Requests of the declared run that do not share the prefix (their own
+    tables, or a context not past the prefix) are attended without the hint;
+    the run's other requests still use it. The flag says so."""
+    rng = np.random.default_rng(5)
+    specs = [RequestSpec(512 + int(x), 1, shares_prefix=True) for x in rng.integers(0, 200, 20)]
+    specs[7] = RequestSpec(700, 1)    # private table inside the run
+    specs[12] = RequestSpec(300, 1)   # shorter than the prefix
+    step = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, prefix_tokens=512,
+                     seed=5)
+    run_and_check(step, shared_prefix=(512, 0, 20), expect_flags=binding.DEVERR_SHARED)
+
+
+def test_shared_prefix_hint_over_a_prefill_turns_the_run_off():
+    rng = np.random.default_rng(6)
+    specs = [RequestSpec(512 + int(x), 1, shares_prefix=True) for x in rng.integers(0, 200, 9)]
+    specs.insert(4, RequestSpec(600, 30))  # a chunk inside the declared run
+    step = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, prefix_tokens=512,
+                     seed=6)
+    run_and_check(step, shared_prefix=(512, 0, 10), expect_flags=binding.DEVERR_SHARED)
+
+
+@pytest.mark.parametrize("name", ["drift", "steep", "scale"])
+def test_shared_prefix_on_the_rescale_paths(name):
+    """Keys that drift with their position (the shared items' running max
+    moves, their pieces' partials differ by up to thousands of powers of
+    two, and the decode continues from the merged partial), or a raised
+    scale."""
+    rng = np.random.default_rng(7)
+    specs = [RequestSpec(1024 + int(x), 1, shares_prefix=True) for x in rng.integers(0, 300, 64)]
+    kw = {"drift": dict(key_drift=rescale_cases.drift_for(0.01, 128)),
+          "steep": dict(key_drift=rescale_cases.drift_for(1.5, 128)),
+          "scale": dict(scale=8 / math.sqrt(128))}[name]
+    step = make_step(specs, num_q_heads=32, num_kv_heads=8, head_dim=128, prefix_tokens=1024,
+                     seed=8, **kw)
+    run_and_check(step, shared_prefix="auto")
+    run_and_check(step, shared_prefix="auto", decode_splits=300)
 
 
 # ---------------------------------------------------------------- CUDA graphs
