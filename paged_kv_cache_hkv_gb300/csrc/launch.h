@@ -60,8 +60,8 @@ struct AttnArgs {
 // Key pieces of the shared-prefix items: enough items to fill the device
 // (q tiles x kv heads x pieces ~ num_sms), each piece at least two 128-key
 // tiles so that both softmax warpgroups of a CTA take part.
-// At most this many pieces, so that a decode warp merges a row's partials
-// with loads it issues all at once (GW heads x pieces <= 32 lanes).
+// At most this many pieces: each adds one partial per row that the combine
+// kernel reads, and pieces of a few tiles already fill the device.
 constexpr int kMaxSharedPieces = 8;
 
 inline void shared_split(int shared_num, int group, int num_kv_heads, int shared_len,
