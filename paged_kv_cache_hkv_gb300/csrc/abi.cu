@@ -445,6 +445,8 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
                 static_cast<uint32_t>(slab_kh), dec_box, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != PKV_OK) return st;
 
+  a.decode_splits = splits;
+
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void** ev = options ? options->trace_events : nullptr;
   auto mark = [&](int i) -> cudaError_t {

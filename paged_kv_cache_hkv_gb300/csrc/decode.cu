@@ -198,8 +198,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, AttnWorkspace ws
     sum.c += v.c;
   }
   Int3 run = block_exclusive_scan(sum, &total);
+  // Request holding the first position floor(c * N / C) of each decode
+  // CTA's range: request r (chunks [a, a + n) of the stream) holds the
+  // starts of CTAs ceil(a C / N) .. ceil((a + n) C / N) - 1, so each CTA
+  // reads its start instead of searching the prefix sums.
+  const long long N = total.a, C = a.decode_splits;
+  if (N == 0)
+    for (long long c = threadIdx.x; c < C; c += blockDim.x) ws.bound[c] = -1;
   for (int r = r0; r < r1; ++r) {
     const Int3 v = plan_counts(a, ws, r, tile_q, false);
+    if (v.a > 0) {
+      const long long c_lo = (static_cast<long long>(run.a) * C + N - 1) / N;
+      long long c_hi = ((static_cast<long long>(run.a) + v.a) * C + N - 1) / N;
+      if (c_hi > C) c_hi = C;
+      for (long long c = c_lo; c < c_hi; ++c) ws.bound[c] = r;
+    }
     ws.dec_prefix[r] = run.a;
     if (v.b) {
       ws.pf_req[run.b] = r;
@@ -257,7 +270,7 @@ struct DecodeParams {
   const uint32_t* hdr;
   float2* part_ml;
   float* part_o;
-  int* bound;  // [C]: request holding the first position of CTA c's range (-1: none)
+  const int* bound;  // [C]: request holding the first position of CTA c's range (-1: none)
   // Shared prefix: request shared_first + i with shared_use[i] streams only
   // its chunks from shared_chunks on and always leaves partials; the combine
   // kernel merges them with the shared items' partials of its row
@@ -378,17 +391,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
   const long long N = p.hdr[kHdrDecodeBlocks];
   const long long x0 = c * N / Cn, x1 = (c + 1) * N / Cn;
 
-  // ---------------- locate position x0: (request r, chunk blk)
+  // ---------------- locate position x0: (request r, chunk blk); the plan
+  // recorded the request holding it (the combine kernel reads the same
+  // records to find split requests)
   int r = -1, blk = 0, nblk = 0;
   if (x0 < N) {
-    r = warp_upper_index(p.dec_prefix, p.num_reqs, x0);
+    r = __ldg(p.bound + c);
     const int pr = __ldg(p.dec_prefix + r);
     nblk = __ldg(p.dec_prefix + r + 1) - pr;
     blk = static_cast<int>(x0 - pr);
   }
-  // the combine kernel finds split requests from these records (CTAs with an
-  // empty range record the request that holds their start too)
-  if (threadIdx.x == 0 && slab == 0) p.bound[c] = r;
   if (x0 >= x1) return;
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < S; ++s) {

@@ -55,6 +55,7 @@ struct AttnArgs {
   // pieces of shared_tpp 128-key tiles (shared_pieces of them).
   int shared_len, shared_first, shared_num;
   int shared_pieces, shared_tpp;
+  long long decode_splits;  // CTAs along the decode stream (C)
 };
 
 // Key pieces of the shared-prefix items: enough items to fill the device

@@ -290,3 +290,43 @@ def test_producer_walk_with_lookahead_visits_its_range_in_order(seed):
             if x0 < x1:
                 got += producer_walk(prefix, n, x0, x1)
         assert got == want
+
+
+def plan_bounds(nblk, C):
+    """The plan kernel's rule for the request holding the first position of
+    every decode CTA's range: request r (chunks [a, a + n) of the stream)
+    holds the starts of CTAs ceil(a * C / N) .. ceil((a + n) * C / N) - 1."""
+    N = int(sum(nblk))
+    bound = [-1] * C
+    if N == 0:
+        return bound
+    a = 0
+    for r, n in enumerate(nblk):
+        if n:
+            c_lo = -(-(a * C) // N)
+            c_hi = min(C, -(-((a + n) * C) // N))
+            for c in range(c_lo, c_hi):
+                bound[c] = r
+        a += n
+    return bound
+
+
+@pytest.mark.parametrize("trial", range(200))
+def test_plan_bounds_equal_the_search_of_each_range_start(trial):
+    rng = np.random.default_rng(500 + trial)
+    R = int(rng.integers(1, 40))
+    nblk = rng.integers(0, 50, size=R) * (rng.random(R) < 0.8)
+    C = int(rng.integers(1, 400))
+    bound = plan_bounds(nblk, C)
+    prefix = np.concatenate([[0], np.cumsum(nblk)])
+    N = int(prefix[-1])
+    for c in range(C):
+        x0 = c * N // C
+        if N == 0:
+            assert bound[c] == -1
+            continue
+        # brute force: the request whose chunks hold position x0
+        r = int(np.searchsorted(prefix, x0, side="right")) - 1
+        while nblk[r] == 0:  # an empty request holds no position
+            r += 1
+        assert bound[c] == r, (c, x0, r, bound[c])

@@ -290,7 +290,10 @@ def test_prefill_chunks_match_one_shot_on_gpu():
                      seed=77, shuffle_pool=True)
     ds = DeviceStep(full)
     ds.run()
+    torch.cuda.synchronize()
     one_shot = ds.out_host().copy()
+    _, _, ref = oracle_step(full)
+    assert_close(one_shot, ref)  # the one-shot prefill against the oracle
     for c, n in ((0, 150), (150, 131), (281, 119)):
         step = make_step([RequestSpec(c, n)], num_q_heads=32, num_kv_heads=8, head_dim=128,
                          seed=77)
@@ -308,6 +311,9 @@ def test_prefill_chunks_match_one_shot_on_gpu():
                                     workspace=ws)
         torch.cuda.synchronize()
         got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        # each chunk's rows against the oracle's one-shot rows (a chunk over a
+        # cached prefix is the same attention), and against the GPU one-shot
+        assert_close(got, ref[c:c + n], what=f"chunk ({c}, {n})")
         a = got.view(np.uint16).astype(np.uint32) << 16
         b = one_shot[c:c + n].astype(np.uint32) << 16
         diff = np.abs(a.view(np.float32) - b.view(np.float32))
