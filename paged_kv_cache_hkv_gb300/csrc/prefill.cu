@@ -715,7 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[q][i]));
+          for (int i = 0; i < 32; i += 2)
+            mx4[(i >> 1) & 3] = max3f(mx4[(i >> 1) & 3], __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]));
         // (scale > 0 keeps the argmax)
         const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
         if (__any_sync(0xffffffffu, mx > m_run + kRescaleLog2)) {
@@ -739,21 +740,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P = 2^(s * scale - m) as bf16 (-inf -> 0) over S_wg: column j of the
         // row holds keys 2j (low half) and 2j+1
-        float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+        // (pairs of columns in the packed fp32x2 FMA / add: half the issue slots)
+        float2 ps4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
         const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-msub, -msub);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {  // keys 32q .. 32q+31 -> columns 16q .. 16q+15
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float p0 = exp2f(__uint_as_float(sr[q][2 * j]) * p.scale_log2 - msub);
-            const float p1 = exp2f(__uint_as_float(sr[q][2 * j + 1]) * p.scale_log2 - msub);
-            pk[j] = pack_bf16x2(p0, p1);
-            ps4[j & 3] += p0 + p1;
+            const float2 e = ffma2(
+                make_float2(__uint_as_float(sr[q][2 * j]), __uint_as_float(sr[q][2 * j + 1])), sc2, nm2);
+            const float2 pp = make_float2(exp2f(e.x), exp2f(e.y));
+            pk[j] = pack_bf16x2(pp.x, pp.y);
+            ps4[j & 3] = fadd2(ps4[j & 3], pp);
           }
           tc::st16(t_s + 16 * q, pk);
         }
-        l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+        l_run += ((ps4[0].x + ps4[1].x) + (ps4[2].x + ps4[3].x)) +
+                 ((ps4[0].y + ps4[1].y) + (ps4[2].y + ps4[3].y));
         // V rows of keys past kv_len or of chunks not loaded must be zero
         // (0 * NaN): for such a tile wait for its V copy first
         if (ka * kTileN + kTileN > m.kv_len || mask != 0xFFu) {
