@@ -10,24 +10,20 @@
 //
 // Work item = (request, tile of 128 query rows, kv head). The 128 rows of a
 // tile are the G = Hq/Hkv q heads of one kv head for 128/G consecutive
-// queries, so every K/V tile feeds all G heads (GQA). The item's key tiles
-// (128 keys = 8 chunks of 16 keys: 8 blocks of 16 tokens, 4 of 32 or 16 of
-// 8) are split between two softmax warpgroups: tile T of the CTA's tile
-// stream (every item's tiles in order) goes to warpgroup T & 1, which keeps
-// its own accumulators (TMEM columns [256w, 256w+128) for S,
-// [256w+128, 256w+128+D) for O) and its own running max and sum.
-//   S_w = Q K^T      tcgen05.mma M=128 N=128, A = Q (smem), B = K (smem)
-//   O_w += P_w V     tcgen05.mma M=128 N=D, A = P_w (TMEM), B = V (smem)
-// Each softmax thread owns one row: it reads S with tcgen05.ld, applies the
-// causal mask, keeps a base-2 running max (rescaling O in TMEM only when it
-// grows by more than 2^8) and sum, and writes P as bf16 pairs over S_w's
-// columns with tcgen05.st. A K-copy warp (3-slot ring) and a V-copy warp
-// (2-slot ring) stream the tiles by TMA (128-byte swizzle, one 16-key chunk
-// of one kv head per copy, two copies of 8 rows for 8-token blocks); one
-// thread issues every MMA. An item of one tile is finished by its
-// warpgroup alone; at the end of a longer item the two partial (max, sum, O)
-// are merged (the even tiles' partial first, so the bits do not depend on
-// the schedule) and each warpgroup writes half of the output columns. The
+// queries, so every K/V tile feeds all G heads (GQA). Per key tile (128 keys
+// = 8 chunks of 16 keys: 8 blocks of 16 tokens, 4 of 32 or 16 of 8):
+//   S = Q K^T      tcgen05.mma M=128 N=128, A = Q (smem), B = K (smem)
+//   O += P V       tcgen05.mma M=128 N=D, A = P (TMEM), B = V (smem)
+// with S in one of three TMEM buffers (tile T of the CTA's stream uses
+// buffer T % 3) and one O accumulator. Eight softmax warps share every
+// tile: each holds 16 query rows, and each row is split between two threads
+// (keys 0..63 and 64..127). A thread reads its half row of S with
+// tcgen05.ld, applies the causal mask, keeps a base-2 running max (rescaling
+// its half of O in TMEM only when the max grows by more than 2^8) and sum,
+// and writes P as bf16 pairs over the S buffer's columns with tcgen05.st.
+// A K-copy warp (3-slot ring) and a V-copy warp (2-slot ring) stream the
+// tiles by TMA (128-byte swizzle, one 16-key chunk of one kv head per copy,
+// two copies of 8 rows for 8-token blocks); one thread issues every MMA. The
 // CTAs are persistent and take items from a counter; the roles meet only at
 // mbarriers, so consecutive items overlap.
 //
@@ -166,6 +162,47 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&v)[32]) {
       : "memory");
 }
 
+// The 16-lane x 2 access shape: 16 TMEM lanes from the address's lane,
+// threads 0-15 at columns col .. col+31 of lanes 0-15, threads 16-31 at
+// columns col+OFF .. col+OFF+31 of the same lanes (asynchronous like ld32).
+template <int OFF>
+__device__ __forceinline__ void ld_half32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], %33;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "n"(OFF));
+}
+
+template <int OFF>
+__device__ __forceinline__ void st_half16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17};" ::"r"(taddr),
+      "n"(OFF), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+      "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+      "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+template <int OFF>
+__device__ __forceinline__ void st_half32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};" ::"r"(
+          taddr),
+      "n"(OFF), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+      "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+      "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]),
+      "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
 }  // namespace tc
 
 
@@ -173,10 +210,12 @@ constexpr int kTileM = 128;    // query rows (query x head) per tile
 constexpr int kTileN = 128;    // keys per tile (8 chunks of 16)
 constexpr int kKStages = 3;    // K ring: global tile T uses slot T % 3
 constexpr int kVStages = 2;    // V ring: global tile T uses slot T % 2
+constexpr int kSBufs = 3;      // S (then P) buffers in TMEM: global tile T uses buffer T % 3
+constexpr uint32_t kTmemS = 128;  // TMEM columns: O at [0, D), S buffer b at [128 + 128b, +128)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kItemQ = 4;      // claimed work items in flight between the roles
 constexpr int kMetaReqs = 128;  // prefill requests whose metadata a CTA keeps in shared memory
-constexpr int kThreads = 352;  // 2 softmax warpgroups + MMA warp + K-copy warp + V-copy warp
+constexpr int kThreads = 352;  // 8 softmax warps + MMA warp + K-copy warp + V-copy warp
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (powers of two)
 
 template <int D>
@@ -187,10 +226,9 @@ struct PrefillLayout {
   static constexpr uint32_t kTileKV = DH * kChunk;         // K (or V) of one 128-key tile
   static constexpr uint32_t kK = kQ + DH * kChunk;         // K ring
   static constexpr uint32_t kV = kK + kKStages * kTileKV;  // V ring
-  static constexpr uint32_t kML = kV + kVStages * kTileKV; // float2 [item parity][warpgroup][row]
   // request metadata: int4 (request, cached, first row, new tokens) [kMetaReqs],
   // then the item prefix int [kMetaReqs + 1]
-  static constexpr uint32_t kMeta = kML + 2 * 2 * kTileM * 8;
+  static constexpr uint32_t kMeta = kV + kVStages * kTileKV;
   static constexpr uint32_t kBar = kMeta + kMetaReqs * 16 + (kMetaReqs + 1) * 4 + 124;
   static constexpr uint32_t kBytes = kBar + 512;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base
@@ -225,12 +263,11 @@ struct PrefillShared {
   uint64_t k_free[kKStages];     // commit: the S that read the K slot is done
   uint64_t v_full[kVStages];     // V tile landed (TMA)
   uint64_t v_free[kVStages];     // commit: the PV that read the V slot is done
-  uint64_t s_full[2];            // commit: S of warpgroup w in TMEM
-  uint64_t p_ready[2];           // 128 arrivals: P of warpgroup w in TMEM, O rescaled, V cleaned
-  uint64_t o_full[2];            // commit: the item's last PV into O_w done
-  uint64_t o_free[2];            // 256 arrivals: O_w of its item read (a warpgroup that
-                                 // finishes an item alone arrives twice per thread)
-  uint64_t ml_full[2];           // 256 arrivals: both (m, l) of a merged item published
+  uint64_t s_full[kSBufs];       // commit: S of the buffer's tile in TMEM
+  uint64_t p_ready[kSBufs];      // 256 arrivals: P of the buffer's tile in TMEM, O
+                                 // rescaled, V cleaned (and, for an item's first tile,
+                                 // the previous item's O read)
+  uint64_t o_full;               // commit: the item's last PV done
   uint64_t drain;
   uint64_t iq_full[kItemQ];      // item id j published in item_q[j % kItemQ]
   uint64_t iq_free[kItemQ];      // 10 arrivals: every role has read it
@@ -375,19 +412,15 @@ __device__ __forceinline__ bool chunk_ok(const PrefillParams& p, const PrefillIt
 //   warp 9:  Q copy (once the previous item's last S is done) and K tiles
 //            into a 3-slot ring (a slot is refilled once its S is done);
 //   warp 10: V tiles into a 2-slot ring (refilled once its PV is done);
-//   warp 8, lane 0: every MMA, in the order S(0), S(1), PV(0), S(2), PV(1),
-//            S(3), ...: S_w = Q K^T into TMEM columns [256w, 256w+128), and
-//            O_w += P_w V with P_w read from TMEM, where softmax w wrote it
-//            over S_w (bf16 pairs, one pair per 32-bit column). MMAs run in
-//            issue order, so S(kt+2) overwrites P_w only after PV(kt) read it.
-//   warpgroups 0 and 1: tile number T of the CTA (counting every item's
-//            tiles) belongs to warpgroup T & 1. A warpgroup keeps its own
-//            running max and sum and its own O_w at TMEM columns
-//            [256w+128, 256w+128+D). An item of one tile is finished by its
-//            warpgroup alone, so consecutive one-tile items run on both
-//            warpgroups at once; an item of several tiles ends with the two
-//            partials merged (log-sum-exp), each warpgroup writing half of
-//            the output columns.
+//   warp 8, lane 0: every MMA, per item in the order S(0), S(1), S(2),
+//            PV(0), S(3), PV(1), S(4), ...: S(kt) = Q K^T into S buffer
+//            (T+kt) % 3, and O += P V with P read from TMEM, where the
+//            softmax warps wrote it over the tile's S (bf16 pairs, one pair
+//            per 32-bit column). MMAs run in issue order, so S(kt+3)
+//            overwrites P(kt) only after PV(kt) read it.
+//   warps 0..7: the softmax of every tile, 16 query rows per warp and half
+//            of each row per thread, and the item's epilogue (each thread
+//            normalises and writes half of its row's output columns).
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
@@ -414,15 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.v_full[i], 1);
       mbar_init(&sh.v_free[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&sh.s_full[i], 1);
-      mbar_init(&sh.p_ready[i], 128);
+      mbar_init(&sh.p_ready[i], 256);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sh.o_full[i], 1);
-      mbar_init(&sh.o_free[i], 256);
-      mbar_init(&sh.ml_full[i], 256);
-    }
+    mbar_init(&sh.o_full, 1);
     mbar_init(&sh.drain, 1);
     for (int i = 0; i < kItemQ; ++i) {
       mbar_init(&sh.iq_full[i], 1);
@@ -584,8 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((tid & 31) == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16(kTileM, kTileN, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(kTileM, D, 1);
-      // uses[w]: items so far whose PV wrote O_w
-      uint32_t T = 0, np[2] = {0, 0}, uses[2] = {0, 0};
+      uint32_t T = 0;  // tiles of earlier items
       bool ok = true;
       for (int it = 0; ok; ++it) {
         const int item = take_item(sh, it, abort_flag, false);
@@ -593,57 +621,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok || !valid(item)) break;
         const PrefillItem m = prefill_item(p, n_req, item, QT, meta, meta_prefix);
         const int nkv = m.nkv;
-        const int rot = static_cast<int>(T & 1u);  // tile kt goes to warpgroup (kt + rot) & 1
-        auto issue_s = [&](int kt) -> bool {  // S_w = Q K^T for tile kt
-          const int w = (kt + rot) & 1;
+        auto issue_s = [&](int kt) -> bool {  // S buffer of tile T+kt = Q K^T
           const uint32_t Tk = T + kt;
           const int slot = static_cast<int>(Tk % kKStages);
+          const uint32_t b = Tk % kSBufs;
           if (!wait_or_abort(&sh.k_full[slot], (Tk / kKStages) & 1u, abort_flag)) return false;
           tc::fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Lay::kChunk + (kk & 3) * 32;
             const uint64_t a = tc::sw128_desc(base + Lay::kQ + off, 16, 1024);
-            const uint64_t b = tc::sw128_desc(base + Lay::kK + slot * Lay::kTileKV + off, 16, 1024);
-            tc::mma_bf16(tmem + w * 256u, a, b, idesc_qk, kk > 0);
+            const uint64_t bd = tc::sw128_desc(base + Lay::kK + slot * Lay::kTileKV + off, 16, 1024);
+            tc::mma_bf16(tmem + kTmemS + kTileN * b, a, bd, idesc_qk, kk > 0);
           }
-          tc::commit(&sh.s_full[w]);
+          tc::commit(&sh.s_full[b]);
           tc::commit(&sh.k_free[slot]);
           if (kt == nkv - 1) tc::commit(&sh.q_free);
           return true;
         };
-        auto issue_pv = [&](int kt) -> bool {  // O_w += P_w V for tile kt, P_w from TMEM
-          const int w = (kt + rot) & 1;
+        auto issue_pv = [&](int kt) -> bool {  // O += P V, P read from the tile's S buffer
           const uint32_t Tv = T + kt;
           const int slot = static_cast<int>(Tv % kVStages);
+          const uint32_t b = Tv % kSBufs;
           if (!wait_or_abort(&sh.v_full[slot], (Tv / kVStages) & 1u, abort_flag)) return false;
           tc::fence_after_sync();
           const uint32_t vbase = base + Lay::kV + slot * Lay::kTileKV;
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk) {
-            const uint64_t b = tc::sw128_desc(vbase + kk * 2048, Lay::kChunk, 1024);
-            tc::mma_bf16_ts(tmem + w * 256u + 128u, tmem + w * 256u + kk * 8u, b, idesc_pv,
-                            (kt >= 2 || kk > 0) ? 1u : 0u);
+            const uint64_t bd = tc::sw128_desc(vbase + kk * 2048, Lay::kChunk, 1024);
+            tc::mma_bf16_ts(tmem, tmem + kTmemS + kTileN * b + kk * 8u, bd, idesc_pv,
+                            (kt > 0 || kk > 0) ? 1u : 0u);
           }
           tc::commit(&sh.v_free[slot]);
-          if (kt >= nkv - 2) tc::commit(&sh.o_full[w]);  // the item's last PV into O_w
+          if (kt == nkv - 1) tc::commit(&sh.o_full);  // the item's O is complete
           return true;
         };
         ok = wait_or_abort(&sh.q_full, it & 1u, abort_flag);
-        if (ok) ok = issue_s(0);
-        if (ok && nkv > 1) ok = issue_s(1);
+        for (int kt = 0; ok && kt < kSBufs && kt < nkv; ++kt) ok = issue_s(kt);
         for (int kt = 0; ok && kt < nkv; ++kt) {
-          const int w = (kt + rot) & 1;
-          ok = wait_or_abort(&sh.p_ready[w], np[w] & 1u, abort_flag);
-          ++np[w];
-          // the first PV into O_w of the item overwrites it: the last item
-          // that used O_w must have been read
-          if (kt < 2) {
-            if (ok && uses[w] > 0) ok = wait_or_abort(&sh.o_free[w], (uses[w] - 1) & 1u, abort_flag);
-            ++uses[w];
-          }
+          // the first PV of an item overwrites O: the softmax warps publish
+          // P of the item's first tile only after their epilogue of the
+          // previous item has read O
+          const uint32_t Tg = T + kt;
+          ok = wait_or_abort(&sh.p_ready[Tg % kSBufs], (Tg / kSBufs) & 1u, abort_flag);
           if (ok) ok = issue_pv(kt);
-          if (ok && kt + 2 < nkv) ok = issue_s(kt + 2);
+          // PV(kt) was issued first and MMAs run in issue order, so S(kt+3)
+          // overwrites P(kt) only after PV(kt) read it
+          if (ok && kt + kSBufs < nkv) ok = issue_s(kt + kSBufs);
         }
         T += nkv;
       }
@@ -653,19 +677,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ================= softmax warpgroup wg: tiles wg, wg + 2, ... of each item
-    const int wg = tid >> 7;
-    const int row = tid & 127;  // query row of this thread (TMEM lane)
+    // ================= softmax warps 0..7: every tile of every item. Warp w
+    // owns TMEM lanes (query rows) lane0 .. lane0+15 with lane0 = 32*(w%4) +
+    // 16*(w/4) (warp w reaches lanes 32*(w%4) .. +31 only). Of each row,
+    // thread t < 16 takes keys 0..63 of every tile and thread t + 16 keys
+    // 64..127 (the 16x32bx2 TMEM access shape), so a row's max needs one
+    // shuffle and no warp waits for another.
+    constexpr int HC = D / 2;  // O columns per thread
     const int lane = tid & 31;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + wg * 256u;  // S_wg, then P_wg
-    const uint32_t t_o = t_s + 128u;                     // O_wg
-    // Tile number T of the CTA (all items) belongs to warpgroup T & 1, so
-    // one-tile items alternate between the warpgroups and each finishes its
-    // own alone; an item of several tiles is split between them and merged.
-    // Both warpgroups walk every item, so they keep the same counts: T,
-    // uses[x] (items whose PV wrote O_x) and mi (merged items).
-    uint32_t T = 0, ns = 0, uses[2] = {0, 0}, mi = 0;
+    const int ch = lane >> 4;  // key half of this thread
+    const int lane0 = 32 * (warp & 3) + 16 * (warp >> 2);
+    const int row = lane0 + (lane & 15);  // query row of this thread (TMEM lane)
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(lane0) << 16);
+    uint32_t T = 0;
     bool ok = true;
     // chunk validity of tile kt of item m (lanes 0..7), read one tile ahead
     auto load_ids = [&](const PrefillItem& mm, int kt) -> int {
@@ -676,77 +700,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     int next_id = -1;
     if (valid(item)) {
       m = prefill_item(p, n_req, item, QT, meta, meta_prefix);
-      next_id = load_ids(m, wg);  // T = 0: this warpgroup's first tile is tile wg
+      next_id = load_ids(m, 0);
     }
     for (int it = 0; ok && valid(item); ++it) {
       const int nkv = m.nkv;
-      const int rot = static_cast<int>(T & 1u);  // tile kt belongs to warpgroup (kt + rot) & 1
-      const int qi = m.i0 + row / G;                    // query of this row
-      const int lim = min(m.c + qi, m.kv_len - 1);      // last key this row may see
+      const int qi = m.i0 + row / G;                // query of this row
+      const int lim = min(m.c + qi, m.kv_len - 1);  // last key this row may see
       float m_run = -INFINITY, l_run = 0.f;
-      for (int kt = (wg - rot) & 1, nmine = 0; kt < nkv; kt += 2, ++nmine) {
+      for (int kt = 0; kt < nkv; ++kt) {
+        const uint32_t Tg = T + kt;
+        const uint32_t b = Tg % kSBufs;
+        const uint32_t t_s = t_lane + kTmemS + kTileN * b;
         const uint32_t mask = __ballot_sync(0xffffffffu, next_id >= 0) & 0xFFu;
-        ok = wait_or_abort(&sh.s_full[wg], ns & 1u, abort_flag);
-        ++ns;
+        ok = wait_or_abort(&sh.s_full[b], (Tg / kSBufs) & 1u, abort_flag);
         if (!ok) break;
         tc::fence_after_sync();
-        // a tile every row sees in full needs no mask; otherwise column j is
-        // visible iff j <= jlim and its 16-key chunk was loaded (chunk c =
-        // columns 16c .. 16c+15)
+        // a tile every row sees in full needs no mask; otherwise key j of the
+        // tile is visible iff j <= lim - 128 ka and its 16-key chunk was
+        // loaded (chunk c = keys 16c .. 16c+15)
         const int ka = m.kt0 + kt;  // key tile (keys ka*128 ..)
         const bool full = ka * kTileN + kTileN - 1 <= m.c + m.i0 && mask == 0xFFu;
-        const int jlim = lim - ka * kTileN;
-        // the whole S row in one TMEM round trip: 4 x 32 columns, one wait
-        uint32_t sr[4][32];
+        // this thread's keys 64ch .. 64ch+63 of the tile: sr[0] the first 32
+        uint32_t sr[2][32];
+        tc::ld_half32<64>(t_s, sr[0]);
+        tc::ld_half32<64>(t_s + 32, sr[1]);
+        tc::wait32(sr[0]);
+        tc::wait32(sr[1]);
+        if (!full) {  // invisible keys become -inf
+          const int jlim = lim - ka * kTileN - 64 * ch;
+          const uint32_t cm = mask >> (4 * ch);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tc::ld32(t_s + q * 32, sr[q]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tc::wait32(sr[q]);
-        if (!full) {  // invisible columns become -inf
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < 2; ++q)
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int j = q * 32 + i;
-              if (!(((mask >> (j >> 4)) & 1u) && j <= jlim)) sr[q][i] = __float_as_uint(-INFINITY);
+              if (!(((cm >> (j >> 4)) & 1u) && j <= jlim)) sr[q][i] = __float_as_uint(-INFINITY);
             }
         }
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
           for (int i = 0; i < 32; i += 2)
-            mx4[(i >> 1) & 3] = max3f(mx4[(i >> 1) & 3], __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]));
-        // (scale > 0 keeps the argmax)
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            mx4[(i >> 1) & 3] =
+                max3f(mx4[(i >> 1) & 3], __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]));
+        float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        // (scale > 0 keeps the argmax; both threads of the row get the same bits)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * p.scale_log2;
         if (__any_sync(0xffffffffu, mx > m_run + kRescaleLog2)) {
           const float m_new = fmaxf(m_run, mx);
           const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
           l_run *= alpha;
           m_run = m_new;
-          // O_wg holds PV of this warpgroup's earlier tiles (all done: S(kt)
-          // was issued after them)
-          if (nmine > 0) {
+          if (kt > 0) {
+            // O holds PV of the item's earlier tiles; the last of them,
+            // PV(Tg-1), is done when its V slot is released
+            const uint32_t Tp = Tg - 1;
+            ok = wait_or_abort(&sh.v_free[Tp % kVStages], (Tp / kVStages) & 1u, abort_flag);
+            if (!ok) break;
+            tc::fence_after_sync();
 #pragma unroll 1
-            for (int q = 0; q < D / 16; ++q) {
-              uint32_t o[16];
-              tc::ld16(t_o + q * 16, o);
-              tc::wait16(o);
+            for (int q = 0; q < HC / 32; ++q) {  // this thread's O columns HC*ch + 32q ..
+              uint32_t o[32];
+              tc::ld_half32<HC>(t_lane + 32 * q, o);
+              tc::wait32(o);
 #pragma unroll
-              for (int x = 0; x < 16; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-              tc::st16(t_o + q * 16, o);
+              for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+              tc::st_half32<HC>(t_lane + 32 * q, o);
             }
           }
         }
-        // P = 2^(s * scale - m) as bf16 (-inf -> 0) over S_wg: column j of the
-        // row holds keys 2j (low half) and 2j+1
-        // (pairs of columns in the packed fp32x2 FMA / add: half the issue slots)
+        // P = 2^(s * scale - m) as bf16 (-inf -> 0) over the S buffer: column
+        // c holds keys 2c (low half) and 2c+1, so this thread's keys land in
+        // columns 32ch .. 32ch+31 (pairs of keys in the packed fp32x2 FMA / add)
         float2 ps4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
         const float msub = (m_run == -INFINITY) ? 0.f : m_run;
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-msub, -msub);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // keys 32q .. 32q+31 -> columns 16q .. 16q+15
+        for (int q = 0; q < 2; ++q) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -756,36 +788,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[j] = pack_bf16x2(pp.x, pp.y);
             ps4[j & 3] = fadd2(ps4[j & 3], pp);
           }
-          tc::st16(t_s + 16 * q, pk);
+          tc::st_half16<32>(t_s + 16 * q, pk);
         }
         l_run += ((ps4[0].x + ps4[1].x) + (ps4[2].x + ps4[3].x)) +
                  ((ps4[0].y + ps4[1].y) + (ps4[2].y + ps4[3].y));
         // V rows of keys past kv_len or of chunks not loaded must be zero
-        // (0 * NaN): for such a tile wait for its V copy first
+        // (0 * NaN): for such a tile wait for its V copy first; thread (row,
+        // ch) clears 64-element chunk ch of V row `row`
         if (ka * kTileN + kTileN > m.kv_len || mask != 0xFFu) {
-          const uint32_t Tv = T + kt;
-          const int slot = static_cast<int>(Tv % kVStages);
-          ok = wait_or_abort(&sh.v_full[slot], (Tv / kVStages) & 1u, abort_flag);
+          const int slot = static_cast<int>(Tg % kVStages);
+          // S(Tg) done only implies PV(Tg-3) done, so the slot's copy
+          // barrier may be anywhere from V(Tg-2) pending to V(Tg) landed;
+          // once PV(Tg-2) is done (slot released) it is V(Tg) pending or landed
+          if (Tg >= static_cast<uint32_t>(kVStages))
+            ok = wait_or_abort(&sh.v_free[slot], ((Tg - kVStages) / kVStages) & 1u, abort_flag);
+          if (ok) ok = wait_or_abort(&sh.v_full[slot], (Tg / kVStages) & 1u, abort_flag);
           if (!ok) break;
-          const int key = ka * kTileN + row;
-          if (key >= m.kv_len || !(mask >> (row >> 4) & 1u)) {
-            unsigned char* vrow = gbase + Lay::kV + slot * Lay::kTileKV;
+          if (ch < DH && (ka * kTileN + row >= m.kv_len || !(mask >> (row >> 4) & 1u))) {
+            uint4* v4 = reinterpret_cast<uint4*>(gbase + Lay::kV + slot * Lay::kTileKV +
+                                                 ch * Lay::kChunk + row * 128);
 #pragma unroll
-            for (int dh = 0; dh < DH; ++dh) {
-              uint4* v4 = reinterpret_cast<uint4*>(vrow + dh * Lay::kChunk + row * 128);
-#pragma unroll
-              for (int x = 0; x < 8; ++x) v4[x] = make_uint4(0, 0, 0, 0);
-            }
+            for (int x = 0; x < 8; ++x) v4[x] = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
         }
         tc::wait_st();
         tc::fence_before_sync();
-        mbar_arrive(&sh.p_ready[wg]);
-        next_id = load_ids(m, kt + 2);  // its latency hides under the next S wait
+        mbar_arrive(&sh.p_ready[b]);
+        next_id = load_ids(m, kt + 1);  // its latency hides under the next S wait
       }
       if (!ok) break;
-      // ---- the next item's id and metadata, while the last PVs run
+      // ---- the next item's id and metadata, while the last PV runs
       const int item_n = take_item(sh, it + 1, abort_flag, true);
       if (item_n < 0) {  // aborted
         ok = false;
@@ -794,130 +827,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       PrefillItem m_next{};
       if (valid(item_n)) {
         m_next = prefill_item(p, n_req, item_n, QT, meta, meta_prefix);
-        // this warpgroup's first tile of the next item
-        next_id = load_ids(m_next, (wg - static_cast<int>((T + nkv) & 1u)) & 1);
+        next_id = load_ids(m_next, 0);
       }
+      // ---- epilogue: this thread's O columns HC*ch .. HC*ch + HC - 1 of its row
+      ok = wait_or_abort(&sh.o_full, it & 1u, abort_flag);
+      if (!ok) break;
+      tc::fence_after_sync();
+      const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
+      const float inv = 1.f / l_tot;
       const bool store = qi < m.n;
-      uint16_t* dst =
-          p.out + (static_cast<long long>(m.q0 + qi) * p.num_q_heads + m.g * G + row % G) * D;
+      const int head = m.g * G + row % G;
       // shared-prefix items keep the row's partial (max, sum, unnormalised O)
       // for the decode of request shared_first + qi: slot of (piece, qi, head)
       const bool partial = m.piece >= 0;
-      const long long pslot =
-          (static_cast<long long>(m.piece) * p.shared_num + qi) * p.num_q_heads + m.g * G + row % G;
-      if (nkv > 1) {
-        // ---- merge the two partial results of the item: each warpgroup
-        // writes half of the output columns from both O_0 and O_1
-        ok = wait_or_abort(&sh.o_full[0], uses[0] & 1u, abort_flag) &&
-             wait_or_abort(&sh.o_full[1], uses[1] & 1u, abort_flag);
-        if (!ok) break;
-        tc::fence_after_sync();
-        float2* ml = reinterpret_cast<float2*>(gbase + Lay::kML) + (mi & 1u) * 2 * kTileM;
-        ml[wg * kTileM + row] = make_float2(m_run, l_run);
-        mbar_arrive(&sh.ml_full[mi & 1u]);
-        if (!wait_or_abort(&sh.ml_full[mi & 1u], (mi >> 1) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        // the partial of the item's even tiles (warpgroup rot) always comes
-        // first, so the rounding of the merge does not depend on which
-        // warpgroup the schedule gave those tiles: results are the same bits
-        // from run to run
-        const int e = rot;
-        const float2 ml0 = ml[e * kTileM + row];
-        const float2 ml1 = ml[(1 - e) * kTileM + row];
-        const float M = fmaxf(ml0.x, ml1.x);
-        const float a0 = (ml0.x == -INFINITY) ? 0.f : exp2f(ml0.x - M);
-        const float a1 = (ml1.x == -INFINITY) ? 0.f : exp2f(ml1.x - M);
-        const float lsum = ml0.y * a0 + ml1.y * a1;
-        const float inv = 1.f / lsum;
-        if (partial && store && wg == 0) p.shared_ml[pslot] = make_float2(M, lsum);
-        const uint32_t t_o0 = tmem + lane_base + e * 256u + 128u;
-        const uint32_t t_o1 = tmem + lane_base + (1 - e) * 256u + 128u;
+      const long long pslot = (static_cast<long long>(m.piece) * p.shared_num + qi) * p.num_q_heads + head;
+      if (partial && store && ch == 0) p.shared_ml[pslot] = make_float2(m_run, l_tot);
+      uint16_t* dst = p.out + (static_cast<long long>(m.q0 + qi) * p.num_q_heads + head) * D + HC * ch;
 #pragma unroll 1
-        for (int q = 0; q < D / 32; ++q) {
-          const int col = wg * (D / 2) + q * 16;
-          uint32_t o0[16], o1[16];
-          tc::ld16(t_o0 + col, o0);
-          tc::ld16(t_o1 + col, o1);
-          tc::wait16(o0);
-          tc::wait16(o1);
-          if (partial) {
-            if (store) {
-              float4* d4 = reinterpret_cast<float4*>(p.shared_o + pslot * D + col);
+      for (int q = 0; q < HC / 32; ++q) {
+        uint32_t o[32];
+        tc::ld_half32<HC>(t_lane + 32 * q, o);
+        tc::wait32(o);
+        if (!store) continue;
+        if (partial) {
+          float4* d4 = reinterpret_cast<float4*>(p.shared_o + pslot * D + HC * ch + 32 * q);
 #pragma unroll
-              for (int x = 0; x < 4; ++x) {
-                float v[4];
+          for (int x = 0; x < 8; ++x)
+            d4[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
+                                __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
+        } else {
+          uint32_t w[16];
 #pragma unroll
-                for (int y = 0; y < 4; ++y)
-                  v[y] = __uint_as_float(o0[4 * x + y]) * a0 + __uint_as_float(o1[4 * x + y]) * a1;
-                d4[x] = make_float4(v[0], v[1], v[2], v[3]);
-              }
-            }
-          } else if (store) {
-            uint32_t w[8];
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float v0 = (__uint_as_float(o0[2 * e]) * a0 + __uint_as_float(o1[2 * e]) * a1) * inv;
-              const float v1 =
-                  (__uint_as_float(o0[2 * e + 1]) * a0 + __uint_as_float(o1[2 * e + 1]) * a1) * inv;
-              w[e] = pack_bf16x2(v0, v1);
-            }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
-            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          }
+          for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
         }
-        tc::fence_before_sync();
-        mbar_arrive(&sh.o_free[0]);
-        mbar_arrive(&sh.o_free[1]);
-        ++uses[0];
-        ++uses[1];
-        ++mi;
-      } else {
-        // ---- a one-tile item: its warpgroup (rot) writes every column alone
-        if (wg == rot) {
-          if (!wait_or_abort(&sh.o_full[wg], uses[wg] & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const float inv = 1.f / l_run;
-          if (partial && store) p.shared_ml[pslot] = make_float2(m_run, l_run);
-#pragma unroll 1
-          for (int q = 0; q < D / 16; ++q) {
-            uint32_t o[16];
-            tc::ld16(t_o + q * 16, o);
-            tc::wait16(o);
-            if (partial) {
-              if (store) {
-                float4* d4 = reinterpret_cast<float4*>(p.shared_o + pslot * D + q * 16);
-#pragma unroll
-                for (int x = 0; x < 4; ++x)
-                  d4[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
-                                      __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
-              }
-            } else if (store) {
-              uint32_t w[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-              uint4* d4 = reinterpret_cast<uint4*>(dst + q * 16);
-              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-          }
-          tc::fence_before_sync();
-          mbar_arrive_n(&sh.o_free[wg], 2);  // the only reader of O_wg: both shares
-        }
-        ++uses[rot];
       }
       T += nkv;
       m = m_next;
       item = item_n;
     }
   }
-
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 8) {

@@ -4,28 +4,38 @@ Every role of a prefill CTA is restated as the sequence of mbarrier waits
 and arrivals it performs:
 - the K-copy warp claims items and copies Q and K tiles;
 - the V-copy warp copies V tiles;
-- the MMA thread issues S and PV;
-- the two softmax warpgroups take tile T of the CTA's stream on warpgroup
-  T & 1, finish one-tile items alone and merge longer ones.
+- the MMA thread issues, per item, S(0), S(1), S(2), then PV(kt) and
+  S(kt+3) for each tile kt, with S of tile T in TMEM buffer T % 3 and one
+  O accumulator;
+- the softmax warps (modelled as N_SOFTMAX independent agents, each owning
+  some query rows) take every tile of every item, sometimes rescale O
+  (after PV of the previous tile is done), sometimes clean V rows (after the
+  V copy landed), publish P, and write the item's output once its last PV
+  is done.
 
 Copies and MMA completions are asynchronous events. Copies complete in any
 order; MMA commits complete in issue order. Random item lists run under
-many random interleavings.
+many random interleavings, and the optional waits are taken at random.
 
 Each wait names the barrier phase it means (from the role's own counters),
 and a parity wait is only correct if the barrier is then at that phase or
 one past it. The model checks that, that no barrier receives more arrivals
-than a phase takes, and that the CTA never deadlocks.
+than a phase takes, that the CTA never deadlocks, and the TMEM hazards:
+S(T) overwrites buffer T % 3 only after every agent read S(T-3) and PV(T-3)
+read P(T-3); the first PV of an item overwrites O only after every agent
+read the previous item's O; a rescale finds PV(T-1) done and PV(T) not yet
+issued.
 """
 
 import random
 
 import pytest
 
-K_STAGES, V_STAGES, ITEM_Q = 3, 2, 4
+K_STAGES, V_STAGES, S_BUFS, ITEM_Q = 3, 2, 3, 4
+N_SOFTMAX = 4
 # arrivals per phase: item queue slots are released by the MMA thread, the
-# V-copy warp and the 8 softmax warps (4 per warpgroup)
-IQ_FREE_ARRIVALS = 10
+# V-copy warp and every softmax agent
+IQ_FREE_ARRIVALS = 2 + N_SOFTMAX
 
 
 class Barrier:
@@ -41,8 +51,9 @@ class Barrier:
 
 
 class Cta:
-    def __init__(self, items):
+    def __init__(self, items, rng):
         self.items = items  # key tiles of each item, in claim order
+        self.rng = rng
         b = {}
 
         def mk(name, count):
@@ -56,12 +67,10 @@ class Cta:
         for i in range(V_STAGES):
             mk(f"v_full{i}", 1)
             mk(f"v_free{i}", 1)
-        for w in range(2):
-            mk(f"s_full{w}", 1)
-            mk(f"p_ready{w}", 1)  # the warpgroup's 128 arrivals, as one
-            mk(f"o_full{w}", 1)
-            mk(f"o_free{w}", 2)   # two warpgroups' worth of readers
-            mk(f"ml_full{w}", 2)  # one per warpgroup
+        for i in range(S_BUFS):
+            mk(f"s_full{i}", 1)
+            mk(f"p_ready{i}", N_SOFTMAX)
+        mk("o_full", 1)
         for i in range(ITEM_Q):
             mk(f"iq_full{i}", 1)
             mk(f"iq_free{i}", IQ_FREE_ARRIVALS)
@@ -70,6 +79,11 @@ class Cta:
         self.next_claim = 0
         self.tma = []  # copies in flight: (barrier) -- complete in any order
         self.mma = []  # MMA commits in flight -- complete in issue order
+        # TMEM bookkeeping for the hazard checks
+        self.s_read = {}     # tile -> agents that read its S (and wrote P)
+        self.pv_issued = set()
+        self.pv_done = set()
+        self.o_read = {}     # item -> agents whose epilogue read O
 
     def claim(self):
         j = self.next_claim
@@ -78,7 +92,8 @@ class Cta:
 
 
 # Operations a role yields: ("wait", barrier, phase index), ("arrive", barrier, n),
-# ("tma", barrier), ("commit", barrier), ("do", callable).
+# ("tma", barrier), ("commit", barrier), ("pv", tile) -- a PV whose completion
+# is recorded in issue order with the commits.
 
 def k_warp(cta):
     T = 0
@@ -128,102 +143,160 @@ def v_warp(cta):
         it += 1
 
 
-def mma_thread(cta):
+def mma_thread(cta, s_before_pv=False):
     T = 0
-    np_ = [0, 0]
-    uses = [0, 0]
     it = 0
     while True:
         item = yield from take(cta, it, 1)
         if item is None:
             return
         nkv = cta.items[item]
-        rot = T & 1
 
         def issue_s(kt):
-            w = (kt + rot) & 1
-            s = (T + kt) % K_STAGES
-            yield ("wait", f"k_full{s}", (T + kt) // K_STAGES)
-            yield ("commit", f"s_full{w}")
+            Tk = T + kt
+            s = Tk % K_STAGES
+            yield ("wait", f"k_full{s}", Tk // K_STAGES)
+            # S(Tk) overwrites buffer Tk % 3: S(Tk-3) read by every agent and
+            # P(Tk-3) read by its PV (issued earlier: MMAs run in order)
+            if Tk >= S_BUFS:
+                assert cta.s_read.get(Tk - S_BUFS, 0) == N_SOFTMAX, f"S({Tk}) over unread S"
+                assert (Tk - S_BUFS) in cta.pv_issued, f"S({Tk}) before PV({Tk - S_BUFS})"
+            yield ("commit", f"s_full{Tk % S_BUFS}")
             yield ("commit", f"k_free{s}")
             if kt == nkv - 1:
                 yield ("commit", "q_free")
 
-        yield ("wait", "q_full", it)
-        yield from issue_s(0)
-        if nkv > 1:
-            yield from issue_s(1)
-        for kt in range(nkv):
-            w = (kt + rot) & 1
-            yield ("wait", f"p_ready{w}", np_[w])
-            np_[w] += 1
-            if kt < 2:
-                if uses[w] > 0:
-                    yield ("wait", f"o_free{w}", uses[w] - 1)
-                uses[w] += 1
-            s = (T + kt) % V_STAGES
-            yield ("wait", f"v_full{s}", (T + kt) // V_STAGES)
+        def issue_pv(kt):
+            Tv = T + kt
+            s = Tv % V_STAGES
+            yield ("wait", f"v_full{s}", Tv // V_STAGES)
+            if kt == 0 and it > 0:  # O is overwritten: the last item's O read by all
+                assert cta.o_read.get(it - 1, 0) == N_SOFTMAX, f"item {it} PV(0) over unread O"
+            cta.pv_issued.add(Tv)
+            yield ("pv", Tv)
             yield ("commit", f"v_free{s}")
-            if kt >= nkv - 2:
-                yield ("commit", f"o_full{w}")
-            if kt + 2 < nkv:
-                yield from issue_s(kt + 2)
+            if kt == nkv - 1:
+                yield ("commit", "o_full")
+
+        yield ("wait", "q_full", it)
+        for kt in range(min(S_BUFS, nkv)):
+            yield from issue_s(kt)
+        for kt in range(nkv):
+            Tg = T + kt
+            if s_before_pv and kt + S_BUFS < nkv:
+                yield ("wait", f"p_ready{Tg % S_BUFS}", Tg // S_BUFS)
+                yield from issue_s(kt + S_BUFS)
+                yield from issue_pv(kt)
+                continue
+            yield ("wait", f"p_ready{Tg % S_BUFS}", Tg // S_BUFS)
+            yield from issue_pv(kt)
+            if kt + S_BUFS < nkv:
+                yield from issue_s(kt + S_BUFS)
         T += nkv
         it += 1
 
 
-def softmax_wg(cta, wg):
+def softmax_agent(cta, a, epilogue_late=False):
+    rng = random.Random(cta.rng.random())
     T = 0
-    ns = 0
-    uses = [0, 0]
-    mi = 0
     it = 0
-    item = yield from take(cta, 0, 4)
+    item = yield from take(cta, 0, 1)
     while item is not None:
         nkv = cta.items[item]
-        rot = T & 1
-        for kt in range((wg - rot) & 1, nkv, 2):
-            yield ("wait", f"s_full{wg}", ns)
-            ns += 1
-            # a tile with keys past the end or chunks not loaded waits for its
-            # V copy before cleaning it; the model lets every tile do so (a
-            # superset of the kernel's waits, which change no phase)
-            s = (T + kt) % V_STAGES
-            yield ("wait", f"v_full{s}", (T + kt) // V_STAGES)
-            yield ("arrive", f"p_ready{wg}", 1)
-        item_n = yield from take(cta, it + 1, 4)
-        if nkv > 1:
-            yield ("wait", "o_full0", uses[0])
-            yield ("wait", "o_full1", uses[1])
-            yield ("arrive", f"ml_full{mi & 1}", 1)
-            yield ("wait", f"ml_full{mi & 1}", mi >> 1)
-            yield ("arrive", "o_free0", 1)
-            yield ("arrive", "o_free1", 1)
-            uses[0] += 1
-            uses[1] += 1
-            mi += 1
-        else:
-            if wg == rot:
-                yield ("wait", f"o_full{wg}", uses[wg])
-                yield ("arrive", f"o_free{wg}", 2)  # the only reader: both shares
-            uses[rot] += 1
+        for kt in range(nkv):
+            Tg = T + kt
+            if epilogue_late and kt == 0 and it > 0:
+                pass  # (the planted mistake publishes P before the epilogue below)
+            yield ("wait", f"s_full{Tg % S_BUFS}", Tg // S_BUFS)
+            cta.s_read[Tg] = cta.s_read.get(Tg, 0) + 1
+            if kt > 0 and rng.random() < 0.3:  # the max grew: rescale O
+                Tp = Tg - 1
+                yield ("wait", f"v_free{Tp % V_STAGES}", Tp // V_STAGES)
+                assert Tp in cta.pv_done, f"rescale at {Tg} before PV({Tp}) done"
+                assert Tg not in cta.pv_issued, f"rescale at {Tg} after PV({Tg}) issued"
+            if rng.random() < 0.3:  # a ragged tile: clean V rows after the copy
+                # PV(Tg-2) first: S(Tg) only implies PV(Tg-3) done, so the V
+                # slot's barrier may be anywhere from V(Tg-2) pending to V(Tg)
+                # landed; once PV(Tg-2) is done it is at V(Tg) pending or landed
+                if Tg >= V_STAGES:
+                    Tp = Tg - V_STAGES
+                    yield ("wait", f"v_free{Tp % V_STAGES}", Tp // V_STAGES)
+                yield ("wait", f"v_full{Tg % V_STAGES}", Tg // V_STAGES)
+            yield ("arrive", f"p_ready{Tg % S_BUFS}", 1)
+        item_n = yield from take(cta, it + 1, 1)
+        yield ("wait", "o_full", it)
+        assert (T + nkv - 1) in cta.pv_done
+        cta.o_read[it] = cta.o_read.get(it, 0) + 1
         T += nkv
         item = item_n
         it += 1
 
 
-def run(items, seed, mma=None, wg=None):
+def softmax_agent_epilogue_late(cta, a):
+    """A softmax agent with one planted mistake: it publishes P of an item's
+    first tile before its epilogue of the previous item has read O."""
+    rng = random.Random(cta.rng.random())
+    T = 0
+    it = 0
+    pending_epilogue = None
+    item = yield from take(cta, 0, 1)
+    while item is not None:
+        nkv = cta.items[item]
+        for kt in range(nkv):
+            Tg = T + kt
+            yield ("wait", f"s_full{Tg % S_BUFS}", Tg // S_BUFS)
+            cta.s_read[Tg] = cta.s_read.get(Tg, 0) + 1
+            yield ("arrive", f"p_ready{Tg % S_BUFS}", 1)
+            if kt == 0 and pending_epilogue is not None:
+                yield ("wait", "o_full", pending_epilogue)
+                cta.o_read[pending_epilogue] = cta.o_read.get(pending_epilogue, 0) + 1
+                pending_epilogue = None
+        item_n = yield from take(cta, it + 1, 1)
+        pending_epilogue = it
+        T += nkv
+        item = item_n
+        it += 1
+    if pending_epilogue is not None:
+        yield ("wait", "o_full", pending_epilogue)
+        cta.o_read[pending_epilogue] = cta.o_read.get(pending_epilogue, 0) + 1
+
+
+def softmax_agent_epilogue_on_v_free(cta, a):
+    """A softmax agent with one planted mistake: the epilogue waits for the
+    last PV through its V slot's release instead of the item's O barrier."""
+    T = 0
+    it = 0
+    item = yield from take(cta, 0, 1)
+    while item is not None:
+        nkv = cta.items[item]
+        for kt in range(nkv):
+            Tg = T + kt
+            yield ("wait", f"s_full{Tg % S_BUFS}", Tg // S_BUFS)
+            cta.s_read[Tg] = cta.s_read.get(Tg, 0) + 1
+            yield ("arrive", f"p_ready{Tg % S_BUFS}", 1)
+        item_n = yield from take(cta, it + 1, 1)
+        Tl = T + nkv - 1
+        yield ("wait", f"v_free{Tl % V_STAGES}", Tl // V_STAGES)
+        assert Tl in cta.pv_done
+        cta.o_read[it] = cta.o_read.get(it, 0) + 1
+        T += nkv
+        item = item_n
+        it += 1
+
+
+def run(items, seed, mma=None, agent=None):
     rng = random.Random(seed)
-    cta = Cta(items)
-    wg_role = wg or softmax_wg
-    roles = {"k": k_warp(cta), "v": v_warp(cta), "mma": (mma or mma_thread)(cta),
-             "wg0": wg_role(cta, 0), "wg1": wg_role(cta, 1)}
+    cta = Cta(items, rng)
+    agent = agent or softmax_agent
+    roles = {"k": k_warp(cta), "v": v_warp(cta), "mma": (mma or mma_thread)(cta)}
+    for a in range(N_SOFTMAX):
+        roles[f"sm{a}"] = agent(cta, a)
     pending = {name: next(g) for name, g in roles.items()}
     done = set()
     steps = 0
     while len(done) < len(roles) or cta.tma or cta.mma:
         steps += 1
-        assert steps < 200000, "model did not finish"
+        assert steps < 400000, "model did not finish"
         runnable = []
         for name, op in pending.items():
             if name in done:
@@ -245,7 +318,11 @@ def run(items, seed, mma=None, wg=None):
             cta.b[cta.tma.pop(rng.randrange(len(cta.tma)))].arrive()
             continue
         if c == "mma done":
-            cta.b[cta.mma.pop(0)].arrive()
+            ev = cta.mma.pop(0)
+            if isinstance(ev, tuple):
+                cta.pv_done.add(ev[1])
+            else:
+                cta.b[ev].arrive()
             continue
         op = pending[c]
         if op[0] == "arrive":
@@ -254,6 +331,8 @@ def run(items, seed, mma=None, wg=None):
             cta.tma.append(op[1])
         elif op[0] == "commit":
             cta.mma.append(op[1])
+        elif op[0] == "pv":
+            cta.mma.append(("pv", op[1]))
         try:
             pending[c] = roles[c].send(None)
         except StopIteration:
@@ -262,6 +341,7 @@ def run(items, seed, mma=None, wg=None):
     assert cta.next_claim == len(items) + 1
     for bar in cta.b.values():
         assert bar.pending == 0, f"{bar.name} left with {bar.pending} arrivals"
+    assert all(cta.o_read.get(i, 0) == N_SOFTMAX for i in range(len(items)))
 
 
 @pytest.mark.parametrize("case", range(60))
@@ -269,53 +349,55 @@ def test_prefill_protocol_random_items_and_interleavings(case):
     rng = random.Random(1000 + case)
     n = rng.randint(1, 14)
     # one-tile items (short prefills) mixed with items of several tiles
-    items = [rng.choice([1, 1, 1, 2, 3, rng.randint(1, 9)]) for _ in range(n)]
-    for s in range(40):
+    items = [rng.choice([1, 1, 1, 2, 3, 4, rng.randint(1, 9)]) for _ in range(n)]
+    for s in range(30):
         run(items, seed=case * 1000 + s)
 
 
 def test_prefill_protocol_all_one_tile_and_all_long():
-    for items in ([1] * 20, [7] * 6, [2, 1, 1, 1, 2, 1, 3, 1, 1], [1, 2] * 8):
-        for s in range(100):
+    for items in ([1] * 20, [7] * 6, [2, 1, 1, 1, 2, 1, 3, 1, 1], [1, 2] * 8, [3, 4, 5, 1]):
+        for s in range(60):
             run(items, seed=s)
 
 
-def _late_o_free_wait(cta):
-    """The MMA thread with one planted mistake: it waits for the O buffer's
-    free phase one use too late."""
-    g = mma_thread(cta)
-    op = next(g)
-    while True:
-        if op[0] == "wait" and op[1].startswith("o_free"):
-            op = ("wait", op[1], op[2] + 1)
-        yield op
-        try:
-            op = next(g)
-        except StopIteration:
-            return
+def softmax_agent_v_clean_one_wait(cta, a):
+    """A softmax agent with one planted mistake: before cleaning V rows it
+    waits for the tile's V copy alone, not for the release of the slot's
+    previous copy."""
+    rng = random.Random(cta.rng.random())
+    T = 0
+    it = 0
+    item = yield from take(cta, 0, 1)
+    while item is not None:
+        nkv = cta.items[item]
+        for kt in range(nkv):
+            Tg = T + kt
+            yield ("wait", f"s_full{Tg % S_BUFS}", Tg // S_BUFS)
+            cta.s_read[Tg] = cta.s_read.get(Tg, 0) + 1
+            if rng.random() < 0.3:
+                yield ("wait", f"v_full{Tg % V_STAGES}", Tg // V_STAGES)
+            yield ("arrive", f"p_ready{Tg % S_BUFS}", 1)
+        item_n = yield from take(cta, it + 1, 1)
+        yield ("wait", "o_full", it)
+        cta.o_read[it] = cta.o_read.get(it, 0) + 1
+        T += nkv
+        item = item_n
+        it += 1
 
 
-def _single_arrival_owner(cta, wg):
-    """A softmax warpgroup with one planted mistake: finishing a one-tile item
-    alone, it arrives once on the O free barrier instead of for both shares."""
-    g = softmax_wg(cta, wg)
-    op = next(g)
-    while True:
-        if op[0] == "arrive" and op[1].startswith("o_free") and op[2] == 2:
-            op = ("arrive", op[1], 1)
-        yield op
-        try:
-            op = next(g)
-        except StopIteration:
-            return
-
-
-@pytest.mark.parametrize("mistake", ["late_o_free_wait", "single_arrival_owner"])
+@pytest.mark.parametrize("mistake", ["s_before_pv", "epilogue_late", "epilogue_on_v_free",
+                                     "v_clean_one_wait"])
 def test_model_catches_planted_protocol_mistakes(mistake):
     """The model is not vacuous: each planted mistake is caught (a wait at the
-    wrong phase, or a deadlock)."""
-    overrides = ({"mma": _late_o_free_wait} if mistake == "late_o_free_wait"
-                 else {"wg": _single_arrival_owner})
+    wrong phase, a TMEM hazard, or a deadlock)."""
+    if mistake == "s_before_pv":
+        kw = {"mma": lambda cta: mma_thread(cta, s_before_pv=True)}
+    elif mistake == "epilogue_late":
+        kw = {"agent": softmax_agent_epilogue_late}
+    elif mistake == "epilogue_on_v_free":
+        kw = {"agent": softmax_agent_epilogue_on_v_free}
+    else:
+        kw = {"agent": softmax_agent_v_clean_one_wait}
     with pytest.raises(AssertionError):
-        for s in range(50):
-            run([1, 1, 2, 1, 1, 3, 1], seed=s, **overrides)
+        for s in range(200):
+            run([1, 5, 2, 1, 6, 3, 1, 4], seed=s, **kw)
