@@ -79,19 +79,16 @@ int32_t encode_fn(EncodeTiledFn* fn) {
   return PKV_OK;
 }
 
-// 3-D bf16 map: dims {d0, d1, d2} (d0 contiguous), byte strides of dims 1, 2.
-int32_t make_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-                 uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
-                 CUtensorMapSwizzle swz) {
+// bf16 map of `rank` dims (dims[0] contiguous); strides[i] is the byte
+// stride of dims[i + 1].
+int32_t make_map_n(CUtensorMap* map, const void* base, uint32_t rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
   EncodeTiledFn fn;
   int32_t st = encode_fn(&fn);
   if (st != PKV_OK) return st;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {stride1, stride2};
-  const cuuint32_t box[3] = {b0, b1, b2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
@@ -99,6 +96,16 @@ int32_t make_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, u
     return PKV_ERR_CUDA;
   }
   return PKV_OK;
+}
+
+// 3-D bf16 map: dims {d0, d1, d2} (d0 contiguous), byte strides of dims 1, 2.
+int32_t make_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
+                 CUtensorMapSwizzle swz) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  return make_map_n(map, base, 3, dims, strides, box, swz);
 }
 
 bool block_size_ok(int32_t b) { return b == 8 || b == 16 || b == 32; }
@@ -457,11 +464,19 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   if (max_query_len > 1 || sh.num > 0) {
-    // pool for the tensor-core path: 64-element (128-byte) swizzled rows,
-    // 16 rows per copy (8 for 8-token blocks)
+    // pool for the tensor-core path, as {64-element half row, row within an
+    // 8-row group, d half, kv head, 8-row group}: one copy takes the K (or V)
+    // rows of one block and one kv head, and lands as 128-byte swizzled
+    // 8-row atoms ordered (group, d half, row)
     CUtensorMap kv_map_sw, q_map;
-    st = make_map(&kv_map_sw, kv_cache, D, Hkv, pool_rows, static_cast<uint64_t>(D) * 2,
-                  row_bytes, 64, 1, B == 8 ? 8u : 16u, CU_TENSOR_MAP_SWIZZLE_128B);
+    {
+      const cuuint64_t dims[5] = {64, 8, static_cast<cuuint64_t>(D / 64),
+                                  static_cast<cuuint64_t>(Hkv), pool_rows / 8};
+      const cuuint64_t strides[4] = {row_bytes, 128, static_cast<uint64_t>(D) * 2, row_bytes * 8};
+      const cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(D / 64), 1,
+                                 static_cast<cuuint32_t>(B / 8)};
+      st = make_map_n(&kv_map_sw, kv_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (st != PKV_OK) return st;
     st = make_map(&q_map, q, D, num_q_heads, num_tokens, static_cast<uint64_t>(D) * 2,
                   static_cast<uint64_t>(q_row_stride) * 2, 64, group, 128 / group,

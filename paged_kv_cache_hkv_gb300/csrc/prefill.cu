@@ -22,8 +22,9 @@
 // its half of O in TMEM only when the max grows by more than 2^8) and sum,
 // and writes P as bf16 pairs over the S buffer's columns with tcgen05.st.
 // A K-copy warp (3-slot ring) and a V-copy warp (2-slot ring) stream the
-// tiles by TMA (128-byte swizzle, one 16-key chunk of one kv head per copy,
-// two copies of 8 rows for 8-token blocks); one thread issues every MMA. The
+// tiles by TMA (128-byte swizzle, one copy per cache block and kv head: the
+// fewer and larger the copies, the faster one SM's copy engine goes); one
+// thread issues every S and another every PV. The
 // CTAs are persistent and take items from a counter; the roles meet only at
 // mbarriers, so consecutive items overlap.
 //
@@ -211,11 +212,12 @@ constexpr int kTileN = 128;    // keys per tile (8 chunks of 16)
 constexpr int kKStages = 3;    // K ring: global tile T uses slot T % 3
 constexpr int kVStages = 2;    // V ring: global tile T uses slot T % 2
 constexpr int kSBufs = 3;      // S (then P) buffers in TMEM: global tile T uses buffer T % 3
+static_assert(kKStages == kSBufs, "K slot T % 3 is freed by the commit of S buffer T % 3");
 constexpr uint32_t kTmemS = 128;  // TMEM columns: O at [0, D), S buffer b at [128 + 128b, +128)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kItemQ = 4;      // claimed work items in flight between the roles
 constexpr int kMetaReqs = 128;  // prefill requests whose metadata a CTA keeps in shared memory
-constexpr int kThreads = 352;  // 8 softmax warps + MMA warp + K-copy warp + V-copy warp
+constexpr int kThreads = 384;  // 8 softmax warps, S-MMA warp, K-copy warp, V-copy warp, PV-MMA warp
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (powers of two)
 
 template <int D>
@@ -223,7 +225,10 @@ struct PrefillLayout {
   static constexpr int DH = D / 64;                 // 64-element (128-byte) column chunks
   static constexpr uint32_t kChunk = kTileM * 128;  // 128 rows x 128 bytes = 16 KB
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kTileKV = DH * kChunk;         // K (or V) of one 128-key tile
+  // K (or V) of one 128-key tile: 16 groups of 8 keys, each DH 128-byte
+  // swizzled 8-row atoms (one per 64-element half of d), group-major
+  static constexpr uint32_t kGroupBytes = DH * 1024;
+  static constexpr uint32_t kTileKV = 16 * kGroupBytes;
   static constexpr uint32_t kK = kQ + DH * kChunk;         // K ring
   static constexpr uint32_t kV = kK + kKStages * kTileKV;  // V ring
   // request metadata: int4 (request, cached, first row, new tokens) [kMetaReqs],
@@ -260,17 +265,18 @@ struct PrefillShared {
   uint64_t q_full;               // Q tile of the item landed (TMA)
   uint64_t q_free;               // commit: the item's last S read Q
   uint64_t k_full[kKStages];     // K tile landed (TMA)
-  uint64_t k_free[kKStages];     // commit: the S that read the K slot is done
   uint64_t v_full[kVStages];     // V tile landed (TMA)
-  uint64_t v_free[kVStages];     // commit: the PV that read the V slot is done
-  uint64_t s_full[kSBufs];       // commit: S of the buffer's tile in TMEM
+  uint64_t s_full[kSBufs];       // commit: S of the buffer's tile in TMEM (and the
+                                 // K slot of the same index free: both rings have 3)
+  uint64_t pv_done[kSBufs];      // commit: PV of the buffer's tile done (its P read,
+                                 // its V slot free, O updated)
   uint64_t p_ready[kSBufs];      // 256 arrivals: P of the buffer's tile in TMEM, O
                                  // rescaled, V cleaned (and, for an item's first tile,
                                  // the previous item's O read)
   uint64_t o_full;               // commit: the item's last PV done
-  uint64_t drain;
+  uint64_t drain[2];
   uint64_t iq_full[kItemQ];      // item id j published in item_q[j % kItemQ]
-  uint64_t iq_free[kItemQ];      // 10 arrivals: every role has read it
+  uint64_t iq_free[kItemQ];      // 11 arrivals: every role has read it
   int item_q[kItemQ];
   uint32_t tmem;
   int abort;
@@ -439,23 +445,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_free, 1);
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(&sh.k_full[i], 1);
-      mbar_init(&sh.k_free[i], 1);
-    }
-    for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&sh.v_full[i], 1);
-      mbar_init(&sh.v_free[i], 1);
-    }
+    for (int i = 0; i < kKStages; ++i) mbar_init(&sh.k_full[i], 1);
+    for (int i = 0; i < kVStages; ++i) mbar_init(&sh.v_full[i], 1);
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.pv_done[i], 1);
       mbar_init(&sh.p_ready[i], 256);
     }
     mbar_init(&sh.o_full, 1);
-    mbar_init(&sh.drain, 1);
+    mbar_init(&sh.drain[0], 1);
+    mbar_init(&sh.drain[1], 1);
     for (int i = 0; i < kItemQ; ++i) {
       mbar_init(&sh.iq_full[i], 1);
-      mbar_init(&sh.iq_free[i], 10);
+      mbar_init(&sh.iq_free[i], 11);
     }
     sh.abort = 0;
     fence_barrier_init();
@@ -512,7 +514,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_v = warp == 10;
     const int S = is_v ? kVStages : kKStages;
     uint64_t* full = is_v ? sh.v_full : sh.k_full;
-    uint64_t* empty = is_v ? sh.v_free : sh.k_free;
     const uint32_t ring = is_v ? Lay::kV : Lay::kK;
     const int bsh = p.block_shift;
     const int E = kTileN >> bsh;  // table entries per tile
@@ -558,7 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kt = 0; kt < m.nkv; ++kt) {
         const int slot = static_cast<int>(T % S);
         if (T >= static_cast<uint32_t>(S)) {
-          ok = wait_or_abort(&empty[slot], ((T - S) / S) & 1u, abort_flag);
+          // K slot T % 3 is free once S(T-3) is done; V slot T % 2 once
+          // PV(T-2) is done
+          const uint32_t Tp = T - S;
+          ok = is_v ? wait_or_abort(&sh.pv_done[Tp % kSBufs], (Tp / kSBufs) & 1u, abort_flag)
+                    : wait_or_abort(&sh.s_full[Tp % kSBufs], (Tp / kSBufs) & 1u, abort_flag);
           if (!ok) break;
         }
         const int ka = m.kt0 + kt;  // key tile (keys ka*128 ..)
@@ -569,34 +574,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!is_v && (e << bsh) < m.kv_len && win_val < 0)
             atomicOr(&g_errors_prefill, kErrBlockRange);
         }
-        const int b = (ln / DH) & 7, dh = ln % DH;
-        // pool rows of one kv head: (block * 2 + k|v) * B + offset
-        int id0, id1 = -1, row0, row1 = 0;
-        if (bsh == 4) {
-          id0 = __shfl_sync(0xffffffffu, win_val, ka * 8 + b - win_base);
-          row0 = id0 * 32 + (is_v ? 16 : 0);
-        } else if (bsh == 5) {
-          id0 = __shfl_sync(0xffffffffu, win_val, ka * 4 + (b >> 1) - win_base);
-          row0 = id0 * 64 + (b & 1) * 16 + (is_v ? 32 : 0);
-        } else {
-          id0 = __shfl_sync(0xffffffffu, win_val, ka * 16 + 2 * b - win_base);
-          id1 = __shfl_sync(0xffffffffu, win_val, ka * 16 + 2 * b + 1 - win_base);
-          row0 = id0 * 16 + (is_v ? 8 : 0);
-          row1 = id1 * 16 + (is_v ? 8 : 0);
-        }
-        const bool mine0 = ln < 8 * DH && id0 >= 0;
-        const bool mine1 = ln < 8 * DH && id1 >= 0;
-        const uint32_t bytes = bsh == 3 ? (mine0 ? 1024u : 0u) + (mine1 ? 1024u : 0u)
-                                        : (mine0 ? 2048u : 0u);
-        const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes);
+        // lane j < E copies the K (or V) rows of table entry ka*E + j, kv
+        // head g: one box of B rows x D, 8-row groups of pool row
+        // (block * 2 + k|v) * B
+        const int id = __shfl_sync(0xffffffffu, win_val, (ka * E + (ln & (E - 1)) - win_base) & 31);
+        const bool mine = ln < E && id >= 0;
+        const uint32_t box = static_cast<uint32_t>(Lay::kGroupBytes) << (bsh - 3);
+        const uint32_t tx = __reduce_add_sync(0xffffffffu, mine ? box : 0u);
         if (ln == 0) {
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(&full[slot], tx);
         }
         __syncwarp();
-        unsigned char* dst = gbase + ring + slot * Lay::kTileKV + dh * Lay::kChunk + b * 2048;
-        if (mine0) tma_load_3d(dst, &kv_map, dh * 64, m.g, row0, &full[slot]);
-        if (mine1) tma_load_3d(dst + 1024, &kv_map, dh * 64, m.g, row1, &full[slot]);
+        if (mine)
+          tma_load_5d(gbase + ring + slot * Lay::kTileKV + ln * box, &kv_map, 0, 0, 0, m.g,
+                      ((id * 2 + (is_v ? 1 : 0)) << bsh) >> 3, &full[slot]);
         ++T;
       }
     }
@@ -608,9 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       if (!is_v && q_loads > 0) mbar_wait(&sh.q_full, (q_loads - 1) & 1u, kDrainLimitNs);
     }
-  } else if (warp == 8) {
-    // ================= MMA thread
+  } else if (warp == 8 || warp == 11) {
+    // ================= MMA threads: warp 8 issues every S, warp 11 every PV
     if ((tid & 31) == 0) {
+      const bool is_s = warp == 8;
       constexpr uint32_t idesc_qk = tc::idesc_bf16(kTileM, kTileN, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(kTileM, D, 1);
       uint32_t T = 0;  // tiles of earlier items
@@ -621,59 +614,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok || !valid(item)) break;
         const PrefillItem m = prefill_item(p, n_req, item, QT, meta, meta_prefix);
         const int nkv = m.nkv;
-        auto issue_s = [&](int kt) -> bool {  // S buffer of tile T+kt = Q K^T
-          const uint32_t Tk = T + kt;
-          const int slot = static_cast<int>(Tk % kKStages);
-          const uint32_t b = Tk % kSBufs;
-          if (!wait_or_abort(&sh.k_full[slot], (Tk / kKStages) & 1u, abort_flag)) return false;
-          tc::fence_after_sync();
+        if (is_s) {
+          ok = wait_or_abort(&sh.q_full, it & 1u, abort_flag);
+          for (int kt = 0; ok && kt < nkv; ++kt) {
+            // S(Tk) = Q K^T into buffer Tk % 3, once PV(Tk-3) has read the
+            // P that the buffer holds and K(Tk) has landed
+            const uint32_t Tk = T + kt;
+            const uint32_t b = Tk % kSBufs;
+            if (Tk >= static_cast<uint32_t>(kSBufs))
+              ok = wait_or_abort(&sh.pv_done[b], ((Tk - kSBufs) / kSBufs) & 1u, abort_flag);
+            if (ok) ok = wait_or_abort(&sh.k_full[b], (Tk / kKStages) & 1u, abort_flag);
+            if (!ok) break;
+            tc::fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * Lay::kChunk + (kk & 3) * 32;
-            const uint64_t a = tc::sw128_desc(base + Lay::kQ + off, 16, 1024);
-            const uint64_t bd = tc::sw128_desc(base + Lay::kK + slot * Lay::kTileKV + off, 16, 1024);
-            tc::mma_bf16(tmem + kTmemS + kTileN * b, a, bd, idesc_qk, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t sub = (kk & 3) * 32;  // 16 elements within the 64-element half
+              const uint64_t a = tc::sw128_desc(base + Lay::kQ + (kk >> 2) * Lay::kChunk + sub, 16, 1024);
+              const uint64_t bd = tc::sw128_desc(
+                  base + Lay::kK + b * Lay::kTileKV + (kk >> 2) * 1024 + sub, 16, Lay::kGroupBytes);
+              tc::mma_bf16(tmem + kTmemS + kTileN * b, a, bd, idesc_qk, kk > 0);
+            }
+            tc::commit(&sh.s_full[b]);  // S in TMEM, and the K slot free
+            if (kt == nkv - 1) tc::commit(&sh.q_free);
           }
-          tc::commit(&sh.s_full[b]);
-          tc::commit(&sh.k_free[slot]);
-          if (kt == nkv - 1) tc::commit(&sh.q_free);
-          return true;
-        };
-        auto issue_pv = [&](int kt) -> bool {  // O += P V, P read from the tile's S buffer
-          const uint32_t Tv = T + kt;
-          const int slot = static_cast<int>(Tv % kVStages);
-          const uint32_t b = Tv % kSBufs;
-          if (!wait_or_abort(&sh.v_full[slot], (Tv / kVStages) & 1u, abort_flag)) return false;
-          tc::fence_after_sync();
-          const uint32_t vbase = base + Lay::kV + slot * Lay::kTileKV;
+        } else {
+          for (int kt = 0; ok && kt < nkv; ++kt) {
+            // O += P V for tile Tg, P read from its S buffer. The first PV of
+            // an item overwrites O: the softmax warps publish P of an item's
+            // first tile only after their epilogue of the previous item has
+            // read O.
+            const uint32_t Tg = T + kt;
+            const uint32_t b = Tg % kSBufs;
+            const int slot = static_cast<int>(Tg % kVStages);
+            ok = wait_or_abort(&sh.p_ready[b], (Tg / kSBufs) & 1u, abort_flag);
+            if (ok) ok = wait_or_abort(&sh.v_full[slot], (Tg / kVStages) & 1u, abort_flag);
+            if (!ok) break;
+            tc::fence_after_sync();
+            const uint32_t vbase = base + Lay::kV + slot * Lay::kTileKV;
 #pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk) {
-            const uint64_t bd = tc::sw128_desc(vbase + kk * 2048, Lay::kChunk, 1024);
-            tc::mma_bf16_ts(tmem, tmem + kTmemS + kTileN * b + kk * 8u, bd, idesc_pv,
-                            (kt > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kTileN / 16; ++kk) {
+              // keys 16kk .. 16kk+15: two 8-key groups (SBO), d halves 1 KB apart (LBO)
+              const uint64_t bd = tc::sw128_desc(vbase + kk * 2 * Lay::kGroupBytes, 1024, Lay::kGroupBytes);
+              tc::mma_bf16_ts(tmem, tmem + kTmemS + kTileN * b + kk * 8u, bd, idesc_pv,
+                              (kt > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::commit(&sh.pv_done[b]);  // P's buffer and the V slot free
+            if (kt == nkv - 1) tc::commit(&sh.o_full);  // the item's O is complete
           }
-          tc::commit(&sh.v_free[slot]);
-          if (kt == nkv - 1) tc::commit(&sh.o_full);  // the item's O is complete
-          return true;
-        };
-        ok = wait_or_abort(&sh.q_full, it & 1u, abort_flag);
-        for (int kt = 0; ok && kt < kSBufs && kt < nkv; ++kt) ok = issue_s(kt);
-        for (int kt = 0; ok && kt < nkv; ++kt) {
-          // the first PV of an item overwrites O: the softmax warps publish
-          // P of the item's first tile only after their epilogue of the
-          // previous item has read O
-          const uint32_t Tg = T + kt;
-          ok = wait_or_abort(&sh.p_ready[Tg % kSBufs], (Tg / kSBufs) & 1u, abort_flag);
-          if (ok) ok = issue_pv(kt);
-          // PV(kt) was issued first and MMAs run in issue order, so S(kt+3)
-          // overwrites P(kt) only after PV(kt) read it
-          if (ok && kt + kSBufs < nkv) ok = issue_s(kt + kSBufs);
         }
         T += nkv;
       }
-      // every MMA (and the arrivals of its commits) done before teardown
-      tc::commit(&sh.drain);
-      mbar_wait(&sh.drain, 0, ok ? kWaitLimitNs : kDrainLimitNs);
+      // every MMA of this thread (and the arrivals of its commits) done
+      // before teardown
+      tc::commit(&sh.drain[is_s ? 0 : 1]);
+      mbar_wait(&sh.drain[is_s ? 0 : 1], 0, ok ? kWaitLimitNs : kDrainLimitNs);
     }
     __syncwarp();
   } else {
@@ -753,10 +747,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= alpha;
           m_run = m_new;
           if (kt > 0) {
-            // O holds PV of the item's earlier tiles; the last of them,
-            // PV(Tg-1), is done when its V slot is released
+            // O holds PV of the item's earlier tiles; the last of them is PV(Tg-1)
             const uint32_t Tp = Tg - 1;
-            ok = wait_or_abort(&sh.v_free[Tp % kVStages], (Tp / kVStages) & 1u, abort_flag);
+            ok = wait_or_abort(&sh.pv_done[Tp % kSBufs], (Tp / kSBufs) & 1u, abort_flag);
             if (!ok) break;
             tc::fence_after_sync();
 #pragma unroll 1
@@ -800,13 +793,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S(Tg) done only implies PV(Tg-3) done, so the slot's copy
           // barrier may be anywhere from V(Tg-2) pending to V(Tg) landed;
           // once PV(Tg-2) is done (slot released) it is V(Tg) pending or landed
-          if (Tg >= static_cast<uint32_t>(kVStages))
-            ok = wait_or_abort(&sh.v_free[slot], ((Tg - kVStages) / kVStages) & 1u, abort_flag);
+          if (Tg >= static_cast<uint32_t>(kVStages)) {
+            const uint32_t Tp = Tg - kVStages;
+            ok = wait_or_abort(&sh.pv_done[Tp % kSBufs], (Tp / kSBufs) & 1u, abort_flag);
+          }
           if (ok) ok = wait_or_abort(&sh.v_full[slot], (Tg / kVStages) & 1u, abort_flag);
           if (!ok) break;
           if (ch < DH && (ka * kTileN + row >= m.kv_len || !(mask >> (row >> 4) & 1u))) {
             uint4* v4 = reinterpret_cast<uint4*>(gbase + Lay::kV + slot * Lay::kTileKV +
-                                                 ch * Lay::kChunk + row * 128);
+                                                 (row >> 3) * Lay::kGroupBytes + ch * 1024 +
+                                                 (row & 7) * 128);
 #pragma unroll
             for (int x = 0; x < 8; ++x) v4[x] = make_uint4(0, 0, 0, 0);
           }

@@ -2,11 +2,14 @@
 
 Every role of a prefill CTA is restated as the sequence of mbarrier waits
 and arrivals it performs:
-- the K-copy warp claims items and copies Q and K tiles;
-- the V-copy warp copies V tiles;
-- the MMA thread issues, per item, S(0), S(1), S(2), then PV(kt) and
-  S(kt+3) for each tile kt, with S of tile T in TMEM buffer T % 3 and one
-  O accumulator;
+- the K-copy warp claims items and copies Q and K tiles (K slot T % 3 is
+  refilled once S(T-3) is done);
+- the V-copy warp copies V tiles (V slot T % 2 is refilled once PV(T-2) is
+  done);
+- the S thread issues S(T) into TMEM buffer T % 3 once PV(T-3) is done and
+  K(T) landed;
+- the PV thread issues PV(T) once P(T) is published and V(T) landed, into
+  one O accumulator;
 - the softmax warps (modelled as N_SOFTMAX independent agents, each owning
   some query rows) take every tile of every item, sometimes rescale O
   (after PV of the previous tile is done), sometimes clean V rows (after the
@@ -14,8 +17,9 @@ and arrivals it performs:
   is done.
 
 Copies and MMA completions are asynchronous events. Copies complete in any
-order; MMA commits complete in issue order. Random item lists run under
-many random interleavings, and the optional waits are taken at random.
+order; each MMA thread's commits complete in its issue order. Random item
+lists run under many random interleavings, and the optional waits are taken
+at random.
 
 Each wait names the barrier phase it means (from the role's own counters),
 and a parity wait is only correct if the barrier is then at that phase or
@@ -33,9 +37,9 @@ import pytest
 
 K_STAGES, V_STAGES, S_BUFS, ITEM_Q = 3, 2, 3, 4
 N_SOFTMAX = 4
-# arrivals per phase: item queue slots are released by the MMA thread, the
-# V-copy warp and every softmax agent
-IQ_FREE_ARRIVALS = 2 + N_SOFTMAX
+# arrivals per phase: item queue slots are released by the two MMA threads,
+# the V-copy warp and every softmax agent
+IQ_FREE_ARRIVALS = 3 + N_SOFTMAX
 
 
 class Barrier:
@@ -63,12 +67,11 @@ class Cta:
         mk("q_free", 1)
         for i in range(K_STAGES):
             mk(f"k_full{i}", 1)
-            mk(f"k_free{i}", 1)
         for i in range(V_STAGES):
             mk(f"v_full{i}", 1)
-            mk(f"v_free{i}", 1)
         for i in range(S_BUFS):
             mk(f"s_full{i}", 1)
+            mk(f"pv_done{i}", 1)
             mk(f"p_ready{i}", N_SOFTMAX)
         mk("o_full", 1)
         for i in range(ITEM_Q):
@@ -78,7 +81,7 @@ class Cta:
         self.item_q = [None] * ITEM_Q
         self.next_claim = 0
         self.tma = []  # copies in flight: (barrier) -- complete in any order
-        self.mma = []  # MMA commits in flight -- complete in issue order
+        self.mma = {"s": [], "pv": []}  # each MMA thread's commits, in issue order
         # TMEM bookkeeping for the hazard checks
         self.s_read = {}     # tile -> agents that read its S (and wrote P)
         self.pv_issued = set()
@@ -93,9 +96,9 @@ class Cta:
 
 # Operations a role yields: ("wait", barrier, phase index), ("arrive", barrier, n),
 # ("tma", barrier), ("commit", barrier), ("pv", tile) -- a PV whose completion
-# is recorded in issue order with the commits.
+# is recorded in issue order with that thread's commits.
 
-def k_warp(cta):
+def k_warp(cta, phase_slip=0):
     T = 0
     it = 0
     while True:
@@ -113,7 +116,8 @@ def k_warp(cta):
         for _ in range(cta.items[item]):
             s = T % K_STAGES
             if T >= K_STAGES:
-                yield ("wait", f"k_free{s}", (T - K_STAGES) // K_STAGES)
+                Tp = T - K_STAGES
+                yield ("wait", f"s_full{Tp % S_BUFS}", Tp // S_BUFS + phase_slip)
             yield ("tma", f"k_full{s}")
             T += 1
         it += 1
@@ -137,13 +141,14 @@ def v_warp(cta):
         for _ in range(cta.items[item]):
             s = T % V_STAGES
             if T >= V_STAGES:
-                yield ("wait", f"v_free{s}", (T - V_STAGES) // V_STAGES)
+                Tp = T - V_STAGES
+                yield ("wait", f"pv_done{Tp % S_BUFS}", Tp // S_BUFS)
             yield ("tma", f"v_full{s}")
             T += 1
         it += 1
 
 
-def mma_thread(cta, s_before_pv=False):
+def s_thread(cta, skip_pv_wait=False):
     T = 0
     it = 0
     while True:
@@ -151,52 +156,49 @@ def mma_thread(cta, s_before_pv=False):
         if item is None:
             return
         nkv = cta.items[item]
-
-        def issue_s(kt):
+        yield ("wait", "q_full", it)
+        for kt in range(nkv):
             Tk = T + kt
-            s = Tk % K_STAGES
-            yield ("wait", f"k_full{s}", Tk // K_STAGES)
+            if Tk >= S_BUFS and not skip_pv_wait:
+                Tp = Tk - S_BUFS
+                yield ("wait", f"pv_done{Tp % S_BUFS}", Tp // S_BUFS)
+            yield ("wait", f"k_full{Tk % K_STAGES}", Tk // K_STAGES)
             # S(Tk) overwrites buffer Tk % 3: S(Tk-3) read by every agent and
-            # P(Tk-3) read by its PV (issued earlier: MMAs run in order)
+            # P(Tk-3) read by its PV
             if Tk >= S_BUFS:
                 assert cta.s_read.get(Tk - S_BUFS, 0) == N_SOFTMAX, f"S({Tk}) over unread S"
-                assert (Tk - S_BUFS) in cta.pv_issued, f"S({Tk}) before PV({Tk - S_BUFS})"
-            yield ("commit", f"s_full{Tk % S_BUFS}")
-            yield ("commit", f"k_free{s}")
+                assert (Tk - S_BUFS) in cta.pv_done, f"S({Tk}) before PV({Tk - S_BUFS}) done"
+            yield ("commit", "s", f"s_full{Tk % S_BUFS}")
             if kt == nkv - 1:
-                yield ("commit", "q_free")
-
-        def issue_pv(kt):
-            Tv = T + kt
-            s = Tv % V_STAGES
-            yield ("wait", f"v_full{s}", Tv // V_STAGES)
-            if kt == 0 and it > 0:  # O is overwritten: the last item's O read by all
-                assert cta.o_read.get(it - 1, 0) == N_SOFTMAX, f"item {it} PV(0) over unread O"
-            cta.pv_issued.add(Tv)
-            yield ("pv", Tv)
-            yield ("commit", f"v_free{s}")
-            if kt == nkv - 1:
-                yield ("commit", "o_full")
-
-        yield ("wait", "q_full", it)
-        for kt in range(min(S_BUFS, nkv)):
-            yield from issue_s(kt)
-        for kt in range(nkv):
-            Tg = T + kt
-            if s_before_pv and kt + S_BUFS < nkv:
-                yield ("wait", f"p_ready{Tg % S_BUFS}", Tg // S_BUFS)
-                yield from issue_s(kt + S_BUFS)
-                yield from issue_pv(kt)
-                continue
-            yield ("wait", f"p_ready{Tg % S_BUFS}", Tg // S_BUFS)
-            yield from issue_pv(kt)
-            if kt + S_BUFS < nkv:
-                yield from issue_s(kt + S_BUFS)
+                yield ("commit", "s", "q_free")
         T += nkv
         it += 1
 
 
-def softmax_agent(cta, a, epilogue_late=False):
+def pv_thread(cta):
+    T = 0
+    it = 0
+    while True:
+        item = yield from take(cta, it, 1)
+        if item is None:
+            return
+        nkv = cta.items[item]
+        for kt in range(nkv):
+            Tg = T + kt
+            yield ("wait", f"p_ready{Tg % S_BUFS}", Tg // S_BUFS)
+            yield ("wait", f"v_full{Tg % V_STAGES}", Tg // V_STAGES)
+            if kt == 0 and it > 0:  # O is overwritten: the last item's O read by all
+                assert cta.o_read.get(it - 1, 0) == N_SOFTMAX, f"item {it} PV(0) over unread O"
+            cta.pv_issued.add(Tg)
+            yield ("pv", Tg)
+            yield ("commit", "pv", f"pv_done{Tg % S_BUFS}")
+            if kt == nkv - 1:
+                yield ("commit", "pv", "o_full")
+        T += nkv
+        it += 1
+
+
+def softmax_agent(cta, a, v_clean_one_wait=False):
     rng = random.Random(cta.rng.random())
     T = 0
     it = 0
@@ -205,22 +207,20 @@ def softmax_agent(cta, a, epilogue_late=False):
         nkv = cta.items[item]
         for kt in range(nkv):
             Tg = T + kt
-            if epilogue_late and kt == 0 and it > 0:
-                pass  # (the planted mistake publishes P before the epilogue below)
             yield ("wait", f"s_full{Tg % S_BUFS}", Tg // S_BUFS)
             cta.s_read[Tg] = cta.s_read.get(Tg, 0) + 1
             if kt > 0 and rng.random() < 0.3:  # the max grew: rescale O
                 Tp = Tg - 1
-                yield ("wait", f"v_free{Tp % V_STAGES}", Tp // V_STAGES)
+                yield ("wait", f"pv_done{Tp % S_BUFS}", Tp // S_BUFS)
                 assert Tp in cta.pv_done, f"rescale at {Tg} before PV({Tp}) done"
                 assert Tg not in cta.pv_issued, f"rescale at {Tg} after PV({Tg}) issued"
             if rng.random() < 0.3:  # a ragged tile: clean V rows after the copy
                 # PV(Tg-2) first: S(Tg) only implies PV(Tg-3) done, so the V
                 # slot's barrier may be anywhere from V(Tg-2) pending to V(Tg)
                 # landed; once PV(Tg-2) is done it is at V(Tg) pending or landed
-                if Tg >= V_STAGES:
+                if Tg >= V_STAGES and not v_clean_one_wait:
                     Tp = Tg - V_STAGES
-                    yield ("wait", f"v_free{Tp % V_STAGES}", Tp // V_STAGES)
+                    yield ("wait", f"pv_done{Tp % S_BUFS}", Tp // S_BUFS)
                 yield ("wait", f"v_full{Tg % V_STAGES}", Tg // V_STAGES)
             yield ("arrive", f"p_ready{Tg % S_BUFS}", 1)
         item_n = yield from take(cta, it + 1, 1)
@@ -235,7 +235,6 @@ def softmax_agent(cta, a, epilogue_late=False):
 def softmax_agent_epilogue_late(cta, a):
     """A softmax agent with one planted mistake: it publishes P of an item's
     first tile before its epilogue of the previous item has read O."""
-    rng = random.Random(cta.rng.random())
     T = 0
     it = 0
     pending_epilogue = None
@@ -261,40 +260,19 @@ def softmax_agent_epilogue_late(cta, a):
         cta.o_read[pending_epilogue] = cta.o_read.get(pending_epilogue, 0) + 1
 
 
-def softmax_agent_epilogue_on_v_free(cta, a):
-    """A softmax agent with one planted mistake: the epilogue waits for the
-    last PV through its V slot's release instead of the item's O barrier."""
-    T = 0
-    it = 0
-    item = yield from take(cta, 0, 1)
-    while item is not None:
-        nkv = cta.items[item]
-        for kt in range(nkv):
-            Tg = T + kt
-            yield ("wait", f"s_full{Tg % S_BUFS}", Tg // S_BUFS)
-            cta.s_read[Tg] = cta.s_read.get(Tg, 0) + 1
-            yield ("arrive", f"p_ready{Tg % S_BUFS}", 1)
-        item_n = yield from take(cta, it + 1, 1)
-        Tl = T + nkv - 1
-        yield ("wait", f"v_free{Tl % V_STAGES}", Tl // V_STAGES)
-        assert Tl in cta.pv_done
-        cta.o_read[it] = cta.o_read.get(it, 0) + 1
-        T += nkv
-        item = item_n
-        it += 1
-
-
-def run(items, seed, mma=None, agent=None):
+def run(items, seed, roles_override=None):
     rng = random.Random(seed)
     cta = Cta(items, rng)
-    agent = agent or softmax_agent
-    roles = {"k": k_warp(cta), "v": v_warp(cta), "mma": (mma or mma_thread)(cta)}
+    ro = roles_override or {}
+    roles = {"k": ro.get("k", k_warp)(cta), "v": v_warp(cta), "s": ro.get("s", s_thread)(cta),
+             "pv": pv_thread(cta)}
+    agent = ro.get("agent", softmax_agent)
     for a in range(N_SOFTMAX):
         roles[f"sm{a}"] = agent(cta, a)
     pending = {name: next(g) for name, g in roles.items()}
     done = set()
     steps = 0
-    while len(done) < len(roles) or cta.tma or cta.mma:
+    while len(done) < len(roles) or cta.tma or cta.mma["s"] or cta.mma["pv"]:
         steps += 1
         assert steps < 400000, "model did not finish"
         runnable = []
@@ -310,15 +288,15 @@ def run(items, seed, mma=None, agent=None):
                 if bar.phases == k:
                     continue  # blocked
             runnable.append(name)
-        events = (["copy done"] if cta.tma else []) + (["mma done"] if cta.mma else [])
+        events = (["copy done"] if cta.tma else []) + [f"mma {q}" for q in ("s", "pv") if cta.mma[q]]
         choices = runnable + events
         assert choices, f"deadlock: {pending}"
         c = rng.choice(choices)
         if c == "copy done":
             cta.b[cta.tma.pop(rng.randrange(len(cta.tma)))].arrive()
             continue
-        if c == "mma done":
-            ev = cta.mma.pop(0)
+        if c.startswith("mma "):
+            ev = cta.mma[c[4:]].pop(0)
             if isinstance(ev, tuple):
                 cta.pv_done.add(ev[1])
             else:
@@ -330,9 +308,9 @@ def run(items, seed, mma=None, agent=None):
         elif op[0] == "tma":
             cta.tma.append(op[1])
         elif op[0] == "commit":
-            cta.mma.append(op[1])
+            cta.mma[op[1]].append(op[2])
         elif op[0] == "pv":
-            cta.mma.append(("pv", op[1]))
+            cta.mma["pv"].append(("pv", op[1]))
         try:
             pending[c] = roles[c].send(None)
         except StopIteration:
@@ -360,44 +338,22 @@ def test_prefill_protocol_all_one_tile_and_all_long():
             run(items, seed=s)
 
 
-def softmax_agent_v_clean_one_wait(cta, a):
-    """A softmax agent with one planted mistake: before cleaning V rows it
-    waits for the tile's V copy alone, not for the release of the slot's
-    previous copy."""
-    rng = random.Random(cta.rng.random())
-    T = 0
-    it = 0
-    item = yield from take(cta, 0, 1)
-    while item is not None:
-        nkv = cta.items[item]
-        for kt in range(nkv):
-            Tg = T + kt
-            yield ("wait", f"s_full{Tg % S_BUFS}", Tg // S_BUFS)
-            cta.s_read[Tg] = cta.s_read.get(Tg, 0) + 1
-            if rng.random() < 0.3:
-                yield ("wait", f"v_full{Tg % V_STAGES}", Tg // V_STAGES)
-            yield ("arrive", f"p_ready{Tg % S_BUFS}", 1)
-        item_n = yield from take(cta, it + 1, 1)
-        yield ("wait", "o_full", it)
-        cta.o_read[it] = cta.o_read.get(it, 0) + 1
-        T += nkv
-        item = item_n
-        it += 1
+PLANTED = {
+    # S issued as soon as K landed, without waiting for PV(T-3)
+    "s_without_pv_wait": {"s": lambda cta: s_thread(cta, skip_pv_wait=True)},
+    # P of an item's first tile published before the epilogue read O
+    "epilogue_late": {"agent": softmax_agent_epilogue_late},
+    # V rows cleaned after a wait for the tile's own copy alone
+    "v_clean_one_wait": {"agent": lambda cta, a: softmax_agent(cta, a, v_clean_one_wait=True)},
+    # the K-copy warp waits for the phase after the one it means
+    "k_slot_phase_late": {"k": lambda cta: k_warp(cta, phase_slip=1)},
+}
 
 
-@pytest.mark.parametrize("mistake", ["s_before_pv", "epilogue_late", "epilogue_on_v_free",
-                                     "v_clean_one_wait"])
+@pytest.mark.parametrize("mistake", sorted(PLANTED))
 def test_model_catches_planted_protocol_mistakes(mistake):
     """The model is not vacuous: each planted mistake is caught (a wait at the
     wrong phase, a TMEM hazard, or a deadlock)."""
-    if mistake == "s_before_pv":
-        kw = {"mma": lambda cta: mma_thread(cta, s_before_pv=True)}
-    elif mistake == "epilogue_late":
-        kw = {"agent": softmax_agent_epilogue_late}
-    elif mistake == "epilogue_on_v_free":
-        kw = {"agent": softmax_agent_epilogue_on_v_free}
-    else:
-        kw = {"agent": softmax_agent_v_clean_one_wait}
     with pytest.raises(AssertionError):
         for s in range(200):
-            run([1, 5, 2, 1, 6, 3, 1, 4], seed=s, **kw)
+            run([1, 5, 2, 1, 6, 3, 1, 4], seed=s, roles_override=PLANTED[mistake])
