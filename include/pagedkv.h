@@ -197,6 +197,33 @@ int32_t pkv_paged_kv_write(void* kv_cache, const void* key, const void* value,
                            pkv_cache_layout layout, void* stream);
 
 /*
+ * pkv_slot_mapping_and_write -- pkv_slot_mapping and pkv_paged_kv_write fused
+ * into one kernel (the pages compute the slot mapping on the device and then
+ * store the rows: "vllm v1 源码精读（三）" §3.4; "vLLM 架构源码解析（一）"
+ * §3.3.3 step 2). Each new token's slot is computed as pkv_slot_mapping
+ * defines it, and its K and V rows are stored there as pkv_paged_kv_write
+ * does, with one launch instead of two.
+ *
+ * slot_mapping  out, device int64 [num_tokens], or NULL (not stored). For a
+ *               non-decreasing query_start_loc it receives exactly what
+ *               pkv_slot_mapping writes; a token with slot -1 is not written.
+ *               Tokens are assigned to requests by searching
+ *               query_start_loc, so where it decreases (inconsistent
+ *               lengths, PKV_DEVERR_LENGTHS) the rows that get -1 may differ
+ *               from pkv_slot_mapping's.
+ * kv_cache, key, value, key_row_stride, value_row_stride, layout
+ *               as pkv_paged_kv_write (layout.num_blocks is the range check).
+ * block_table, max_blocks_per_req, query_start_loc, num_computed_tokens,
+ * num_reqs, num_tokens   as pkv_slot_mapping.
+ */
+int32_t pkv_slot_mapping_and_write(void* kv_cache, const void* key, const void* value,
+                                   int64_t key_row_stride, int64_t value_row_stride,
+                                   int64_t* slot_mapping, const int32_t* block_table,
+                                   int32_t max_blocks_per_req, const int32_t* query_start_loc,
+                                   const int32_t* num_computed_tokens, int32_t num_reqs,
+                                   int32_t num_tokens, pkv_cache_layout layout, void* stream);
+
+/*
  * pkv_copy_blocks -- copy whole blocks (K and V of every kv head) between two
  * pools of the same block shape:
  *   - copy-on-write: before a new token is written into a block that other

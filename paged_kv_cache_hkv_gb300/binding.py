@@ -60,6 +60,9 @@ _SIGNATURES = {
     "pkv_get_device_errors": (c_i32, [ctypes.POINTER(c_u32), c_i32, c_void_p]),
     "pkv_copy_blocks": (c_i32, [c_void_p, c_i32, c_void_p, c_i32, c_void_p, c_i32,
                                 pkv_cache_layout, c_void_p]),
+    "pkv_slot_mapping_and_write": (c_i32, [c_void_p, c_void_p, c_void_p, c_i64, c_i64, c_void_p,
+                                           c_void_p, c_i32, c_void_p, c_void_p, c_i32, c_i32,
+                                           pkv_cache_layout, c_void_p]),
     "pkv_paged_attention_static_workspace": (
         c_i32, [c_void_p, c_void_p, c_i64, c_void_p, c_void_p, c_i32, c_void_p, c_void_p,
                 c_void_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_float, pkv_cache_layout,
@@ -163,6 +166,31 @@ def pkv_paged_kv_write(kv_cache, key, value, slot_mapping, stream=None):
     _check("pkv_paged_kv_write", load().pkv_paged_kv_write(
         _ptr(kv_cache), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
         _ptr(slot_mapping), key.shape[0], lay, _stream(stream)))
+
+
+def pkv_slot_mapping_and_write(kv_cache, key, value, block_table, query_start_loc,
+                               num_computed_tokens, slot_mapping=None, stream=None):
+    """Slot mapping and cache write in one launch (see pagedkv.h). slot_mapping
+    (int64 [T]) receives the slots when given."""
+    for t, n in ((kv_cache, "kv_cache"), (key, "key"), (value, "value")):
+        _require(t, torch.bfloat16, n)
+    for t, n in ((block_table, "block_table"), (query_start_loc, "query_start_loc"),
+                 (num_computed_tokens, "num_computed_tokens")):
+        _require(t, torch.int32, n)
+    if slot_mapping is not None:
+        _require(slot_mapping, torch.int64, "slot_mapping")
+    for t, n in ((key, "key"), (value, "value")):
+        if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} must be [T, Hkv, D] with contiguous rows")
+    if not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous")
+    lay = layout_of(kv_cache)
+    _check("pkv_slot_mapping_and_write", load().pkv_slot_mapping_and_write(
+        _ptr(kv_cache), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
+        _ptr(slot_mapping), _ptr(block_table), block_table.shape[1], _ptr(query_start_loc),
+        _ptr(num_computed_tokens), num_computed_tokens.shape[0], key.shape[0], lay,
+        _stream(stream)))
+    return slot_mapping
 
 
 def pkv_copy_blocks(dst_pool, src_pool, block_pairs, stream=None):
@@ -280,7 +308,8 @@ def pkv_paged_attention_static_workspace(out, q, kv_cache, block_table, seq_lens
 
 
 class StepCalls:
-    """The three calls of one step -- pkv_slot_mapping, pkv_paged_kv_write,
+    """The calls of one step -- pkv_slot_mapping, pkv_paged_kv_write,
+    pkv_paged_attention, or with fused_write pkv_slot_mapping_and_write then
     pkv_paged_attention -- with their arguments checked and marshalled once.
 
     A serving loop that keeps its step buffers (as DeviceStep does) pays the
@@ -292,7 +321,7 @@ class StepCalls:
     def __init__(self, *, slot_mapping, block_table, query_start_loc, num_computed_tokens,
                  kv_cache, key, value, out, q, seq_lens, max_query_len: int,
                  max_seq_len: int, scale: float, workspace, decode_splits=None,
-                 shared_prefix=None):
+                 shared_prefix=None, fused_write=False):
         _require(slot_mapping, torch.int64, "slot_mapping")
         for t, n in ((block_table, "block_table"), (query_start_loc, "query_start_loc"),
                      (num_computed_tokens, "num_computed_tokens"), (seq_lens, "seq_lens")):
@@ -315,6 +344,11 @@ class StepCalls:
         self.write_args = (
             _ptr(kv_cache), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
             _ptr(slot_mapping), key.shape[0], lay)
+        self.fused_write = bool(fused_write)
+        self.mapped_write_args = (
+            _ptr(kv_cache), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
+            _ptr(slot_mapping), _ptr(block_table), block_table.shape[1], _ptr(query_start_loc),
+            _ptr(num_computed_tokens), num_computed_tokens.shape[0], key.shape[0], lay)
         self.attn_args = (
             _ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), _ptr(block_table),
             block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc),
@@ -335,6 +369,11 @@ class StepCalls:
         if status:
             raise PagedKVError("pkv_paged_kv_write", status)
 
+    def slot_map_and_write(self, stream=None):
+        status = self.lib.pkv_slot_mapping_and_write(*self.mapped_write_args, _stream(stream))
+        if status:
+            raise PagedKVError("pkv_slot_mapping_and_write", status)
+
     def attend(self, stream=None):
         status = self.lib.pkv_paged_attention(*self.attn_args, _stream(stream))
         if status:
@@ -343,12 +382,17 @@ class StepCalls:
     def run(self, stream=None):
         st = _stream(stream)
         lib = self.lib
-        status = lib.pkv_slot_mapping(*self.slot_args, st)
-        if status:
-            raise PagedKVError("pkv_slot_mapping", status)
-        status = lib.pkv_paged_kv_write(*self.write_args, st)
-        if status:
-            raise PagedKVError("pkv_paged_kv_write", status)
+        if self.fused_write:
+            status = lib.pkv_slot_mapping_and_write(*self.mapped_write_args, st)
+            if status:
+                raise PagedKVError("pkv_slot_mapping_and_write", status)
+        else:
+            status = lib.pkv_slot_mapping(*self.slot_args, st)
+            if status:
+                raise PagedKVError("pkv_slot_mapping", status)
+            status = lib.pkv_paged_kv_write(*self.write_args, st)
+            if status:
+                raise PagedKVError("pkv_paged_kv_write", status)
         status = lib.pkv_paged_attention(*self.attn_args, st)
         if status:
             raise PagedKVError("pkv_paged_attention", status)

@@ -291,6 +291,36 @@ int32_t pkv_paged_kv_write(void* kv_cache, const void* key, const void* value,
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_write launch");
 }
 
+int32_t pkv_slot_mapping_and_write(void* kv_cache, const void* key, const void* value,
+                                   int64_t key_row_stride, int64_t value_row_stride,
+                                   int64_t* slot_mapping, const int32_t* block_table,
+                                   int32_t max_blocks_per_req, const int32_t* query_start_loc,
+                                   const int32_t* num_computed_tokens, int32_t num_reqs,
+                                   int32_t num_tokens, pkv_cache_layout layout, void* stream) {
+  int32_t st = check_layout(layout);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0 || num_reqs < 0 || max_blocks_per_req < 0) return PKV_ERR_BAD_SHAPE;
+  const int64_t row = static_cast<int64_t>(layout.num_kv_heads) * layout.head_dim;
+  if (key_row_stride == 0) key_row_stride = row;
+  if (value_row_stride == 0) value_row_stride = row;
+  if (key_row_stride < row || value_row_stride < row) return PKV_ERR_BAD_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!kv_cache || !key || !value || !query_start_loc) return PKV_ERR_NULL_POINTER;
+  if (num_reqs > 0 && (!block_table || !num_computed_tokens)) return PKV_ERR_NULL_POINTER;
+  if (!aligned16(kv_cache) || !aligned16(key) || !aligned16(value) || (key_row_stride % 8) ||
+      (value_row_stride % 8))
+    return PKV_ERR_MISALIGNED;
+  DeviceInfo* d;
+  st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = pkv::launch_mapped_write(
+      kv_cache, key, value, key_row_stride, value_row_stride, slot_mapping, block_table,
+      max_blocks_per_req, query_start_loc, num_computed_tokens, num_reqs, num_tokens,
+      layout.num_blocks, layout.block_size, layout.num_kv_heads, layout.head_dim,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "slot mapping and write launch");
+}
+
 int32_t pkv_copy_blocks(void* dst_pool, int32_t dst_num_blocks, const void* src_pool,
                         int32_t src_num_blocks, const int32_t* block_pairs, int32_t num_pairs,
                         pkv_cache_layout layout, void* stream) {

@@ -132,6 +132,12 @@ cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int 
                                 int num_tokens, int num_blocks, int block_size,
                                 cudaStream_t stream);
 
+cudaError_t launch_mapped_write(void* pool, const void* key, const void* value,
+                                long long key_stride, long long value_stride, int64_t* slots,
+                                const int32_t* block_table, int max_blocks, const int32_t* qsl,
+                                const int32_t* num_computed, int num_reqs, int num_tokens,
+                                int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                                cudaStream_t stream);
 cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long long key_stride,
                             long long value_stride, const int64_t* slots, int num_tokens,
                             int num_blocks, int block_size, int num_kv_heads, int head_dim,

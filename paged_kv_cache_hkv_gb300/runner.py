@@ -46,11 +46,12 @@ class DeviceStep:
     """One step's inputs on the GPU plus its output buffers."""
 
     def __init__(self, step, device="cuda", decode_splits=None, upload_pool=True,
-                 shared_prefix=None):
+                 shared_prefix=None, fused_write=False):
         """shared_prefix: None, or (shared_prefix_len, shared_first_req,
         shared_num_reqs) for the attention call (see pagedkv.h); "auto" takes
         it from the step's shared prefix when its sharing requests form one
-        contiguous run of decodes."""
+        contiguous run of decodes. fused_write: run() maps the slots and
+        writes the rows in one launch (pkv_slot_mapping_and_write)."""
         self.step = step
         self.device = torch.device(device)
         dev = self.device
@@ -67,6 +68,7 @@ class DeviceStep:
         self.out = torch.zeros((T, step.num_q_heads, step.head_dim), dtype=torch.bfloat16,
                                device=dev)
         self.decode_splits = decode_splits
+        self.fused_write = fused_write
         if shared_prefix == "auto":
             shared_prefix = shared_prefix_of(step)
         self.shared_prefix = shared_prefix
@@ -89,6 +91,11 @@ class DeviceStep:
         binding.pkv_paged_kv_write(self.kv_cache, self.k, self.v, self.slot_mapping,
                                    stream=stream)
 
+    def slot_map_and_write(self, stream=None):
+        binding.pkv_slot_mapping_and_write(self.kv_cache, self.k, self.v, self.block_table,
+                                           self.query_start_loc, self.num_computed,
+                                           slot_mapping=self.slot_mapping, stream=stream)
+
     def attend(self, stream=None):
         s = self.step
         binding.pkv_paged_attention(
@@ -98,9 +105,10 @@ class DeviceStep:
             decode_splits=self.decode_splits, shared_prefix=self.shared_prefix, stream=stream)
 
     def run(self, stream=None):
-        """The whole step: slot mapping, cache write, attention. The three
-        calls' arguments are marshalled once and reused while the buffers
-        stay the same objects (a test may swap a buffer between runs)."""
+        """The whole step: slot mapping, cache write (one launch with
+        fused_write), attention. The calls' arguments are marshalled once and
+        reused while the buffers stay the same objects (a test may swap a
+        buffer between runs)."""
         self.calls().run(stream)
 
     def calls(self) -> "binding.StepCalls":
@@ -116,7 +124,8 @@ class DeviceStep:
                 kv_cache=self.kv_cache, key=self.k, value=self.v, out=self.out, q=self.q,
                 seq_lens=self.seq_lens, max_query_len=s.max_query_len,
                 max_seq_len=s.max_seq_len, scale=s.scale, workspace=self.workspace,
-                decode_splits=self.decode_splits, shared_prefix=self.shared_prefix)
+                decode_splits=self.decode_splits, shared_prefix=self.shared_prefix,
+                fused_write=self.fused_write)
             self._calls_bufs = bufs
         return self._calls
 
