@@ -710,8 +710,12 @@ def run_native(args):
     prefill = None
     if work["prefill_flops"] and pf_ms > 0:
         tf = work["prefill_flops"] / (pf_ms * 1e-3) / 1e12
+        # the burst peak: the launches here run for at most milliseconds (the
+        # seconds-long sustained figure is given beside it for context)
+        tc_sus = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
         prefill = {"kernel": "prefill_kernel", "bound": "tensor", "achieved": tf,
                    "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
+                   "peak_sustained": tc_sus, "frac_of_sustained": tf / tc_sus if tc_sus else None,
                    "algorithmic_flops_per_launch": work["prefill_flops"]}
 
     cpu = None
