@@ -260,7 +260,8 @@ struct PrefillParams {
   float* shared_o;
 };
 
-// mbarriers. "commit" ones are arrived on by tcgen05.commit of the MMA thread.
+// mbarriers. "commit" ones are arrived on by a tcgen05.commit of an MMA thread
+// (S: s_full, q_free, drain[0]; PV: pv_done, o_full, drain[1]).
 struct PrefillShared {
   uint64_t q_full;               // Q tile of the item landed (TMA)
   uint64_t q_free;               // commit: the item's last S read Q
@@ -274,7 +275,7 @@ struct PrefillShared {
                                  // rescaled, V cleaned (and, for an item's first tile,
                                  // the previous item's O read)
   uint64_t o_full;               // commit: the item's last PV done
-  uint64_t drain[2];
+  uint64_t drain[2];             // commit: every MMA of the S / PV thread done (teardown)
   uint64_t iq_full[kItemQ];      // item id j published in item_q[j % kItemQ]
   uint64_t iq_free[kItemQ];      // 11 arrivals: every role has read it
   int item_q[kItemQ];
