@@ -58,9 +58,10 @@ def parse_args():
     p.add_argument("--shared-prefix", choices=["auto", "off"], default="auto",
                    help="pass the shared-prefix hint when the workload's sharing requests "
                         "form one run of decodes (auto), or never (off)")
-    p.add_argument("--write", choices=["separate", "fused"], default="fused",
-                   help="slot mapping and cache write as two launches, or fused into one "
-                        "(pkv_slot_mapping_and_write)")
+    p.add_argument("--write", choices=["separate", "fused", "attention"], default="attention",
+                   help="slot mapping and cache write as two launches (separate), fused into "
+                        "one (pkv_slot_mapping_and_write), or inside the attention call's "
+                        "first launch (pkv_paged_attention_with_write)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -164,12 +165,12 @@ def block_tradeoff(step):
             "slots_wasted_frac": (allocated - stored) / allocated if allocated else 0.0}
 
 
-def kernels_per_step(step, fused_write=False, shared_prefix=None):
-    """Launches of one step: slot mapping and write (one launch when fused),
-    the plan, the prefill (prefill rows or shared-prefix items), decode and
-    combine."""
-    return ((1 if fused_write else 2) + 1 + (1 if step.max_query_len > 1 or shared_prefix else 0)
-            + 2)
+def kernels_per_step(step, fused_write=False, shared_prefix=None, write_in_attention=False):
+    """Launches of one step: slot mapping and write (one launch when fused,
+    none of their own inside the attention call), the plan, the prefill
+    (prefill rows or shared-prefix items), decode and combine."""
+    write = 0 if write_in_attention else (1 if fused_write else 2)
+    return write + 1 + (1 if step.max_query_len > 1 or shared_prefix else 0) + 2
 
 
 # ------------------------------------------------------------------ clocks
@@ -473,7 +474,7 @@ def run_e2e(ds, step, work, K, world, pg, sync_all):
     from paged_kv_cache_hkv_gb300.runner import DeviceStep
 
     ds2 = DeviceStep(step, upload_pool=False, shared_prefix=ds.shared_prefix,
-                     fused_write=ds.fused_write)
+                     fused_write=ds.fused_write, write_in_attention=ds.write_in_attention)
     ds2.kv_cache = ds.kv_cache
     sets = [ds, ds2]
     names = ("q", "k", "v", "block_table", "seq_lens", "query_start_loc", "num_computed")
@@ -630,7 +631,8 @@ def run_native(args):
     seed = replica_seed(base_seed, rank)
     step = synth.WORKLOADS[args.workload](seed=seed, block_size=args.block_size)
     ds = DeviceStep(step, shared_prefix="auto" if args.shared_prefix == "auto" else None,
-                    fused_write=args.write == "fused")
+                    fused_write=args.write == "fused",
+                    write_in_attention=args.write == "attention")
     binding.pkv_get_device_errors(clear=True)
     work = step_work(step)
     stream = torch.cuda.current_stream()
@@ -747,8 +749,10 @@ def run_native(args):
                                           if ds.shared_prefix else None),
                    "parallelism": f"replicas x{world}",
                    "launch": "cuda graph replay" if args.graph else "direct, programmatic dependent launch",
-                   "write": ("slot mapping fused into the write (one launch)" if args.write == "fused"
-                             else "slot mapping, then the write")},
+                   "write": {"fused": "slot mapping fused into the write (one launch)",
+                             "attention": "slot mapping and write inside the attention call's "
+                                          "first launch",
+                             "separate": "slot mapping, then the write"}[args.write]},
         "block_tradeoff": block_tradeoff(step),
         "decode_kv_read_gbs": dec_gbs,
         # the same bytes over decode + combine time (both kernels of split-KV)
@@ -775,7 +779,8 @@ def run_native(args):
         "prefill_roofline": prefill,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * kernels_per_step(step, ds.fused_write, ds.shared_prefix),
+        "gpu_launches": K * kernels_per_step(step, ds.fused_write, ds.shared_prefix,
+                                             ds.write_in_attention),
         "clocks": clocks,
     }
     if rank == 0:

@@ -311,6 +311,33 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride,
                             const pkv_attention_options* options, void* stream);
 
 /*
+ * pkv_paged_attention_with_write -- the whole step of one layer in one call:
+ * the slot mapping and cache write of every new token
+ * (pkv_slot_mapping_and_write) and then pkv_paged_attention over the pool
+ * that now holds them, as the pages' engine does per layer ("vLLM 架构源码解析
+ * （一）" §3.3.3: write the step's K/V, then attend; "Inside vLLM" §3.4-3.5:
+ * one attention call over the mixed batch). The write runs in the same
+ * launch as the attention's plan (its own CTAs next to the plan's), so the
+ * step takes one launch fewer than the two calls.
+ *
+ * Arguments: those of pkv_paged_attention, plus key, value,
+ * key_row_stride, value_row_stride and slot_mapping (out, may be NULL) as in
+ * pkv_slot_mapping_and_write; kv_cache is written. Results, error bits and
+ * the workspace are those of the two calls. A call with no attention to do
+ * (num_reqs, num_tokens or max_query_len 0) still maps and writes (padding
+ * rows get slot -1). With trace_events, bracket [0, 1) covers the write and
+ * the plan.
+ */
+int32_t pkv_paged_attention_with_write(
+    void* out, const void* q, int64_t q_row_stride, void* kv_cache, const void* key,
+    const void* value, int64_t key_row_stride, int64_t value_row_stride, int64_t* slot_mapping,
+    const int32_t* block_table, int32_t max_blocks_per_req, const int32_t* seq_lens,
+    const int32_t* query_start_loc, const int32_t* num_computed_tokens, int32_t num_reqs,
+    int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+    float scale, pkv_cache_layout layout, void* workspace, size_t workspace_bytes,
+    const pkv_attention_options* options, void* stream);
+
+/*
  * pkv_paged_attention_static_workspace -- pkv_paged_attention for callers
  * that cannot allocate device memory. The pages have no counterpart to this
  * entry point; it exists for how the library is called, not for what it

@@ -63,6 +63,11 @@ _SIGNATURES = {
     "pkv_slot_mapping_and_write": (c_i32, [c_void_p, c_void_p, c_void_p, c_i64, c_i64, c_void_p,
                                            c_void_p, c_i32, c_void_p, c_void_p, c_i32, c_i32,
                                            pkv_cache_layout, c_void_p]),
+    "pkv_paged_attention_with_write": (
+        c_i32, [c_void_p, c_void_p, c_i64, c_void_p, c_void_p, c_void_p, c_i64, c_i64, c_void_p,
+                c_void_p, c_i32, c_void_p, c_void_p, c_void_p, c_i32, c_i32, c_i32, c_i32, c_i32,
+                c_float, pkv_cache_layout, c_void_p, c_size_t,
+                ctypes.POINTER(pkv_attention_options), c_void_p]),
     "pkv_paged_attention_static_workspace": (
         c_i32, [c_void_p, c_void_p, c_i64, c_void_p, c_void_p, c_i32, c_void_p, c_void_p,
                 c_void_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_float, pkv_cache_layout,
@@ -273,6 +278,41 @@ def pkv_paged_attention(out, q, kv_cache, block_table, seq_lens, query_start_loc
     return out
 
 
+def pkv_paged_attention_with_write(out, q, kv_cache, key, value, block_table, seq_lens,
+                                   query_start_loc, num_computed_tokens, *, max_query_len: int,
+                                   max_seq_len: int, scale: float, workspace, slot_mapping=None,
+                                   decode_splits=None, trace_events=None, shared_prefix=None,
+                                   stream=None):
+    """The step of one layer in one call: slot mapping and cache write of the
+    new tokens, then attention (see pagedkv.h). slot_mapping (int64 [T])
+    receives the slots when given."""
+    for t, n in ((out, "out"), (q, "q"), (kv_cache, "kv_cache"), (key, "key"),
+                 (value, "value")):
+        _require(t, torch.bfloat16, n)
+    for t, n in ((block_table, "block_table"), (seq_lens, "seq_lens"),
+                 (query_start_loc, "query_start_loc"),
+                 (num_computed_tokens, "num_computed_tokens")):
+        _require(t, torch.int32, n)
+    if slot_mapping is not None:
+        _require(slot_mapping, torch.int64, "slot_mapping")
+    if not out.is_contiguous() or not block_table.is_contiguous():
+        raise ValueError("out and block_table must be contiguous")
+    for t, n in ((q, "q"), (key, "key"), (value, "value")):
+        if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} must be [T, H, D] with contiguous rows")
+    if key.shape[0] != q.shape[0]:
+        raise ValueError("key and q must have the same number of rows")
+    lay = layout_of(kv_cache)
+    _check("pkv_paged_attention_with_write", load().pkv_paged_attention_with_write(
+        _ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), _ptr(key), _ptr(value), key.stride(0),
+        value.stride(0), _ptr(slot_mapping), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), _ptr(query_start_loc), _ptr(num_computed_tokens), seq_lens.shape[0],
+        q.shape[0], int(max_query_len), int(max_seq_len), q.shape[1], float(scale), lay,
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _options(decode_splits, trace_events, shared_prefix), _stream(stream)))
+    return out
+
+
 def pkv_get_device_errors(clear: bool = True, stream=None) -> int:
     """Synchronise and read (optionally clear) the sticky device error bits."""
     v = c_u32(0)
@@ -309,8 +349,10 @@ def pkv_paged_attention_static_workspace(out, q, kv_cache, block_table, seq_lens
 
 class StepCalls:
     """The calls of one step -- pkv_slot_mapping, pkv_paged_kv_write,
-    pkv_paged_attention, or with fused_write pkv_slot_mapping_and_write then
-    pkv_paged_attention -- with their arguments checked and marshalled once.
+    pkv_paged_attention; with fused_write pkv_slot_mapping_and_write then
+    pkv_paged_attention; with write_in_attention the one call
+    pkv_paged_attention_with_write -- with their arguments checked and
+    marshalled once.
 
     A serving loop that keeps its step buffers (as DeviceStep does) pays the
     argument checks and the tensor-to-pointer conversion once, not on every
@@ -321,7 +363,7 @@ class StepCalls:
     def __init__(self, *, slot_mapping, block_table, query_start_loc, num_computed_tokens,
                  kv_cache, key, value, out, q, seq_lens, max_query_len: int,
                  max_seq_len: int, scale: float, workspace, decode_splits=None,
-                 shared_prefix=None, fused_write=False):
+                 shared_prefix=None, fused_write=False, write_in_attention=False):
         _require(slot_mapping, torch.int64, "slot_mapping")
         for t, n in ((block_table, "block_table"), (query_start_loc, "query_start_loc"),
                      (num_computed_tokens, "num_computed_tokens"), (seq_lens, "seq_lens")):
@@ -345,12 +387,22 @@ class StepCalls:
             _ptr(kv_cache), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
             _ptr(slot_mapping), key.shape[0], lay)
         self.fused_write = bool(fused_write)
+        self.write_in_attention = bool(write_in_attention)
+        if self.write_in_attention and key.shape[0] != q.shape[0]:
+            raise ValueError("key and q must have the same number of rows")
         self.mapped_write_args = (
             _ptr(kv_cache), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
             _ptr(slot_mapping), _ptr(block_table), block_table.shape[1], _ptr(query_start_loc),
             _ptr(num_computed_tokens), num_computed_tokens.shape[0], key.shape[0], lay)
         self.attn_args = (
             _ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), _ptr(block_table),
+            block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc),
+            _ptr(num_computed_tokens), seq_lens.shape[0], q.shape[0], int(max_query_len),
+            int(max_seq_len), q.shape[1], float(scale), lay, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), self._opts)
+        self.attn_write_args = (
+            _ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), _ptr(key), _ptr(value),
+            key.stride(0), value.stride(0), _ptr(slot_mapping), _ptr(block_table),
             block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc),
             _ptr(num_computed_tokens), seq_lens.shape[0], q.shape[0], int(max_query_len),
             int(max_seq_len), q.shape[1], float(scale), lay, _ptr(workspace),
@@ -382,6 +434,11 @@ class StepCalls:
     def run(self, stream=None):
         st = _stream(stream)
         lib = self.lib
+        if self.write_in_attention:
+            status = lib.pkv_paged_attention_with_write(*self.attn_write_args, st)
+            if status:
+                raise PagedKVError("pkv_paged_attention_with_write", status)
+            return
         if self.fused_write:
             status = lib.pkv_slot_mapping_and_write(*self.mapped_write_args, st)
             if status:

@@ -10,6 +10,7 @@
 
 #include "../../include/pagedkv.h"
 #include "launch.h"
+#include "write_rows.cuh"
 
 namespace {
 
@@ -313,11 +314,11 @@ int32_t pkv_slot_mapping_and_write(void* kv_cache, const void* key, const void* 
   DeviceInfo* d;
   st = device_info(&d);
   if (st != PKV_OK) return st;
-  cudaError_t e = pkv::launch_mapped_write(
+  const pkv::WriteRowsArgs w = pkv::write_rows_args(
       kv_cache, key, value, key_row_stride, value_row_stride, slot_mapping, block_table,
       max_blocks_per_req, query_start_loc, num_computed_tokens, num_reqs, num_tokens,
-      layout.num_blocks, layout.block_size, layout.num_kv_heads, layout.head_dim,
-      static_cast<cudaStream_t>(stream));
+      layout.num_blocks, layout.block_size, layout.num_kv_heads, layout.head_dim);
+  cudaError_t e = pkv::launch_mapped_write(w, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "slot mapping and write launch");
 }
 
@@ -369,14 +370,16 @@ int64_t pkv_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
       ws_layout(num_reqs, virt, gw, layout.head_dim, splits, sh, num_q_heads).total);
 }
 
-int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, const void* kv_cache,
-                            const int32_t* block_table, int32_t max_blocks_per_req,
-                            const int32_t* seq_lens, const int32_t* query_start_loc,
-                            const int32_t* num_computed_tokens, int32_t num_reqs,
-                            int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
-                            int32_t num_q_heads, float scale, pkv_cache_layout layout,
-                            void* workspace, size_t workspace_bytes,
-                            const pkv_attention_options* options, void* stream) {
+// pkv_paged_attention, and with `write` the step's slot mapping and cache
+// write in the plan's launch (pkv_paged_attention_with_write).
+static int32_t attention_impl(void* out, const void* q, int64_t q_row_stride, const void* kv_cache,
+                       const int32_t* block_table, int32_t max_blocks_per_req,
+                       const int32_t* seq_lens, const int32_t* query_start_loc,
+                       const int32_t* num_computed_tokens, int32_t num_reqs, int32_t num_tokens,
+                       int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+                       float scale, pkv_cache_layout layout, void* workspace,
+                       size_t workspace_bytes, const pkv_attention_options* options, void* stream,
+                       const pkv::WriteRowsArgs* write) {
   int32_t st = check_layout(layout);
   if (st != PKV_OK) return st;
   st = check_group(num_q_heads, layout.num_kv_heads);
@@ -388,7 +391,12 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   const int64_t row = static_cast<int64_t>(num_q_heads) * layout.head_dim;
   if (q_row_stride == 0) q_row_stride = row;
   if (q_row_stride < row) return PKV_ERR_BAD_SHAPE;
-  if (num_reqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
+  if (num_reqs == 0 || num_tokens == 0 || max_query_len == 0) {
+    // no attention to do; the write (padding rows: slots -1) still runs
+    if (!write) return PKV_OK;
+    cudaError_t e = pkv::launch_mapped_write(*write, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "slot mapping and write launch");
+  }
   if (static_cast<long long>(max_seq_len) >
       static_cast<long long>(max_blocks_per_req) * layout.block_size)
     return PKV_ERR_BAD_SHAPE;
@@ -490,7 +498,7 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
     return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
   };
   cudaError_t e = mark(0);
-  if (e == cudaSuccess) e = pkv::launch_plan(a, ws, s);
+  if (e == cudaSuccess) e = pkv::launch_plan(a, ws, s, write);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   if (max_query_len > 1 || sh.num > 0) {
@@ -523,6 +531,52 @@ int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, cons
   return PKV_OK;
 }
 
+int32_t pkv_paged_attention(void* out, const void* q, int64_t q_row_stride, const void* kv_cache,
+                            const int32_t* block_table, int32_t max_blocks_per_req,
+                            const int32_t* seq_lens, const int32_t* query_start_loc,
+                            const int32_t* num_computed_tokens, int32_t num_reqs,
+                            int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                            int32_t num_q_heads, float scale, pkv_cache_layout layout,
+                            void* workspace, size_t workspace_bytes,
+                            const pkv_attention_options* options, void* stream) {
+  return attention_impl(out, q, q_row_stride, kv_cache, block_table, max_blocks_per_req,
+                        seq_lens, query_start_loc, num_computed_tokens, num_reqs, num_tokens,
+                        max_query_len, max_seq_len, num_q_heads, scale, layout, workspace,
+                        workspace_bytes, options, stream, nullptr);
+}
+
+int32_t pkv_paged_attention_with_write(
+    void* out, const void* q, int64_t q_row_stride, void* kv_cache, const void* key,
+    const void* value, int64_t key_row_stride, int64_t value_row_stride, int64_t* slot_mapping,
+    const int32_t* block_table, int32_t max_blocks_per_req, const int32_t* seq_lens,
+    const int32_t* query_start_loc, const int32_t* num_computed_tokens, int32_t num_reqs,
+    int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+    float scale, pkv_cache_layout layout, void* workspace, size_t workspace_bytes,
+    const pkv_attention_options* options, void* stream) {
+  int32_t st = check_layout(layout);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0 || num_reqs < 0 || max_blocks_per_req < 0) return PKV_ERR_BAD_SHAPE;
+  const int64_t row = static_cast<int64_t>(layout.num_kv_heads) * layout.head_dim;
+  if (key_row_stride == 0) key_row_stride = row;
+  if (value_row_stride == 0) value_row_stride = row;
+  if (key_row_stride < row || value_row_stride < row) return PKV_ERR_BAD_SHAPE;
+  if (num_tokens > 0) {
+    if (!kv_cache || !key || !value || !query_start_loc) return PKV_ERR_NULL_POINTER;
+    if (num_reqs > 0 && (!block_table || !num_computed_tokens)) return PKV_ERR_NULL_POINTER;
+    if (!aligned16(kv_cache) || !aligned16(key) || !aligned16(value) || (key_row_stride % 8) ||
+        (value_row_stride % 8))
+      return PKV_ERR_MISALIGNED;
+  }
+  const pkv::WriteRowsArgs w = pkv::write_rows_args(
+      kv_cache, key, value, key_row_stride, value_row_stride, slot_mapping, block_table,
+      max_blocks_per_req, query_start_loc, num_computed_tokens, num_reqs, num_tokens,
+      layout.num_blocks, layout.block_size, layout.num_kv_heads, layout.head_dim);
+  return attention_impl(out, q, q_row_stride, kv_cache, block_table, max_blocks_per_req,
+                        seq_lens, query_start_loc, num_computed_tokens, num_reqs, num_tokens,
+                        max_query_len, max_seq_len, num_q_heads, scale, layout, workspace,
+                        workspace_bytes, options, stream, num_tokens > 0 ? &w : nullptr);
+}
+
 int32_t pkv_get_device_errors(uint32_t* flags, int32_t clear, void* stream) {
   if (!flags) return PKV_ERR_NULL_POINTER;
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
@@ -531,6 +585,7 @@ int32_t pkv_get_device_errors(uint32_t* flags, int32_t clear, void* stream) {
   e = pkv::read_errors_kvwrite(&v, clear != 0);
   if (e == cudaSuccess) e = pkv::read_errors_decode(&v, clear != 0);
   if (e == cudaSuccess) e = pkv::read_errors_prefill(&v, clear != 0);
+  if (e == cudaSuccess) e = pkv::read_errors_plan(&v, clear != 0);
   if (e != cudaSuccess) return cuda_fail(e, "reading device error word");
   *flags = v;
   return PKV_OK;

@@ -13,6 +13,7 @@
 // sides.
 #include "common.cuh"
 #include "launch.h"
+#include "write_rows.cuh"
 
 namespace pkv {
 
@@ -121,82 +122,15 @@ __global__ void __launch_bounds__(kWriteThreads)
   }
 }
 
-// The slot mapping fused into the write: one warp per new token. The warp
-// issues the loads of its token's K and V rows first (the first 8 16-byte
-// words per lane of each), finds the token's request with a 32-way search of
-// query_start_loc (non-decreasing), computes the slot as slot_mapping_kernel
-// does and stores the rows. A token that the search puts in no request
-// (before query_start_loc[0] or at / past query_start_loc[num_reqs]) or in a
-// request with inconsistent lengths gets slot -1 and is not written.
-constexpr int kMappedWarps = 8;     // warps (tokens) per CTA
-constexpr int kMappedPrefetch = 8;  // 16-byte words per lane loaded before the slot is known
+// The slot mapping fused into the write: one warp per new token (the body
+// is write_token_rows).
+constexpr int kMappedWarps = 8;  // warps (tokens) per CTA
 
-__global__ void __launch_bounds__(kMappedWarps * 32)
-    mapped_write_kernel(uint4* __restrict__ pool, const uint4* __restrict__ key,
-                        const uint4* __restrict__ value, long long key_stride_v,
-                        long long value_stride_v, int64_t* __restrict__ slots_out,
-                        const int32_t* __restrict__ block_table, int max_blocks,
-                        const int32_t* __restrict__ qsl, const int32_t* __restrict__ num_computed,
-                        int num_reqs, int num_tokens, int num_blocks, int shift, int vec_per_row) {
+__global__ void __launch_bounds__(kMappedWarps * 32) mapped_write_kernel(const WriteRowsArgs w) {
   pdl_trigger();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
   const long long t = static_cast<long long>(blockIdx.x) * kMappedWarps + (threadIdx.x >> 5);
-  if (t >= num_tokens) return;
-  const uint4* ksrc = key + t * key_stride_v;
-  const uint4* vsrc = value + t * value_stride_v;
-  uint4 kw[kMappedPrefetch], vw[kMappedPrefetch];
-#pragma unroll
-  for (int i = 0; i < kMappedPrefetch; ++i) {
-    const int e = lane + 32 * i;
-    if (e < vec_per_row) {
-      kw[i] = __ldg(ksrc + e);
-      vw[i] = __ldg(vsrc + e);
-    }
-  }
-  const int tt = static_cast<int>(t);
-  long long slot = -1;
-  const int qend = __ldg(qsl + num_reqs), qfirst = __ldg(qsl);
-  if (tt < qend && tt >= qfirst) {
-    const int r = warp_upper_index(qsl, num_reqs, tt);
-    const int q0 = __ldg(qsl + r), q1 = __ldg(qsl + r + 1);
-    const int c = __ldg(num_computed + r);
-    if (q0 < 0 || q1 < q0 || q1 > num_tokens || c < 0 || (r == 0 && q0 != 0)) {
-      if (lane == 0) atomicOr(&g_errors_kvwrite, kErrLengths);
-    } else {
-      const long long pos = static_cast<long long>(c) + (tt - q0);
-      const long long lb = pos >> shift;
-      if (lb >= max_blocks) {
-        if (lane == 0) atomicOr(&g_errors_kvwrite, kErrLengths);
-      } else {
-        const int phys = __ldg(block_table + static_cast<long long>(r) * max_blocks + lb);
-        if (phys < 0 || phys >= num_blocks) {
-          if (lane == 0) atomicOr(&g_errors_kvwrite, kErrBlockRange);
-        } else {
-          slot = (static_cast<long long>(phys) << shift) + (pos & ((1 << shift) - 1));
-        }
-      }
-    }
-  } else if (tt < qend || qfirst != 0) {  // rows before a non-zero query_start_loc[0]
-    if (lane == 0) atomicOr(&g_errors_kvwrite, kErrLengths);
-  }
-  if (slots_out && lane == 0) slots_out[t] = slot;
-  if (slot < 0) return;
-  const long long blk = slot >> shift, off = slot & ((1 << shift) - 1);
-  uint4* kdst = pool + (((blk * 2) << shift) + off) * vec_per_row;
-  uint4* vdst = pool + (((blk * 2 + 1) << shift) + off) * vec_per_row;
-#pragma unroll
-  for (int i = 0; i < kMappedPrefetch; ++i) {
-    const int e = lane + 32 * i;
-    if (e < vec_per_row) {
-      kdst[e] = kw[i];
-      vdst[e] = vw[i];
-    }
-  }
-  for (int e = lane + 32 * kMappedPrefetch; e < vec_per_row; e += 32) {  // rows over 4 KB
-    kdst[e] = __ldg(ksrc + e);
-    vdst[e] = __ldg(vsrc + e);
-  }
+  if (t < w.num_tokens) write_token_rows(w, t, &g_errors_kvwrite);
 }
 
 // Whole-block copies between two pools of one layout (copy-on-write of a
@@ -272,20 +206,34 @@ cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long
                     num_slots);
 }
 
-cudaError_t launch_mapped_write(void* pool, const void* key, const void* value,
-                                long long key_stride, long long value_stride, int64_t* slots,
-                                const int32_t* block_table, int max_blocks, const int32_t* qsl,
-                                const int32_t* num_computed, int num_reqs, int num_tokens,
-                                int num_blocks, int block_size, int num_kv_heads, int head_dim,
-                                cudaStream_t stream) {
-  if (num_tokens == 0) return cudaSuccess;
-  const int grid = (num_tokens + kMappedWarps - 1) / kMappedWarps;
-  return launch_pdl(mapped_write_kernel, dim3(grid), dim3(kMappedWarps * 32), 0, stream,
-                    static_cast<uint4*>(pool), static_cast<const uint4*>(key),
-                    static_cast<const uint4*>(value), key_stride / 8, value_stride / 8, slots,
-                    block_table, max_blocks, qsl, num_computed, num_reqs, num_tokens, num_blocks,
-                    static_cast<int>(__builtin_ctz(static_cast<unsigned>(block_size))),
-                    num_kv_heads * head_dim / 8);
+WriteRowsArgs write_rows_args(void* pool, const void* key, const void* value,
+                              long long key_stride, long long value_stride, int64_t* slots,
+                              const int32_t* block_table, int max_blocks, const int32_t* qsl,
+                              const int32_t* num_computed, int num_reqs, int num_tokens,
+                              int num_blocks, int block_size, int num_kv_heads, int head_dim) {
+  WriteRowsArgs w;
+  w.pool = static_cast<uint4*>(pool);
+  w.key = static_cast<const uint4*>(key);
+  w.value = static_cast<const uint4*>(value);
+  w.key_stride_v = key_stride / 8;
+  w.value_stride_v = value_stride / 8;
+  w.slots_out = slots;
+  w.block_table = block_table;
+  w.max_blocks = max_blocks;
+  w.qsl = qsl;
+  w.num_computed = num_computed;
+  w.num_reqs = num_reqs;
+  w.num_tokens = num_tokens;
+  w.num_blocks = num_blocks;
+  w.shift = static_cast<int>(__builtin_ctz(static_cast<unsigned>(block_size)));
+  w.vec_per_row = num_kv_heads * head_dim / 8;
+  return w;
+}
+
+cudaError_t launch_mapped_write(const WriteRowsArgs& w, cudaStream_t stream) {
+  if (w.num_tokens == 0) return cudaSuccess;
+  const int grid = (w.num_tokens + kMappedWarps - 1) / kMappedWarps;
+  return launch_pdl(mapped_write_kernel, dim3(grid), dim3(kMappedWarps * 32), 0, stream, w);
 }
 
 cudaError_t read_errors_kvwrite(uint32_t* out, bool clear) {

@@ -132,12 +132,13 @@ cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_table, int 
                                 int num_tokens, int num_blocks, int block_size,
                                 cudaStream_t stream);
 
-cudaError_t launch_mapped_write(void* pool, const void* key, const void* value,
-                                long long key_stride, long long value_stride, int64_t* slots,
-                                const int32_t* block_table, int max_blocks, const int32_t* qsl,
-                                const int32_t* num_computed, int num_reqs, int num_tokens,
-                                int num_blocks, int block_size, int num_kv_heads, int head_dim,
-                                cudaStream_t stream);
+struct WriteRowsArgs;
+WriteRowsArgs write_rows_args(void* pool, const void* key, const void* value,
+                              long long key_stride, long long value_stride, int64_t* slots,
+                              const int32_t* block_table, int max_blocks, const int32_t* qsl,
+                              const int32_t* num_computed, int num_reqs, int num_tokens,
+                              int num_blocks, int block_size, int num_kv_heads, int head_dim);
+cudaError_t launch_mapped_write(const WriteRowsArgs& w, cudaStream_t stream);
 cudaError_t launch_kv_write(void* pool, const void* key, const void* value, long long key_stride,
                             long long value_stride, const int64_t* slots, int num_tokens,
                             int num_blocks, int block_size, int num_kv_heads, int head_dim,
@@ -147,7 +148,11 @@ cudaError_t launch_copy_blocks(void* dst, int dst_num_blocks, const void* src, i
                                const int32_t* pairs, int num_pairs, int block_size,
                                int num_kv_heads, int head_dim, int num_sms, cudaStream_t stream);
 
-cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream);
+// The plan kernel; with `write`, one launch that also maps the slots of the
+// step's new tokens and writes their K and V rows (the write's CTAs next to
+// the plan's).
+cudaError_t launch_plan(const AttnArgs& a, const AttnWorkspace& ws, cudaStream_t stream,
+                        const WriteRowsArgs* write = nullptr);
 
 // Decode splits (CTAs along the decode stream) in one full wave of the device.
 cudaError_t decode_full_wave_splits(int head_dim, int num_kv_heads, int group, int block_shift,
@@ -164,5 +169,6 @@ cudaError_t launch_prefill(const AttnArgs& a, const AttnWorkspace& ws, const CUt
 cudaError_t read_errors_kvwrite(uint32_t* out, bool clear);
 cudaError_t read_errors_decode(uint32_t* out, bool clear);
 cudaError_t read_errors_prefill(uint32_t* out, bool clear);
+cudaError_t read_errors_plan(uint32_t* out, bool clear);
 
 }  // namespace pkv

@@ -46,12 +46,14 @@ class DeviceStep:
     """One step's inputs on the GPU plus its output buffers."""
 
     def __init__(self, step, device="cuda", decode_splits=None, upload_pool=True,
-                 shared_prefix=None, fused_write=False):
+                 shared_prefix=None, fused_write=False, write_in_attention=False):
         """shared_prefix: None, or (shared_prefix_len, shared_first_req,
         shared_num_reqs) for the attention call (see pagedkv.h); "auto" takes
         it from the step's shared prefix when its sharing requests form one
         contiguous run of decodes. fused_write: run() maps the slots and
-        writes the rows in one launch (pkv_slot_mapping_and_write)."""
+        writes the rows in one launch (pkv_slot_mapping_and_write);
+        write_in_attention: run() is the single call
+        pkv_paged_attention_with_write."""
         self.step = step
         self.device = torch.device(device)
         dev = self.device
@@ -69,6 +71,7 @@ class DeviceStep:
                                device=dev)
         self.decode_splits = decode_splits
         self.fused_write = fused_write
+        self.write_in_attention = write_in_attention
         if shared_prefix == "auto":
             shared_prefix = shared_prefix_of(step)
         self.shared_prefix = shared_prefix
@@ -95,6 +98,15 @@ class DeviceStep:
         binding.pkv_slot_mapping_and_write(self.kv_cache, self.k, self.v, self.block_table,
                                            self.query_start_loc, self.num_computed,
                                            slot_mapping=self.slot_mapping, stream=stream)
+
+    def attend_with_write(self, stream=None):
+        s = self.step
+        binding.pkv_paged_attention_with_write(
+            self.out, self.q, self.kv_cache, self.k, self.v, self.block_table, self.seq_lens,
+            self.query_start_loc, self.num_computed, max_query_len=s.max_query_len,
+            max_seq_len=s.max_seq_len, scale=s.scale, workspace=self.workspace,
+            slot_mapping=self.slot_mapping, decode_splits=self.decode_splits,
+            shared_prefix=self.shared_prefix, stream=stream)
 
     def attend(self, stream=None):
         s = self.step
@@ -125,7 +137,7 @@ class DeviceStep:
                 seq_lens=self.seq_lens, max_query_len=s.max_query_len,
                 max_seq_len=s.max_seq_len, scale=s.scale, workspace=self.workspace,
                 decode_splits=self.decode_splits, shared_prefix=self.shared_prefix,
-                fused_write=self.fused_write)
+                fused_write=self.fused_write, write_in_attention=self.write_in_attention)
             self._calls_bufs = bufs
         return self._calls
 

@@ -1,4 +1,5 @@
-"""pkv_slot_mapping_and_write (the slot mapping fused into the cache write)
+"""pkv_slot_mapping_and_write (the slot mapping fused into the cache write) and
+pkv_paged_attention_with_write (the whole step of a layer in one call)
 against the oracle on the GPU: slots and the whole pool bit-exact, the same
 handling of padding rows and inconsistent lengths as the two separate calls.
 """
@@ -153,3 +154,82 @@ def test_fused_write_agrees_with_the_two_calls_on_random_batches():
         assert binding.pkv_get_device_errors(clear=True) == 0
         assert np.array_equal(a.slots_host(), b.slots_host())
         assert np.array_equal(a.pool_host(), b.pool_host())
+
+
+# ------------------------------------------------- the one-call step (write + attention)
+def one_call_step_matches_oracle(step, shared_prefix=None, expect_flags=0, rows=None):
+    ds = DeviceStep(step, write_in_attention=True, shared_prefix=shared_prefix)
+    ds.slot_mapping.fill_(12345)
+    ds.run()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_errors(clear=True) == expect_flags
+    slots, pool, ref = oracle_step(step, rows=rows)
+    assert np.array_equal(ds.slots_host(), slots)
+    assert np.array_equal(ds.pool_host(), pool)
+    assert_close(ds.out_host(), ref, rows=rows)
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_one_call_mixed_step(B):
+    one_call_step_matches_oracle(synth.mixed_step(block_size=B))
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "llama_decode", "prefill_rows"])
+def test_one_call_workloads(name):
+    one_call_step_matches_oracle(synth.WORKLOADS[name]())
+
+
+def test_one_call_with_the_shared_prefix_hint():
+    from paged_kv_cache_hkv_gb300.runner import shared_prefix_of
+    step = synth.prefix_sharing()
+    one_call_step_matches_oracle(step, shared_prefix=shared_prefix_of(step))
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(12, 3, 128), (8, 8, 64), (16, 2, 64)])
+def test_one_call_head_shapes_with_chunks(Hq, Hkv, D):
+    """Chunked prefills and decodes in one batch at group sizes 4, 1 and 8:
+    the prefill's query tile is 128 / G queries."""
+    specs = [RequestSpec(40, 70), RequestSpec(300, 1), RequestSpec(0, 33), RequestSpec(129, 1),
+             RequestSpec(17, 200)]
+    one_call_step_matches_oracle(make_step(specs, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                                           seed=Hq * 10 + D))
+
+
+def test_one_call_without_attention_still_writes():
+    """max_query_len 0 leaves the attention out; the slots and rows are
+    still mapped and written."""
+    step = synth.tiny_decode()
+    ds = DeviceStep(step)
+    ds.out.fill_(3.0)
+    s = step
+    binding.pkv_paged_attention_with_write(
+        ds.out, ds.q, ds.kv_cache, ds.k, ds.v, ds.block_table, ds.seq_lens, ds.query_start_loc,
+        ds.num_computed, max_query_len=0, max_seq_len=s.max_seq_len, scale=s.scale,
+        workspace=ds.workspace, slot_mapping=ds.slot_mapping)
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_errors(clear=True) == 0
+    slots, pool, _ = oracle_step(step, rows=[])
+    assert np.array_equal(ds.slots_host(), slots)
+    assert np.array_equal(ds.pool_host(), pool)
+    assert (ds.out_host() == 0x4040).all()  # untouched (3.0 in bf16)
+
+
+def test_one_call_bad_lengths_flagged_and_not_written():
+    specs = [RequestSpec(40, 3), RequestSpec(70, 5), RequestSpec(9, 1)]
+    step = make_step(specs, num_q_heads=8, num_kv_heads=2, head_dim=64, seed=12)
+    ds = DeviceStep(step)
+    before = ds.pool_host()
+    nc = ds.num_computed.clone()
+    nc[1] = -1  # request 1: rows 3..7
+    s = step
+    binding.pkv_paged_attention_with_write(
+        ds.out, ds.q, ds.kv_cache, ds.k, ds.v, ds.block_table, ds.seq_lens, ds.query_start_loc,
+        nc, max_query_len=s.max_query_len, max_seq_len=s.max_seq_len, scale=s.scale,
+        workspace=ds.workspace, slot_mapping=ds.slot_mapping)
+    assert binding.pkv_get_device_errors(clear=True) & binding.DEVERR_LENGTHS
+    slots = ds.slots_host()
+    ref = oracle_step(step, rows=[])[0]
+    assert (slots[3:8] == -1).all()
+    kept = ref.copy()
+    kept[3:8] = -1
+    assert np.array_equal(ds.pool_host(), oracle.kv_write(before, step.k, step.v, kept))
