@@ -1,22 +1,26 @@
-"""CPU restatement of the kernels' online-softmax update, merge and combine.
+"""CPU restatement of the kernels' online-softmax update and combine.
 
 The decode and prefill kernels keep a running max in base 2 and move it
 lazily: only when a new chunk (decode: 16 keys) or tile (prefill: 128 keys)
 beats it by more than 2^8 -- decided once per warp, for every head or row the
 warp holds -- are the running sum and the unnormalised output rescaled by
-alpha = 2^(m_old - m_new). A prefill item's key tiles alternate between two
-softmax warpgroups, whose partials are merged at the end (the even tiles'
-partial first); a decode request cut by split-KV ranges leaves one partial
-per range, merged by the combine kernel with weights 2^(m_p - M).
+alpha = 2^(m_old - m_new). In the prefill each query row is split between
+two threads of one warp (keys 0..63 and 64..127 of every tile, and the two
+halves of O's columns): the row max is taken over both halves, each half
+keeps its own running sum and both rescale with the same alpha; the row's
+sum is the two halves' sums added at the end. A warp holds 16 rows. A
+decode request cut by split-KV ranges leaves one partial per range, merged
+by the combine kernel with weights 2^(m_p - M).
 
 These tests restate those rules in numpy fp32 (the kernels' precision; the
 prefill's P rounded to bf16 before P.V as on the tensor cores) on the
 rescale-path inputs of ``rescale_cases`` -- the same inputs the GPU parity
 tests run -- and require the oracle's result within the attention tolerance.
 They also check that the inputs really drive each branch (rescales that keep
-weight on earlier keys, alphas and merge weights that underflow to zero), and
-that each plausible slip in the update (a wrong alpha, a missing rescale of
-the sum or of the output, a wrong merge weight) fails against the oracle.
+weight on earlier keys, alphas and combine weights that underflow to zero),
+and that each plausible slip in the update (a wrong alpha, a missing rescale
+of the sum or of (half of) the output, a half-row sum left out, a wrong
+combine weight) fails against the oracle.
 """
 
 import numpy as np
@@ -159,19 +163,24 @@ def decode_restated(step, r, rng, bug=None, st=None):
 
 
 # ---------------------------------------------------------------- prefill
-def prefill_partial(S_tiles, keep, scale_log2, bug=None, st=None):
-    """One softmax warpgroup's partial over its tiles. S_tiles: list of
-    [rows, 128] unscaled scores of its tiles, masked keys at -inf; keep:
-    [rows] rows that take part in the warp vote. Returns (m, l, O) with O
-    from bf16-rounded P; rows are grouped 32 to a warp."""
+def prefill_rows(S_tiles, keep, scale_log2, bug=None, st=None):
+    """The softmax warps over an item's tiles, in order. S_tiles: list of
+    ([rows, 128] unscaled scores, masked keys at -inf; [128, D] V); keep:
+    [rows] rows that take part in the warp vote. Each row's keys 0..63 and
+    64..127 (and O's first and second halves of columns) belong to two
+    threads; rows are grouped 16 to a warp. Returns the normalised output,
+    with P rounded to bf16 before P.V."""
     rows = S_tiles[0][0].shape[0]
+    D = S_tiles[0][1].shape[1]
     m = np.full(rows, -np.inf, F32)
-    lsum = np.zeros(rows, F32)
-    O = np.zeros((rows, S_tiles[0][1].shape[1]), F32)
-    for nmine, (S, Vt) in enumerate(S_tiles):
-        mx = (S.max(axis=1) * scale_log2).astype(F32)
+    lh = np.zeros((2, rows), F32)  # the two halves' running sums
+    O = np.zeros((rows, D), F32)
+    for kt, (S, Vt) in enumerate(S_tiles):
+        # each half's max, then the pair's (both threads get the same value)
+        mh = np.stack([S[:, :64].max(axis=1), S[:, 64:].max(axis=1)])
+        mx = (mh.max(axis=0) * scale_log2).astype(F32)
         vote = (mx > m + THRESH) & keep
-        need = vote.reshape(-1, 32).any(axis=1).repeat(32)
+        need = vote.reshape(-1, 16).any(axis=1).repeat(16)
         if need.any():
             m_new = np.where(need, np.maximum(m, mx), m)
             with np.errstate(invalid="ignore", over="ignore"):
@@ -180,20 +189,25 @@ def prefill_partial(S_tiles, keep, scale_log2, bug=None, st=None):
             if st is not None:
                 mid = need & np.isfinite(m) & keep
                 st.zero_alphas += int((mid & (alpha == 0)).sum())
-                old = alpha * lsum
+                old = alpha * (lh[0] + lh[1])
                 with np.errstate(over="ignore", invalid="ignore"):
                     new = np.exp2(S * scale_log2 - m_new[:, None]).sum(axis=1)
                 st.rescales_with_weight += int((mid & (old > 0.05 * (old + new))).sum())
-            lsum = lsum * alpha
-            if nmine > 0 and bug != "o_not_rescaled":
-                O = O * alpha[:, None]
+            lh = lh * alpha[None, :]
+            if kt > 0 and bug != "o_not_rescaled":
+                O[:, : D // 2] *= alpha[:, None]
+                if bug != "o_half_not_rescaled":
+                    O[:, D // 2:] *= alpha[:, None]
             m = m_new.astype(F32)
         msub = np.where(np.isfinite(m), m, F32(0))
         with np.errstate(over="ignore", invalid="ignore"):
             p = np.exp2((S * scale_log2).astype(F32) - msub[:, None]).astype(F32)
-        lsum = lsum + p.sum(axis=1, dtype=F32)
+        lh[0] += p[:, :64].sum(axis=1, dtype=F32)
+        lh[1] += p[:, 64:].sum(axis=1, dtype=F32)
         O = O + (bf16_round(p) @ Vt).astype(F32)
-    return m, lsum, O
+    l_row = lh[0] if bug == "l_half_missing" else lh[0] + lh[1]
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        return O / l_row[:, None]
 
 
 def prefill_restated(step, r, g, bug=None, st=None):
@@ -228,23 +242,7 @@ def prefill_restated(step, r, g, bug=None, st=None):
             Vt = np.zeros((TILE, D), F32)
             Vt[: k1 - k0] = V[k0:k1]
             tiles.append((S, Vt))
-        ma, la, Oa = prefill_partial(tiles[0::2], keep, scale_log2, bug, st)
-        if nkv == 1:
-            res = Oa / la[:, None]
-        else:
-            mb, lb, Ob = prefill_partial(tiles[1::2], keep, scale_log2, bug, st)
-            M = np.maximum(ma, mb)
-            with np.errstate(over="ignore", invalid="ignore"):
-                a0 = np.where(ma == -np.inf, F32(0), np.exp2(ma - M)).astype(F32)
-                a1 = np.where(mb == -np.inf, F32(0), np.exp2(mb - M)).astype(F32)
-            if bug == "merge_unweighted":
-                a0, a1 = np.ones_like(a0), np.ones_like(a1)
-            if bug == "merge_weights_swapped":
-                a0, a1 = a1, a0
-            if st is not None:
-                st.zero_weights += int((keep & (((a0 == 0) & (la > 0)) |
-                                                ((a1 == 0) & (lb > 0)))).sum())
-            res = (Oa * a0[:, None] + Ob * a1[:, None]) / (la * a0 + lb * a1)[:, None]
+        res = prefill_rows(tiles, keep, scale_log2, bug, st)
         res = res.reshape(QT, G, D)
         out[qi[valid]] = res[valid]
     return out
@@ -306,14 +304,14 @@ def test_decode_update_and_combine_match_the_oracle(name, D):
 
 @pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("name", PREFILL_CASES)
-def test_prefill_update_and_merge_match_the_oracle(name, D):
+def test_prefill_update_matches_the_oracle(name, D):
     assert run_prefill(name, D)
 
 
 def test_the_inputs_drive_every_branch():
     """The drift cases rescale partials that still hold weight; the steep
-    and spike cases make alphas, merge weights and combine weights underflow
-    to exactly zero."""
+    and spike cases make alphas and combine weights underflow to exactly
+    zero."""
     st = {n: Stats() for n in DECODE_CASES + PREFILL_CASES}
     for n in DECODE_CASES:
         run_decode(n, 128, st=st[n])
@@ -324,7 +322,7 @@ def test_the_inputs_drive_every_branch():
     assert st["decode_steep"].zero_weights > 0 and st["decode_spike"].zero_weights > 0
     assert st["decode_spike"].zero_alphas > 0 or st["decode_steep"].zero_alphas > 0
     assert st["prefill_drift"].rescales_with_weight > 100
-    assert st["prefill_steep"].zero_weights > 0
+    assert st["prefill_steep"].zero_alphas > 0
 
 
 @pytest.mark.parametrize("bug,cases", [
@@ -338,7 +336,7 @@ def test_planted_decode_slips_fail(bug, cases):
     assert not all(run_decode(n, 128, bug=bug) for n in cases)
 
 
-@pytest.mark.parametrize("bug", ["alpha_inverted", "o_not_rescaled", "merge_unweighted",
-                                 "merge_weights_swapped"])
+@pytest.mark.parametrize("bug", ["alpha_inverted", "o_not_rescaled", "o_half_not_rescaled",
+                                 "l_half_missing"])
 def test_planted_prefill_slips_fail(bug):
     assert not all(run_prefill(n, 128, bug=bug) for n in ("prefill_drift", "prefill_steep"))
