@@ -126,6 +126,73 @@ def test_slot_mapping_and_errors_reject_bad_arguments(lib):
     assert lib.pkv_get_device_errors(None, 0, None) == E("PKV_ERR_NULL_POINTER")
 
 
+def test_slot_mapping_and_write_rejects_bad_arguments(lib):
+    E = header_define
+
+    def SW(**kw):
+        a = dict(kv=FAKE, k=FAKE, v=FAKE, ks=0, vs=0, slots=FAKE, bt=FAKE, maxb=8, qsl=FAKE,
+                 nc=FAKE, R=2, T=4, lay=_layout())
+        a.update(kw)
+        return lib.pkv_slot_mapping_and_write(a["kv"], a["k"], a["v"], a["ks"], a["vs"],
+                                              a["slots"], a["bt"], a["maxb"], a["qsl"], a["nc"],
+                                              a["R"], a["T"], a["lay"], None)
+
+    assert SW(lay=_layout(bs=12)) == E("PKV_ERR_UNSUPPORTED")
+    assert SW(lay=_layout(bs=0)) == E("PKV_ERR_BAD_SHAPE")
+    assert SW(lay=_layout(d=96)) == E("PKV_ERR_UNSUPPORTED")
+    assert SW(lay=_layout(nb=0)) == E("PKV_ERR_BAD_SHAPE")
+    assert SW(T=-1) == E("PKV_ERR_BAD_SHAPE")
+    assert SW(R=-1) == E("PKV_ERR_BAD_SHAPE")
+    assert SW(maxb=-1) == E("PKV_ERR_BAD_SHAPE")
+    assert SW(ks=64) == E("PKV_ERR_BAD_SHAPE")       # row stride < Hkv * D = 128
+    assert SW(vs=130) == E("PKV_ERR_MISALIGNED")     # not a whole number of 16-byte words
+    assert SW(kv=None) == E("PKV_ERR_NULL_POINTER")
+    assert SW(qsl=None) == E("PKV_ERR_NULL_POINTER")
+    assert SW(bt=None) == E("PKV_ERR_NULL_POINTER")
+    assert SW(nc=None) == E("PKV_ERR_NULL_POINTER")
+    assert SW(k=MISALIGNED) == E("PKV_ERR_MISALIGNED")
+    assert SW(kv=MISALIGNED) == E("PKV_ERR_MISALIGNED")
+    # nothing to write: OK without touching the device
+    assert SW(kv=None, k=None, v=None, slots=None, bt=None, qsl=None, nc=None, T=0) == E("PKV_OK")
+
+
+def test_attention_with_write_rejects_bad_arguments(lib):
+    E = header_define
+
+    def AW(**kw):
+        a = dict(out=FAKE, q=FAKE, qs=0, kv=FAKE, k=FAKE, v=FAKE, ks=0, vs=0, slots=FAKE, bt=FAKE,
+                 maxb=8, sl=FAKE, qsl=FAKE, nc=FAKE, R=2, T=2, mq=1, ms=100, Hq=4, scale=0.125,
+                 lay=_layout(), ws=ctypes.c_void_p(0x10000), wsb=1 << 20, opt=None)
+        a.update(kw)
+        return lib.pkv_paged_attention_with_write(
+            a["out"], a["q"], a["qs"], a["kv"], a["k"], a["v"], a["ks"], a["vs"], a["slots"],
+            a["bt"], a["maxb"], a["sl"], a["qsl"], a["nc"], a["R"], a["T"], a["mq"], a["ms"],
+            a["Hq"], a["scale"], a["lay"], a["ws"], a["wsb"], a["opt"], None)
+
+    # the write's arguments
+    assert AW(lay=_layout(bs=12)) == E("PKV_ERR_UNSUPPORTED")
+    assert AW(T=-1) == E("PKV_ERR_BAD_SHAPE")
+    assert AW(ks=64) == E("PKV_ERR_BAD_SHAPE")
+    assert AW(ks=130) == E("PKV_ERR_MISALIGNED")
+    assert AW(k=None) == E("PKV_ERR_NULL_POINTER")
+    assert AW(v=MISALIGNED) == E("PKV_ERR_MISALIGNED")
+    assert AW(nc=None) == E("PKV_ERR_NULL_POINTER")
+    # then the attention's: nothing is launched when either part is bad
+    assert AW(Hq=3) == E("PKV_ERR_BAD_SHAPE")
+    assert AW(Hq=6) == E("PKV_ERR_UNSUPPORTED")
+    assert AW(scale=float("nan")) == E("PKV_ERR_BAD_SHAPE")
+    assert AW(ms=200) == E("PKV_ERR_BAD_SHAPE")
+    assert AW(qs=100) == E("PKV_ERR_BAD_SHAPE")
+    assert AW(sl=None) == E("PKV_ERR_NULL_POINTER")
+    assert AW(out=MISALIGNED) == E("PKV_ERR_MISALIGNED")
+    assert AW(ws=None) == E("PKV_ERR_WORKSPACE")
+    assert AW(ws=ctypes.c_void_p(0x10010)) == E("PKV_ERR_WORKSPACE")
+    # no tokens and no requests: OK without touching the device
+    none = dict(out=None, q=None, kv=None, k=None, v=None, slots=None, bt=None, sl=None, qsl=None,
+                nc=None, ws=None)
+    assert AW(R=0, T=0, **none) == E("PKV_OK")
+
+
 def test_copy_blocks_rejects_bad_arguments(lib):
     E = header_define
     C = lib.pkv_copy_blocks
