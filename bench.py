@@ -599,15 +599,25 @@ def timed_region(ds, run_step, K, stream, device_index, sync_all):
     for _ in range(NW):
         calls.write()
     w1.record(stream)
+    # the same rows through the slot mapping fused into the write (the per-token
+    # routine that the one-call step runs inside its first launch)
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run_step()
+    m0.record(stream)
+    for _ in range(NW):
+        calls.slot_map_and_write()
+    m1.record(stream)
     sync_all()
     write_b2b_ms = w0.elapsed_time(w1) / NW
+    mapped_b2b_ms = m0.elapsed_time(m1) / NW
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_stop)
     # ms per launch, the median over the traced steps: plan, prefill, decode, combine
     per_kernel = np.median(np.array([[ev[i].elapsed_time(ev[i + 1])
                                       for i in range(binding.PKV_TRACE_EVENTS - 1)]
                                      for ev in trace]), axis=0)
-    write_ms = (float(np.median([a.elapsed_time(b) for a, b in write_ev])), write_b2b_ms)
+    write_ms = (float(np.median([a.elapsed_time(b) for a, b in write_ev])), write_b2b_ms,
+                mapped_b2b_ms)
     return total_ms, per_kernel, write_ms, clocks
 
 
@@ -763,11 +773,15 @@ def run_native(args):
         "decode_kv_logical_gbs": (work["decode_kv_logical_bytes"] / (dec_ms * 1e-3) / 1e9
                                   if dec_ms > 0 else None),
         # cache write: each new token's K and V rows read and written
-        "kv_write": {"us": write_ms[0] * 1e3,
+        "kv_write": {"kernel": "kv_write_kernel (pkv_paged_kv_write, slots given)",
+                     "us": write_ms[0] * 1e3,
                      "gbs": work["write_bytes"] / (write_ms[0] * 1e-3) / 1e9 if write_ms[0] > 0 else None,
                      "us_back_to_back": write_ms[1] * 1e3,
                      "gbs_back_to_back": (work["write_bytes"] / (write_ms[1] * 1e-3) / 1e9
-                                          if write_ms[1] > 0 else None)},
+                                          if write_ms[1] > 0 else None),
+                     "mapped_us_back_to_back": write_ms[2] * 1e3,
+                     "mapped_gbs_back_to_back": (work["write_bytes"] / (write_ms[2] * 1e-3) / 1e9
+                                                 if write_ms[2] > 0 else None)},
         "kernel_ms": {"plan": per_kernel[0], "prefill": per_kernel[1],
                       "decode": per_kernel[2], "combine": per_kernel[3]},
         # a step of decodes only: the K/V bytes over every attention kernel
