@@ -31,9 +31,17 @@ def _clear_errors():
     yield
 
 
+WRITE_PATHS = {"separate": {}, "fused": {"fused_write": True},
+               "attention": {"write_in_attention": True}}
+
+
 def run_and_check(step, decode_splits=None, rows=None, check_pool=True, shared_prefix=None,
-                  expect_flags=0):
-    ds = DeviceStep(step, decode_splits=decode_splits, shared_prefix=shared_prefix)
+                  expect_flags=0, write="separate"):
+    """One step through the library -- slot mapping, write, attention made as
+    three calls (separate), as the fused write plus attention (fused), or as
+    the one call with the write inside (attention) -- against the oracle."""
+    ds = DeviceStep(step, decode_splits=decode_splits, shared_prefix=shared_prefix,
+                    **WRITE_PATHS[write])
     ds.run()
     torch.cuda.synchronize()
     assert binding.pkv_get_device_errors(clear=True) == expect_flags
@@ -599,12 +607,12 @@ FUZZ_SHAPES = [(4, 4, 64), (8, 4, 64), (16, 4, 64), (32, 4, 64), (8, 8, 128), (1
                (32, 8, 128), (64, 8, 128), (8, 2, 128), (4, 1, 128), (16, 2, 64), (12, 3, 128)]
 
 
-@pytest.mark.parametrize("trial", range(24))
+@pytest.mark.parametrize("trial", range(36))
 def test_seeded_fuzz(trial):
     """Random shapes, block sizes, request mixes (decodes, fresh prefills,
-    chunks over a cached prefix, empty requests) and split-KV CTA counts;
-    the slots, the whole pool and sampled rows are checked, and a second run
-    of the step must give the same bits."""
+    chunks over a cached prefix, empty requests), split-KV CTA counts and the
+    three ways to make a step's calls; the slots, the whole pool and sampled
+    rows are checked, and a second run of the step must give the same bits."""
     rng = np.random.default_rng(9000 + trial)
     Hq, Hkv, D = FUZZ_SHAPES[trial % len(FUZZ_SHAPES)]
     B = int(rng.choice([8, 16, 32]))
@@ -625,9 +633,10 @@ def test_seeded_fuzz(trial):
                      seed=trial)
     splits = None if trial % 3 == 0 else int(rng.integers(1, 3000))
     rows = rng.choice(step.num_tokens, size=min(step.num_tokens, 400), replace=False)
-    run_and_check(step, decode_splits=splits, rows=np.sort(rows))
+    write = ("separate", "fused", "attention")[(trial + trial // len(FUZZ_SHAPES)) % 3]  # each shape: all three
+    run_and_check(step, decode_splits=splits, rows=np.sort(rows), write=write)
     # the same step again gives the same bits, whatever the CTAs' schedule
-    ds = DeviceStep(step, decode_splits=splits)
+    ds = DeviceStep(step, decode_splits=splits, **WRITE_PATHS[write])
     outs = []
     for _ in range(2):
         ds.run()
