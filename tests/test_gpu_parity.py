@@ -643,3 +643,48 @@ def test_seeded_fuzz(trial):
         torch.cuda.synchronize()
         outs.append(ds.out.clone())
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+@pytest.mark.parametrize("trial", range(40))
+def test_wide_fuzz(trial):
+    """Wider random steps: up to ~90 requests with chunks of up to 1200 new
+    tokens over 4000 cached and decodes over up to 5000 keys; in two steps of
+    five, a run of decodes over one shared prefix (a multiple of 16 and of
+    B), attended with the shared-prefix hint in most of them; keys that
+    drift along the sequence or one key that dwarfs the others (the
+    online-softmax rescale paths); a random split-KV CTA count and one of the
+    three ways to make the step's calls. Slots, the whole pool and sampled
+    rows against the oracle."""
+    from paged_kv_cache_hkv_gb300.runner import shared_prefix_of
+    rng = np.random.default_rng(77000 + trial)
+    Hq, Hkv, D = FUZZ_SHAPES[int(rng.integers(0, len(FUZZ_SHAPES)))]
+    B = int(rng.choice([8, 16, 32]))
+    specs = []
+    for _ in range(int(rng.integers(1, 90))):
+        kind = rng.choice(["decode", "decode", "decode", "prefill", "chunk", "empty"])
+        if kind == "decode":
+            specs.append(RequestSpec(int(rng.integers(0, 5000)), 1))
+        elif kind == "prefill":
+            specs.append(RequestSpec(0, int(rng.integers(2, 700))))
+        elif kind == "chunk":
+            specs.append(RequestSpec(int(rng.integers(1, 4000)), int(rng.integers(2, 1200))))
+        else:
+            specs.append(RequestSpec(int(rng.integers(0, 500)), 0))
+    prefix = 0
+    if rng.random() < 0.4:
+        prefix = max(B, 16) * int(rng.integers(1, 48))
+        run = [RequestSpec(prefix + int(rng.integers(0, 600)), 1, shares_prefix=True)
+               for _ in range(int(rng.integers(2, 70)))]
+        at = int(rng.integers(0, len(specs) + 1))
+        specs = specs[:at] + run + specs[at:]
+    if all(s.query_len == 0 for s in specs):
+        specs.append(RequestSpec(10, 1))
+    drift = float(rng.choice([0.0, 0.0, 0.03, 0.08]))
+    spike = float(rng.choice([0.0, 0.0, 25.0]))
+    step = make_step(specs, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=B,
+                     seed=trial, prefix_tokens=prefix, key_drift=drift, spike=spike)
+    hint = shared_prefix_of(step) if rng.random() < 0.8 else None
+    splits = None if rng.random() < 0.5 else int(rng.integers(1, 4000))
+    write = ("separate", "fused", "attention")[int(rng.integers(0, 3))]
+    rows = np.sort(rng.choice(step.num_tokens, size=min(step.num_tokens, 250), replace=False))
+    run_and_check(step, decode_splits=splits, rows=rows, write=write, shared_prefix=hint)
