@@ -181,26 +181,54 @@ __global__ void __launch_bounds__(kDecodeThreads)
   uint64_t* full = reinterpret_cast<uint64_t*>(base + lay.bar_off);
   uint64_t* empty = full + S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the tensor map is a kernel parameter: its descriptor can be fetched
+  // before the previous kernel is done
+  if (warp == VH && lane == 0) prefetch_tensormap(&kv_map);
   // no early trigger here: a next kernel's CTAs, resident next to these for
   // the whole decode while they wait for it, slow the decode down
   pdl_wait();
 
   const long long Cn = p.splits, c = blockIdx.x;
   const int slab = blockIdx.y;
+  // the stream's length and this CTA's start record are independent loads
   const long long N = p.hdr[kHdrDecodeBlocks];
+  const int r_start = __ldg(p.bound + c);  // -1 when the step has no decode chunk
   const long long x0 = c * N / Cn, x1 = (c + 1) * N / Cn;
 
   // ---------------- locate position x0: (request r, chunk blk); the plan
   // recorded the request holding it (the combine kernel reads the same
   // records to find split requests)
-  int r = -1, blk = 0, nblk = 0;
+  int r = -1, blk = 0, nblk = 0, pr = 0;
   if (x0 < N) {
-    r = __ldg(p.bound + c);
-    const int pr = __ldg(p.dec_prefix + r);
+    r = r_start;
+    pr = __ldg(p.dec_prefix + r);  // stream position of the request's first chunk
     nblk = __ldg(p.dec_prefix + r + 1) - pr;
     blk = static_cast<int>(x0 - pr);
   }
   if (x0 >= x1) return;
+  constexpr int sh = SH;
+  // chunks of request rr before its first streamed one (its shared prefix)
+  auto chunk_off = [&](int rr) -> int {
+    const int i = rr - p.shared_first;
+    return (p.shared_num > 0 && i >= 0 && i < p.shared_num && __ldg(p.shared_use + i))
+               ? p.shared_chunks
+               : 0;
+  };
+  // table entry of absolute chunk a
+  auto entry_of = [&](int a) -> int { return (sh == 4) ? a : (sh == 5 ? a >> 1 : 2 * a); };
+  // the producer's first loads go out before the barrier: the first
+  // request's lengths and the 32 block-table entries from its first chunk on
+  int L = 0, t = 0, nent = 0, skip = 0, win_r = -1, win_base = 0, win_val = -1;
+  if (warp == VH) {
+    L = __ldg(p.seq_lens + r);
+    t = __ldg(p.qsl + r);
+    skip = chunk_off(r);  // chunk = blk + skip
+    nent = (L + (1 << sh) - 1) >> sh;  // table entries the request uses
+    win_r = r;
+    win_base = entry_of(blk + skip);
+    const int j = win_base + lane;
+    win_val = (j < nent) ? __ldg(p.block_table + static_cast<long long>(r) * p.max_blocks + j) : -1;
+  }
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -213,25 +241,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
   if (warp == VH) {
     // ================= producer warp: metadata, block-table lookups and the
     // copies of every chunk of the range, S stages ahead of the consumers
-    if (lane == 0) prefetch_tensormap(&kv_map);
-    constexpr int sh = SH;
     // K/V rows are read once per step: evict them from L2 first, so that the
     // split-KV partials, q rows and tables stay (mixed step: 827 -> 819 us)
     const uint64_t l2_policy = l2_evict_first_policy();
-    // chunks of request rr before its first streamed one (its shared prefix)
-    auto chunk_off = [&](int rr) -> int {
-      const int i = rr - p.shared_first;
-      return (p.shared_num > 0 && i >= 0 && i < p.shared_num && __ldg(p.shared_use + i))
-                 ? p.shared_chunks
-                 : 0;
-    };
-    // table entry of absolute chunk a
-    auto entry_of = [&](int a) -> int { return (sh == 4) ? a : (sh == 5 ? a >> 1 : 2 * a); };
-    int L = __ldg(p.seq_lens + r), t = __ldg(p.qsl + r);
-    int nent = (L + (1 << sh) - 1) >> sh;  // table entries the request uses
-    int pr = __ldg(p.dec_prefix + r);       // stream position of the request's first chunk
-    int off = chunk_off(r);                 // chunk = blk + off
-    int win_r = -1, win_base = 0, win_val = -1;
     // The next request's lengths and the 32 entries of its block table row
     // from its first streamed chunk on, loaded one request ahead: a request
     // boundary then waits on no load.
@@ -276,10 +288,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
         // attended elsewhere, leaves a partial for the combine kernel
         const long long a = pr;
         const long long cf = owner_cta(a, N, Cn), cl = owner_cta(a + nblk - 1, N, Cn);
-        out_base = (cf == cl && off == 0) ? -1 : static_cast<int>((r + c) * p.virt_heads);
+        out_base = (cf == cl && skip == 0) ? -1 : static_cast<int>((r + c) * p.virt_heads);
       }
       // table entries of chunk blk: e0, and e0 + 1 for 8-token blocks
-      const int ab = blk + off;  // the chunk's place in the request
+      const int ab = blk + skip;  // the chunk's place in the request
       const int e0 = entry_of(ab);
       const int e_hi = (sh == 3) ? e0 + 1 : e0;
       if (r != win_r || e0 < win_base || e_hi >= win_base + 32) {
@@ -353,10 +365,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
             nblk = nx_pn - pr;
             L = nx_L;
             t = nx_t;
-            off = nx_off;
+            skip = nx_off;
             nent = (L + (1 << sh) - 1) >> sh;
             win_r = r;
-            win_base = entry_of(off);
+            win_base = entry_of(skip);
             win_val = win_base + lane < nent ? nx_win : -1;
           } else {
             do {
@@ -365,7 +377,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
             } while (nblk == 0);
             L = __ldg(p.seq_lens + r);
             t = __ldg(p.qsl + r);
-            off = chunk_off(r);
+            skip = chunk_off(r);
             nent = (L + (1 << sh) - 1) >> sh;
           }
           prefetch_next();
