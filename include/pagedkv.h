@@ -31,11 +31,15 @@
  *   head_dim must be 64 or 128.
  *
  * Launches: every kernel is launched with programmatic stream serialization.
- * A kernel may start (set up barriers, allocate tensor memory) while the
- * previous kernel in the stream is still running, and it waits for that
- * kernel to complete -- and its writes to be visible -- before reading
- * anything. Work the caller queued earlier on the stream is therefore seen
- * as with plain stream order. The calls can be recorded into a CUDA graph.
+ * A kernel may start (set up barriers, allocate tensor memory, fetch the
+ * descriptors passed as its own parameters) while the previous kernel in the
+ * stream is still running, and it waits for that kernel to complete -- and
+ * its writes to be visible -- before reading any buffer. Work the caller
+ * queued earlier on the stream is therefore seen as with plain stream order.
+ * The write calls (pkv_slot_mapping, pkv_paged_kv_write,
+ * pkv_slot_mapping_and_write) and the attention calls that take the caller's
+ * workspace (pkv_paged_attention, pkv_paged_attention_with_write) can be
+ * recorded into a CUDA graph.
  */
 #ifndef PAGEDKV_H_
 #define PAGEDKV_H_
@@ -359,9 +363,8 @@ int32_t pkv_paged_attention_with_write(
  *   Llama-3-8B layer shape (32 q / 8 kv heads, d = 128) fits about 1860
  *   requests per call on a 152-SM GB300.
  * - First call per device: it looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make this first call
- *   before any stream capture. The address is kept for the life of the
- *   process: do not call this entry point again on a device after
+ *   (cudaGetSymbolAddress) with that device current. The address is kept
+ *   for the life of the process: do not call this entry point again on a device after
  *   cudaDeviceReset (or after its primary context was released and made
  *   anew), since the library's device memory may then sit elsewhere.
  * - Shared state: every call on a device uses the same array and leaves its
